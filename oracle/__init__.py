@@ -1,0 +1,173 @@
+"""fp64 CPU oracle for the block-quantized decode matvec (test infrastructure).
+
+Only the test suite, the package smoke check and the benchmark's CPU-baseline
+leg may import this package. It wraps oracle.c (built by oracle/build.py) with
+ctypes and numpy arrays; it shares nothing with the CUDA library.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        u8p, i8p, u16p = C.POINTER(C.c_uint8), C.POINTER(C.c_int8), C.POINTER(C.c_uint16)
+        f32p, f64p, i32p, i64p = (C.POINTER(C.c_float), C.POINTER(C.c_double),
+                                  C.POINTER(C.c_int32), C.POINTER(C.c_int64))
+        i64 = C.c_int64
+        for name, res, args in [
+            ("oracle_e2m1", C.c_double, [C.c_uint8]),
+            ("oracle_e4m3", C.c_double, [C.c_uint8]),
+            ("oracle_fp16", C.c_double, [C.c_uint16]),
+            ("oracle_bf16", C.c_double, [C.c_uint16]),
+            ("oracle_nvfp4_dequant_f64", None, [u8p, u8p, C.c_float, i64, i64, f64p]),
+            ("oracle_nvfp4_dequant_f32", None, [u8p, u8p, C.c_float, i64, i64, f32p]),
+            ("oracle_q8_0_dequant_f64", None, [i8p, u16p, i64, i64, f64p]),
+            ("oracle_q8_0_dequant_f32", None, [i8p, u16p, i64, i64, f32p]),
+            ("oracle_nvfp4_gemv", None, [u8p, u8p, C.c_float, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
+            ("oracle_nvfp4_gemv_f64x", None, [u8p, u8p, C.c_float, f64p, i64, i64, i64, f64p, f64p]),
+            ("oracle_q8_0_gemv", None, [i8p, u16p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
+            ("oracle_moe_route", None, [f32p, i64, i64, i64, i32p, f64p]),
+            ("oracle_moe_layer", None, [u8p, u8p, f32p, u8p, u8p, f32p, u16p, i32p, f64p,
+                                        i64, i64, i64, i64] + [f64p] * 8),
+        ]:
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(a, ctype):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(C.POINTER(ctype))
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- decoders
+def e2m1(code: int) -> float:
+    return lib().oracle_e2m1(code)
+
+
+def e4m3(b: int) -> float:
+    return lib().oracle_e4m3(b)
+
+
+def fp16(h: int) -> float:
+    return lib().oracle_fp16(h)
+
+
+def bf16(b: int) -> float:
+    return lib().oracle_bf16(b)
+
+
+# ---------------------------------------------------------------- dequant
+def nvfp4_dequant(codes, scales, ts, M, K, dtype=np.float64):
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
+    w = np.empty((M, K), dtype=dtype)
+    if dtype == np.float64:
+        lib().oracle_nvfp4_dequant_f64(_p(codes, C.c_uint8), _p(scales, C.c_uint8), ts, M, K, _p(w, C.c_double))
+    else:
+        lib().oracle_nvfp4_dequant_f32(_p(codes, C.c_uint8), _p(scales, C.c_uint8), ts, M, K, _p(w, C.c_float))
+    return w
+
+
+def q8_0_dequant(q, d, M, K, dtype=np.float64):
+    q, d = _c(q, np.int8), _c(d, np.uint16)
+    w = np.empty((M, K), dtype=dtype)
+    if dtype == np.float64:
+        lib().oracle_q8_0_dequant_f64(_p(q, C.c_int8), _p(d, C.c_uint16), M, K, _p(w, C.c_double))
+    else:
+        lib().oracle_q8_0_dequant_f32(_p(q, C.c_int8), _p(d, C.c_uint16), M, K, _p(w, C.c_float))
+    return w
+
+
+# ---------------------------------------------------------------- GEMV
+def nvfp4_gemv(codes, scales, ts, x, M, K, rows=None):
+    """(y, a) as fp64 arrays [N][len(rows) or M]; x is bf16 bits [N][K]."""
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
+    x = _c(x, np.uint16).reshape(-1, K)
+    N = x.shape[0]
+    r = None if rows is None else _c(rows, np.int64)
+    R = M if r is None else len(r)
+    y = np.empty((N, R)); a = np.empty((N, R))
+    lib().oracle_nvfp4_gemv(_p(codes, C.c_uint8), _p(scales, C.c_uint8), ts, _p(x, C.c_uint16),
+                            M, K, N, _p(r, C.c_int64), 0 if r is None else len(r),
+                            _p(y, C.c_double), _p(a, C.c_double))
+    return y, a
+
+
+def nvfp4_gemv_f64x(codes, scales, ts, x, M, K):
+    codes, scales = _c(codes, np.uint8), _c(scales, np.uint8)
+    x = _c(x, np.float64).reshape(-1, K)
+    N = x.shape[0]
+    y = np.empty((N, M)); a = np.empty((N, M))
+    lib().oracle_nvfp4_gemv_f64x(_p(codes, C.c_uint8), _p(scales, C.c_uint8), ts, _p(x, C.c_double),
+                                 M, K, N, _p(y, C.c_double), _p(a, C.c_double))
+    return y, a
+
+
+def q8_0_gemv(q, d, x, M, K, rows=None):
+    q, d = _c(q, np.int8), _c(d, np.uint16)
+    x = _c(x, np.uint16).reshape(-1, K)
+    N = x.shape[0]
+    r = None if rows is None else _c(rows, np.int64)
+    R = M if r is None else len(r)
+    y = np.empty((N, R)); a = np.empty((N, R))
+    lib().oracle_q8_0_gemv(_p(q, C.c_int8), _p(d, C.c_uint16), _p(x, C.c_uint16), M, K, N,
+                           _p(r, C.c_int64), 0 if r is None else len(r),
+                           _p(y, C.c_double), _p(a, C.c_double))
+    return y, a
+
+
+# ---------------------------------------------------------------- MoE
+def moe_route(logits, topk):
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    if not 0 < topk <= E:
+        raise ValueError("need 0 < topk <= E")
+    sel = np.empty((T, topk), dtype=np.int32)
+    w = np.empty((T, topk))
+    lib().oracle_moe_route(_p(logits, C.c_float), T, E, topk, _p(sel, C.c_int32), _p(w, C.c_double))
+    return sel, w
+
+
+def moe_layer(layer: dict, sel=None, weights=None, want_parts: bool = False):
+    """Routed MoE FFN of a layer dict (synthetic.moe_layer layout).
+
+    Returns y [T][H] (fp64) and, with want_parts, a dict of the stage values
+    g, u, h, ag, au [T][topk][I] and d, ad [T][topk][H].
+    """
+    T, H, I, topk = layer["T"], layer["H"], layer["I"], layer["topk"]
+    if sel is None:
+        sel, weights = moe_route(layer["logits"], topk)
+    sel = _c(sel, np.int32); weights = _c(weights, np.float64)
+    y = np.empty((T, H))
+    parts = {k: (np.empty((T, topk, I)) if want_parts else None) for k in ("g", "u", "h", "ag", "au")}
+    parts.update({k: (np.empty((T, topk, H)) if want_parts else None) for k in ("d", "ad")})
+    arr = [_c(layer[k], t) for k, t in (("gu_codes", np.uint8), ("gu_scales", np.uint8), ("gu_ts", np.float32),
+                                        ("dn_codes", np.uint8), ("dn_scales", np.uint8), ("dn_ts", np.float32),
+                                        ("x", np.uint16))]
+    lib().oracle_moe_layer(_p(arr[0], C.c_uint8), _p(arr[1], C.c_uint8), _p(arr[2], C.c_float),
+                           _p(arr[3], C.c_uint8), _p(arr[4], C.c_uint8), _p(arr[5], C.c_float),
+                           _p(arr[6], C.c_uint16), _p(sel, C.c_int32), _p(weights, C.c_double),
+                           T, H, I, topk, _p(y, C.c_double),
+                           *[_p(parts[k], C.c_double) for k in ("g", "u", "h", "ag", "au", "d", "ad")])
+    if want_parts:
+        return y, parts
+    return y

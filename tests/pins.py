@@ -1,0 +1,50 @@
+"""Independent decoders for pinning the oracle: published tables and library
+conversions only (numpy float16, torch float8_e4m3fn and bfloat16)."""
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def e2m1_table() -> np.ndarray:
+    vals = np.zeros(16)
+    with open(os.path.join(_HERE, "golden", "e2m1_table.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                c, v = line.split()
+                vals[int(c)] = float(v)
+    return vals
+
+
+def e4m3_lib(b: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(b, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def bf16_lib(b: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(b, dtype=np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def fp16_lib(h: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(h, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def nvfp4_codes_unpacked(codes: np.ndarray) -> np.ndarray:
+    """[M][K/2] bytes -> [M][K] nibbles, low nibble first (the storage rule)."""
+    lo = codes & 0x0F
+    hi = codes >> 4
+    return np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)
+
+
+def nvfp4_weight_lib(codes, scales, ts) -> np.ndarray:
+    """Real-valued NVFP4 weight (fp64) from library/table decoders."""
+    c = nvfp4_codes_unpacked(codes)
+    s = np.repeat(e4m3_lib(scales), 16, axis=1)
+    return e2m1_table()[c] * s * float(np.float32(ts))
+
+
+def q8_0_weight_lib(q, d) -> np.ndarray:
+    return q.astype(np.float64) * np.repeat(fp16_lib(d), 32, axis=1)
