@@ -1,0 +1,24 @@
+"""Block-quantized decode matvec for GB300 (sm_103a).
+
+y = W . x with NVFP4 or Q8_0 weights for N = 1..16 tokens, and a top-k routed
+MoE layer over NVFP4 experts, computed by the CUDA kernels of libbqd.so
+behind the C ABI in include/bqd.h. This package holds the ctypes binding
+(same names as the C ABI), the in-tree build and the seeded workload
+generator.
+"""
+from ._binding import (  # noqa: F401
+    BQD_PATH_AUTO,
+    BQD_PATH_CUDA_CORE,
+    BqdError,
+    bqd_moe_read_status,
+    lib,
+    moe_grouped_gemv,
+    moe_route_topk,
+    moe_workspace_bytes,
+    nvfp4_dequant,
+    nvfp4_gemv,
+    nvfp4_gemv_path,
+    q8_0_dequant,
+    q8_0_gemv,
+    version,
+)

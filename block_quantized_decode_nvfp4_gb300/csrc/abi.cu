@@ -1,0 +1,194 @@
+// abi.cu -- the extern "C" entry points declared in include/bqd.h: argument
+// validation (host only, before any CUDA call), the device architecture
+// check, and dispatch to the kernels' launchers.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "bqd.h"
+#include "gemv.h"
+
+namespace {
+
+constexpr int kMaxN = 16;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The current device must be compute capability 10.3 (sm_103a code only).
+bqd_status check_arch()
+{
+    static std::mutex mu;
+    static int state[64] = {0};  // 0 unknown, 1 ok, 2 wrong
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return BQD_ERR_ARCH;
+    }
+    if (dev >= 64) return BQD_ERR_ARCH;
+    std::lock_guard<std::mutex> g(mu);
+    if (state[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return BQD_ERR_ARCH;
+        }
+        state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return state[dev] == 1 ? BQD_OK : BQD_ERR_ARCH;
+}
+
+bqd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BQD_OK : BQD_ERR_LAUNCH; }
+
+bqd_status zero_output(float* y, int64_t count, cudaStream_t s)
+{
+    if (count == 0) return BQD_OK;
+    return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(count) * sizeof(float), s));
+}
+
+// Common shape rules of the dense GEMV / dequant calls.
+bqd_status check_dense(const void* a, const void* b, const void* x, const void* y, int64_t M, int64_t K, int N,
+                       int kdiv, bool has_x)
+{
+    if (M < 0 || K < 0 || K % kdiv != 0) return BQD_ERR_SHAPE;
+    if (has_x && (N < 1 || N > kMaxN)) return BQD_ERR_SHAPE;
+    if (M > 0 && K > 0 && M > (int64_t(1) << 62) / K) return BQD_ERR_SHAPE;
+    if (M == 0) return BQD_OK;
+    if (!y) return BQD_ERR_NULL;
+    if (!aligned16(y)) return BQD_ERR_ALIGN;
+    if (K == 0) return BQD_OK;
+    if (!a || !b || (has_x && !x)) return BQD_ERR_NULL;
+    if (!aligned16(a) || !aligned16(b) || (has_x && !aligned16(x))) return BQD_ERR_ALIGN;
+    return BQD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bqd_status_string(bqd_status s)
+{
+    switch (s) {
+        case BQD_OK: return "ok";
+        case BQD_ERR_NULL: return "a required pointer is NULL";
+        case BQD_ERR_SHAPE: return "a size is out of range or breaks a divisibility rule";
+        case BQD_ERR_ALIGN: return "a base pointer is not 16-byte aligned";
+        case BQD_ERR_ARCH: return "no current CUDA device, or it is not compute capability 10.3";
+        case BQD_ERR_LAUNCH: return "CUDA launch failed";
+        case BQD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case BQD_ERR_PATH: return "unknown compute path, or it does not support these arguments";
+        case BQD_ERR_DEVICE: return "device-side status bits set (malformed MoE list)";
+        default: return "unknown status";
+    }
+}
+
+int bqd_version(void) { return 100; }
+
+bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
+                           float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream)
+{
+    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE) return BQD_ERR_PATH;
+    bqd_status st = check_dense(codes, scales, x, y, M, K, N, 16, true);
+    if (st != BQD_OK || M == 0) return st;
+    if ((st = check_arch()) != BQD_OK) return st;
+    if (K == 0) return zero_output(y, M * N, stream);
+    return from_cuda(bqd::launch_nvfp4_gemv_cuda_core(codes, scales, tensor_scale, x, y, M, K, N, stream));
+}
+
+bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x, float* y,
+                      int64_t M, int64_t K, int N, cudaStream_t stream)
+{
+    return nvfp4_gemv_path(codes, scales, tensor_scale, x, y, M, K, N, BQD_PATH_AUTO, stream);
+}
+
+bqd_status q8_0_gemv(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K, int N,
+                     cudaStream_t stream)
+{
+    bqd_status st = check_dense(q, d, x, y, M, K, N, 32, true);
+    if (st != BQD_OK || M == 0) return st;
+    if ((st = check_arch()) != BQD_OK) return st;
+    if (K == 0) return zero_output(y, M * N, stream);
+    return from_cuda(bqd::launch_q8_0_gemv_cuda_core(q, d, x, y, M, K, N, stream));
+}
+
+bqd_status nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, float* w, int64_t M,
+                         int64_t K, cudaStream_t stream)
+{
+    bqd_status st = check_dense(codes, scales, nullptr, w, M, K, 1, 16, false);
+    if (st != BQD_OK || M == 0 || K == 0) return st;
+    if ((st = check_arch()) != BQD_OK) return st;
+    return from_cuda(bqd::launch_nvfp4_dequant(codes, scales, tensor_scale, w, M, K, stream));
+}
+
+bqd_status q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t stream)
+{
+    bqd_status st = check_dense(q, d, nullptr, w, M, K, 1, 32, false);
+    if (st != BQD_OK || M == 0 || K == 0) return st;
+    if ((st = check_arch()) != BQD_OK) return st;
+    return from_cuda(bqd::launch_q8_0_dequant(q, d, w, M, K, stream));
+}
+
+bqd_status moe_route_topk(const float* logits, int T, int E, int topk, int32_t* expert_offsets, int32_t* pair_token,
+                          float* pair_weight, int32_t* pair_slot, cudaStream_t stream)
+{
+    if (T < 1 || E < 1 || E > bqd::kMoeMaxExperts || topk < 1 || topk > E || topk > bqd::kMoeMaxTopk ||
+        static_cast<int64_t>(T) * topk > bqd::kMoeMaxPairs)
+        return BQD_ERR_SHAPE;
+    if (!logits || !expert_offsets || !pair_token || !pair_weight || !pair_slot) return BQD_ERR_NULL;
+    if (!aligned16(logits) || !aligned16(expert_offsets) || !aligned16(pair_token) || !aligned16(pair_weight) ||
+        !aligned16(pair_slot))
+        return BQD_ERR_ALIGN;
+    bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    return from_cuda(
+        bqd::launch_moe_route(logits, T, E, topk, expert_offsets, pair_token, pair_weight, pair_slot, stream));
+}
+
+size_t moe_workspace_bytes(int T, int topk, int H, int I)
+{
+    if (T < 1 || topk < 1 || H < 1 || I < 1) return 0;
+    return bqd::moe_workspace_size(T, topk, H, I);
+}
+
+bqd_status moe_grouped_gemv(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
+                            const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts, const uint16_t* x,
+                            const int32_t* expert_offsets, const int32_t* pair_token, const float* pair_weight,
+                            const int32_t* pair_slot, float* y, void* workspace, size_t workspace_bytes, int E,
+                            int H, int I, int T, int topk, cudaStream_t stream)
+{
+    if (T < 1 || E < 1 || E > bqd::kMoeMaxExperts || topk < 1 || topk > E || topk > bqd::kMoeMaxTopk ||
+        static_cast<int64_t>(T) * topk > bqd::kMoeMaxPairs || H < 32 || H > 8192 || H % 32 != 0 || I < 32 ||
+        I > 4096 || I % 32 != 0)
+        return BQD_ERR_SHAPE;
+    const void* ptrs[] = {gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts,
+                          x,        expert_offsets, pair_token, pair_weight, pair_slot, y};
+    for (const void* p : ptrs)
+        if (!p) return BQD_ERR_NULL;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return BQD_ERR_ALIGN;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < bqd::moe_workspace_size(T, topk, H, I))
+        return BQD_ERR_WORKSPACE;
+    bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    const bqd::MoeWorkspace ws = bqd::moe_workspace_carve(workspace, T, topk, H, I);
+    return from_cuda(bqd::launch_moe_grouped(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x,
+                                             expert_offsets, pair_token, pair_weight, pair_slot, y, ws, E, H, I, T,
+                                             topk, stream));
+}
+
+bqd_status bqd_moe_read_status(const void* workspace, int32_t* status_out, cudaStream_t stream)
+{
+    if (!workspace || !status_out) return BQD_ERR_NULL;
+    bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return BQD_ERR_LAUNCH;
+    *status_out = v;
+    return v ? BQD_ERR_DEVICE : BQD_OK;
+}
+
+}  // extern "C"

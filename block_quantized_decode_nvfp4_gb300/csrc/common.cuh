@@ -1,0 +1,416 @@
+// common.cuh -- device building blocks of the block-quantized decode matvec
+// (sm_103a): streaming weight loads, in-register element decode, per-chunk dot
+// products with fp32 accumulation, warp-shuffle reductions.
+//
+// What is computed follows the pages' decode path: NVFP4 weights (4-bit E2M1
+// elements, an E4M3 scale per 16 consecutive k, one FP32 tensor scale) and
+// Q8_0 weights (int8 with an fp16 scale per 32 k) multiplied into bf16
+// activations with fp32 accumulation ("robertbfuentes7-cloud/bw24" README,
+// NVFP4 (W4) decode path; "avifenesh/memra" README, Decode kernels;
+// "Vemloir/LumenLLM" README, Kernels: warp-shuffle GEMVs).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+namespace bqd {
+
+constexpr int kWarp = 32;
+
+// ------------------------------------------------------------------ loads
+// Weights are read exactly once per call: bypass L1 allocation so the
+// streamed bytes do not evict the activations staged next to them.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u16(const void* p)
+{
+    uint16_t r;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u8(const void* p)
+{
+    uint16_t r;
+    asm("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(r) : "l"(p));
+    return r & 0xFFu;
+}
+
+// ------------------------------------------------------------------ decode
+// Four bytes of packed E2M1 codes (8 elements, low nibble = lower k) to four
+// f16x2 pairs with the hardware FP4 -> f16x2 conversion (exact: every E2M1
+// value is an f16). Pair j holds elements 2j (low half) and 2j+1 (high half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+        "mov.b32 {q0, q1, q2, q3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, q2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, q3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
+// Two E4M3 bytes (low byte first) to f32 (exact: E4M3 values are f16 values).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_bytes)
+{
+    uint32_t h;
+    uint16_t b = static_cast<uint16_t>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(b));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte)
+{
+    return e4m3x2_to_float2(byte & 0xFFu).x;
+}
+
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h)
+{
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
+
+__device__ __forceinline__ float fp16_to_float(uint32_t bits)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+}
+
+// Four int8 (one 32-bit word) to fp32 without the int->float conversion
+// unit: flip the sign bit to get q + 128 in [1, 255], place it in the low
+// mantissa byte of 2^23 (the float 2^23 + q + 128), subtract 2^23 + 128.
+// Exact for every int8 value.
+__device__ __forceinline__ void s8x4_to_float(uint32_t w, float2& lo, float2& hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    const float2 bias = make_float2(8388736.0f, 8388736.0f);  // 2^23 + 128
+    float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)));
+    float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)));
+    lo = __fadd2_rn(a, make_float2(-bias.x, -bias.y));
+    hi = __fadd2_rn(b, make_float2(-bias.x, -bias.y));
+}
+
+// ------------------------------------------------------------------ formats
+// A "chunk" is the unit one lane loads and multiplies per row: a run of
+// consecutive k of one weight row, with its block scales.
+//
+//   Nvfp4Vec:    32 elements = 16 code bytes + 2 scale bytes (needs K % 32 == 0)
+//   Nvfp4Narrow: 16 elements =  8 code bytes + 1 scale byte
+//   Q8_0Fmt:     32 elements = 32 int8 + 1 fp16 scale
+//
+// dot<RPW, NC>() adds, for RPW rows (one chunk each, same k range) and NC
+// activation columns held in shared memory as fp32 (column n at
+// xs + n * xstride), the partial sums  sum_k w[r][k] * x[n][k]  with block
+// scales applied and the tensor scale not, into acc[r][n] (an even/odd pair
+// of fp32 partial sums; the row total is .x + .y). Each activation value is
+// read from shared memory once per chunk for all RPW rows.
+
+// E2M1 x E4M3 products have at most 6 significant bits and lie in
+// [2^-10, 2688], so scaling the decoded f16 elements by the f16 block scale
+// is exact.
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b)
+{
+    __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Two E4M3 bytes to f16x2 (bits), low byte in the low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
+{
+    uint32_t h;
+    uint16_t b = static_cast<uint16_t>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(b));
+    return h;
+}
+
+// One word of E2M1 codes (8 elements) of each row times NC columns.
+// With kScaled the block scale is already folded into the elements.
+template <int RPW, int NC>
+__device__ __forceinline__ void nvfp4_word(const uint32_t (&w)[RPW], const uint32_t (&s2)[RPW], const float* xs,
+                                           int xstride, int k, float2 (&acc)[RPW][NC])
+{
+    float2 wf[RPW][4];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        uint32_t h[4];
+        e2m1x8_to_f16x2(w[r], h);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) wf[r][q] = f16x2_to_float2(hmul2_bits(h[q], s2[r]));
+    }
+#pragma unroll
+    for (int n = 0; n < NC; ++n) {
+        const float4 xa = *reinterpret_cast<const float4*>(xs + n * xstride + k);
+        const float4 xb = *reinterpret_cast<const float4*>(xs + n * xstride + k + 4);
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            acc[r][n] = __ffma2_rn(wf[r][0], make_float2(xa.x, xa.y), acc[r][n]);
+            acc[r][n] = __ffma2_rn(wf[r][1], make_float2(xa.z, xa.w), acc[r][n]);
+            acc[r][n] = __ffma2_rn(wf[r][2], make_float2(xb.x, xb.y), acc[r][n]);
+            acc[r][n] = __ffma2_rn(wf[r][3], make_float2(xb.z, xb.w), acc[r][n]);
+        }
+    }
+}
+
+// One 16-element block of each row, one column, scale applied per block
+// (cheaper than scaling every element when there is a single column).
+template <int RPW>
+__device__ __forceinline__ void nvfp4_block_n1(const uint32_t (&w0)[RPW], const uint32_t (&w1)[RPW],
+                                               const float (&s)[RPW], const float* xs, int k,
+                                               float2 (&acc)[RPW][1])
+{
+    float2 part[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) part[r] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float4 xa = *reinterpret_cast<const float4*>(xs + k + 8 * j);
+        const float4 xb = *reinterpret_cast<const float4*>(xs + k + 8 * j + 4);
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            uint32_t h[4];
+            e2m1x8_to_f16x2(j ? w1[r] : w0[r], h);
+            part[r] = __ffma2_rn(f16x2_to_float2(h[0]), make_float2(xa.x, xa.y), part[r]);
+            part[r] = __ffma2_rn(f16x2_to_float2(h[1]), make_float2(xa.z, xa.w), part[r]);
+            part[r] = __ffma2_rn(f16x2_to_float2(h[2]), make_float2(xb.x, xb.y), part[r]);
+            part[r] = __ffma2_rn(f16x2_to_float2(h[3]), make_float2(xb.z, xb.w), part[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) acc[r][0].x = fmaf(s[r], part[r].x + part[r].y, acc[r][0].x);
+}
+
+struct Nvfp4Vec {
+    static constexpr int kElems = 32;
+    struct Chunk {
+        uint4 c;
+        uint32_t s;
+    };
+    __device__ static __forceinline__ Chunk load(const uint8_t* codes_row, const uint8_t* scales_row, int c)
+    {
+        Chunk ch;
+        ch.c = ld_stream_v4(codes_row + 16 * c);
+        ch.s = ld_stream_u16(scales_row + 2 * c);
+        return ch;
+    }
+    template <int RPW, int NC>
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride,
+                                               float2 (&acc)[RPW][NC])
+    {
+        if constexpr (NC == 1) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                uint32_t w0[RPW], w1[RPW];
+                float s[RPW];
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    const uint32_t words[4] = {ch[r].c.x, ch[r].c.y, ch[r].c.z, ch[r].c.w};
+                    w0[r] = words[2 * b];
+                    w1[r] = words[2 * b + 1];
+                    const float2 sc = e4m3x2_to_float2(ch[r].s);
+                    s[r] = b ? sc.y : sc.x;
+                }
+                nvfp4_block_n1<RPW>(w0, w1, s, xs, 16 * b, acc);
+            }
+        } else {
+            uint32_t sb[2][RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const uint32_t s2 = e4m3x2_to_f16x2(ch[r].s);
+                sb[0][r] = __byte_perm(s2, 0, 0x1010);  // block 0 scale in both halves
+                sb[1][r] = __byte_perm(s2, 0, 0x3232);  // block 1 scale in both halves
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t w[RPW];
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    const uint32_t words[4] = {ch[r].c.x, ch[r].c.y, ch[r].c.z, ch[r].c.w};
+                    w[r] = words[j];
+                }
+                nvfp4_word<RPW, NC>(w, sb[j / 2], xs, xstride, 8 * j, acc);
+            }
+        }
+    }
+};
+
+struct Nvfp4Narrow {
+    static constexpr int kElems = 16;
+    struct Chunk {
+        uint2 c;
+        uint32_t s;
+    };
+    __device__ static __forceinline__ Chunk load(const uint8_t* codes_row, const uint8_t* scales_row, int c)
+    {
+        Chunk ch;
+        ch.c = ld_stream_v2(codes_row + 8 * c);
+        ch.s = ld_stream_u8(scales_row + c);
+        return ch;
+    }
+    template <int RPW, int NC>
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride,
+                                               float2 (&acc)[RPW][NC])
+    {
+        uint32_t sb[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) sb[r] = __byte_perm(e4m3x2_to_f16x2(ch[r].s), 0, 0x1010);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            uint32_t w[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) w[r] = j ? ch[r].c.y : ch[r].c.x;
+            nvfp4_word<RPW, NC>(w, sb, xs, xstride, 8 * j, acc);
+        }
+    }
+};
+
+struct Q8_0Fmt {
+    static constexpr int kElems = 32;
+    struct Chunk {
+        uint4 a, b;
+        uint32_t d;
+    };
+    // For Q8_0 "codes_row" is the int8 row and "scales_row" the fp16 row.
+    __device__ static __forceinline__ Chunk load(const uint8_t* q_row, const uint8_t* d_row, int c)
+    {
+        Chunk ch;
+        ch.a = ld_stream_v4(q_row + 32 * c);
+        ch.b = ld_stream_v4(q_row + 32 * c + 16);
+        ch.d = ld_stream_u16(d_row + 2 * c);
+        return ch;
+    }
+    template <int RPW, int NC>
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride,
+                                               float2 (&acc)[RPW][NC])
+    {
+        float2 part[RPW][NC];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int n = 0; n < NC; ++n) part[r][n] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float2 lo[RPW], hi[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const uint32_t words[8] = {ch[r].a.x, ch[r].a.y, ch[r].a.z, ch[r].a.w,
+                                           ch[r].b.x, ch[r].b.y, ch[r].b.z, ch[r].b.w};
+                s8x4_to_float(words[j], lo[r], hi[r]);
+            }
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                const float4 xv = *reinterpret_cast<const float4*>(xs + n * xstride + 4 * j);
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    part[r][n] = __ffma2_rn(lo[r], make_float2(xv.x, xv.y), part[r][n]);
+                    part[r][n] = __ffma2_rn(hi[r], make_float2(xv.z, xv.w), part[r][n]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float d = fp16_to_float(ch[r].d);
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[r][n].x = fmaf(d, part[r][n].x + part[r][n].y, acc[r][n].x);
+        }
+    }
+};
+
+// Bytes of the codes plane and of the scales plane per weight row.
+template <class F>
+struct RowPitch;
+template <>
+struct RowPitch<Nvfp4Vec> {
+    __host__ __device__ static int64_t codes(int64_t K) { return K / 2; }
+    __host__ __device__ static int64_t scales(int64_t K) { return K / 16; }
+};
+template <>
+struct RowPitch<Nvfp4Narrow> {
+    __host__ __device__ static int64_t codes(int64_t K) { return K / 2; }
+    __host__ __device__ static int64_t scales(int64_t K) { return K / 16; }
+};
+template <>
+struct RowPitch<Q8_0Fmt> {
+    __host__ __device__ static int64_t codes(int64_t K) { return K; }
+    __host__ __device__ static int64_t scales(int64_t K) { return (K / 32) * 2; }
+};
+
+// ------------------------------------------------------------------ rows
+// Dot products of RPW weight rows with NC activation columns over chunks
+// [c_begin, c_end) of the rows, spread over a group of LG lanes (lane g of
+// the group takes chunks c_begin + g, c_begin + g + LG, ...). Every row
+// pointer must address a valid row (callers repeat a valid row for the
+// unused slots of a partial group). The next chunk of every row is loaded
+// before the current one is multiplied, so each lane keeps 2 * RPW chunks in
+// flight. xs points at the activation of chunk c_begin. acc[r][n] receives
+// this lane's partial sums (not yet reduced).
+template <class F, int RPW, int NC, int LG = kWarp>
+__device__ __forceinline__ void dot_rows(const uint8_t* const (&codes_row)[RPW],
+                                         const uint8_t* const (&scales_row)[RPW], int c_begin, int c_end,
+                                         const float* xs, int xstride, int g, float2 (&acc)[RPW][NC])
+{
+    using Chunk = typename F::Chunk;
+    int c = c_begin + g;
+    if (c >= c_end) return;
+    Chunk cur[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) cur[r] = F::load(codes_row[r], scales_row[r], c);
+    for (;;) {
+        const int cn = c + LG;
+        const bool more = cn < c_end;
+        Chunk nxt[RPW];
+        if (more) {
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) nxt[r] = F::load(codes_row[r], scales_row[r], cn);
+        }
+        F::template dot<RPW, NC>(cur, xs + (c - c_begin) * F::kElems, xstride, acc);
+        if (!more) break;
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) cur[r] = nxt[r];
+        c = cn;
+    }
+}
+
+// Sum over aligned groups of LG lanes (every lane of the group gets the sum).
+template <int LG = kWarp>
+__device__ __forceinline__ float group_sum(float v)
+{
+#pragma unroll
+    for (int o = LG / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) { return group_sum<kWarp>(v); }
+
+// Stage NC bf16 activation columns x[n][k0 .. k0+len) (row pitch K) into
+// shared memory as fp32, column n at xs + n * len. len and k0 are even.
+__device__ __forceinline__ void stage_x_bf16(const uint16_t* x, int64_t K, int ncols, int k0, int len, float* xs)
+{
+    const int pairs = len / 2;
+    for (int i = threadIdx.x; i < ncols * pairs; i += blockDim.x) {
+        const int n = i / pairs, p = i - n * pairs;
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(x + n * K + k0 + 2 * p);
+        xs[n * len + 2 * p] = bf16_lo(v);
+        xs[n * len + 2 * p + 1] = bf16_hi(v);
+    }
+}
+
+}  // namespace bqd

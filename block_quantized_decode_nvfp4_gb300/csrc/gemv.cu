@@ -1,0 +1,237 @@
+// gemv.cu -- CUDA-core block-quantized GEMV for sm_103a, N = 1..16 columns,
+// plus the exact dequantisation kernels used to check the decode bit by bit.
+//
+// Y[n][m] = ts * sum_b scale[m][b] * sum_{k in block b} elem[m][k] * X[n][k]
+// for NVFP4 (E2M1 elements, E4M3 scale per 16 k, FP32 tensor scale ts), and
+// Y[n][m] = sum_b d[m][b] * sum_{k in block b} q[m][k] * X[n][k] for Q8_0
+// (int8 elements, fp16 scale per 32 k). X is bf16 [N][K], Y fp32 [N][M].
+// ("robertbfuentes7-cloud/bw24" README, NVFP4 (W4) decode path and
+// speculative verify of K+1 tokens; "avifenesh/memra" README, Decode kernels.)
+//
+// Design: every weight byte is read once from HBM with 16-byte streaming
+// loads; the activations are staged once per CTA in shared memory as fp32;
+// elements are decoded in registers (E2M1 -> f16x2 by the hardware convert,
+// int8 -> fp32 by a byte-permute trick); products accumulate in fp32 with
+// packed f32x2 FMAs; each warp reduces its rows with xor shuffles. Rows are
+// split evenly over a grid sized to fill every SM once.
+#include "gemv.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "host_util.h"
+
+namespace bqd {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / kWarp;
+// Shared memory for the fp32 activations of one segment of K.
+constexpr int kXsBudgetBytes = 96 * 1024;
+
+template <int NC>
+struct Rpw {
+    static constexpr int value = NC <= 4 ? 4 : 2;
+};
+
+// One launch computes NC columns. When NC * K fp32 activations fit in
+// shared memory (seg_len == K) every warp owns a contiguous, balanced range
+// of rows and never synchronises. Otherwise K is processed in segments of
+// seg_len elements: the CTA owns a balanced row range, walks it in batches of
+// kWarps * RPW rows and restages the activations for each segment.
+template <class F, int RPW, int NC>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const uint8_t* __restrict__ codes,
+                                                        const uint8_t* __restrict__ scales, float ts,
+                                                        const uint16_t* __restrict__ x, float* __restrict__ y,
+                                                        int64_t M, int64_t K, int seg_len)
+{
+    extern __shared__ __align__(16) float xs[];
+    const int lane = threadIdx.x % kWarp;
+    const int warp = threadIdx.x / kWarp;
+    const int64_t cpitch = RowPitch<F>::codes(K);
+    const int64_t spitch = RowPitch<F>::scales(K);
+    const int chunks = static_cast<int>(K / F::kElems);
+
+    if (seg_len == K) {
+        stage_x_bf16(x, K, NC, 0, static_cast<int>(K), xs);
+        __syncthreads();
+        const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+        const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+        const int64_t r_lo = M * gw / nw, r_hi = M * (gw + 1) / nw;
+        for (int64_t r0 = r_lo; r0 < r_hi; r0 += RPW) {
+            const int nrows = static_cast<int>(r_hi - r0 < RPW ? r_hi - r0 : RPW);
+            const uint8_t* crow[RPW];
+            const uint8_t* srow[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const int64_t m = r0 + (r < nrows ? r : 0);
+                crow[r] = codes + m * cpitch;
+                srow[r] = scales + m * spitch;
+            }
+            float2 acc[RPW][NC];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+#pragma unroll
+                for (int n = 0; n < NC; ++n) acc[r][n] = make_float2(0.f, 0.f);
+            dot_rows<F, RPW, NC>(crow, srow, 0, chunks, xs, static_cast<int>(K), lane, acc);
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+#pragma unroll
+                for (int n = 0; n < NC; ++n) {
+                    const float v = warp_sum(acc[r][n].x + acc[r][n].y);
+                    if (lane == 0 && r < nrows) y[n * M + r0 + r] = v * ts;
+                }
+        }
+        return;
+    }
+
+    // Segmented K.
+    const int64_t b_lo = M * blockIdx.x / gridDim.x, b_hi = M * (blockIdx.x + 1) / gridDim.x;
+    const int seg_chunks = seg_len / F::kElems;
+    for (int64_t batch = b_lo; batch < b_hi; batch += static_cast<int64_t>(kWarps) * RPW) {
+        const int64_t r0 = batch + static_cast<int64_t>(warp) * RPW;
+        const int64_t left = b_hi - r0;
+        const int nrows = left <= 0 ? 0 : static_cast<int>(left < RPW ? left : RPW);
+        const uint8_t* crow[RPW];
+        const uint8_t* srow[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const int64_t m = nrows > 0 ? r0 + (r < nrows ? r : 0) : 0;
+            crow[r] = codes + m * cpitch;
+            srow[r] = scales + m * spitch;
+        }
+        float2 acc[RPW][NC];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[r][n] = make_float2(0.f, 0.f);
+        for (int c0 = 0; c0 < chunks; c0 += seg_chunks) {
+            const int c1 = c0 + seg_chunks < chunks ? c0 + seg_chunks : chunks;
+            const int len = (c1 - c0) * F::kElems;
+            __syncthreads();
+            stage_x_bf16(x, K, NC, c0 * F::kElems, len, xs);
+            __syncthreads();
+            if (nrows > 0) dot_rows<F, RPW, NC>(crow, srow, c0, c1, xs, len, lane, acc);
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                const float v = warp_sum(acc[r][n].x + acc[r][n].y);
+                if (lane == 0 && r < nrows) y[n * M + r0 + r] = v * ts;
+            }
+    }
+}
+
+// ------------------------------------------------------------------ dequant
+// w[m][k] = e2m1 * e4m3 * ts in fp32: e2m1 * e4m3 is exact in fp32, the
+// multiply by ts rounds once to nearest.
+__global__ void nvfp4_dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                     float ts, float* __restrict__ w, int64_t M, int64_t K)
+{
+    const int64_t nbytes = M * (K / 2);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nbytes;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / (K / 2), kk = 2 * (i - m * (K / 2));
+        const float s = e4m3_to_float(scales[m * (K / 16) + kk / 16]);
+        uint32_t h[4];
+        e2m1x8_to_f16x2(codes[i], h);  // only the first byte is used
+        const float2 v = f16x2_to_float2(h[0]);
+        w[m * K + kk] = (v.x * s) * ts;
+        w[m * K + kk + 1] = (v.y * s) * ts;
+    }
+}
+
+// w[m][k] = fp16(d) * q in fp32 (exact).
+__global__ void q8_0_dequant_kernel(const int8_t* __restrict__ q, const uint16_t* __restrict__ d,
+                                    float* __restrict__ w, int64_t M, int64_t K)
+{
+    const int64_t n = M * K;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / K, k = i - m * K;
+        w[i] = fp16_to_float(d[m * (K / 32) + k / 32]) * static_cast<float>(q[i]);
+    }
+}
+
+// ------------------------------------------------------------------ host
+template <class F, int NC>
+cudaError_t launch_nc(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
+                      int64_t M, int64_t K, cudaStream_t stream)
+{
+    constexpr int RPW = Rpw<NC>::value;
+    auto kern = gemv_kernel<F, RPW, NC>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const DevInfo di = dev_info(dev);
+    const int64_t budget = kXsBudgetBytes / 4 / NC;  // fp32 elements per column
+    int seg = static_cast<int>(K);
+    if (K > budget) seg = static_cast<int>(budget / F::kElems) * F::kElems;
+    const size_t smem = static_cast<size_t>(NC) * seg * sizeof(float);
+    static OccCache occ;
+    const int bps = blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, kThreads, smem);
+    int64_t grid = static_cast<int64_t>(di.sms) * bps;
+    const int64_t need = (seg == K) ? (M + kWarps - 1) / kWarps : (M + kWarps * RPW - 1) / (kWarps * RPW);
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(codes, scales, ts, x, y, M, K, seg);
+    return cudaGetLastError();
+}
+
+template <class F>
+cudaError_t launch_gemv(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
+                        int64_t M, int64_t K, int N, cudaStream_t s)
+{
+    switch (N) {
+#define BQD_CASE(n) \
+    case n: return launch_nc<F, n>(codes, scales, ts, x, y, M, K, s);
+        BQD_CASE(1) BQD_CASE(2) BQD_CASE(3) BQD_CASE(4) BQD_CASE(5) BQD_CASE(6) BQD_CASE(7) BQD_CASE(8)
+        BQD_CASE(9) BQD_CASE(10) BQD_CASE(11) BQD_CASE(12) BQD_CASE(13) BQD_CASE(14) BQD_CASE(15) BQD_CASE(16)
+#undef BQD_CASE
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_nvfp4_gemv_cuda_core(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                        float* y, int64_t M, int64_t K, int N, cudaStream_t s)
+{
+    if (K % 32 == 0) return launch_gemv<Nvfp4Vec>(codes, scales, ts, x, y, M, K, N, s);
+    return launch_gemv<Nvfp4Narrow>(codes, scales, ts, x, y, M, K, N, s);
+}
+
+cudaError_t launch_q8_0_gemv_cuda_core(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
+                                       int64_t K, int N, cudaStream_t s)
+{
+    return launch_gemv<Q8_0Fmt>(reinterpret_cast<const uint8_t*>(q), reinterpret_cast<const uint8_t*>(d), 1.0f, x,
+                                y, M, K, N, s);
+}
+
+static unsigned dequant_grid(int64_t work)
+{
+    int64_t g = (work + 255) / 256;
+    if (g > 152 * 16) g = 152 * 16;
+    if (g < 1) g = 1;
+    return static_cast<unsigned>(g);
+}
+
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float ts, float* w, int64_t M,
+                                 int64_t K, cudaStream_t s)
+{
+    nvfp4_dequant_kernel<<<dequant_grid(M * K / 2), 256, 0, s>>>(codes, scales, ts, w, M, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t s)
+{
+    q8_0_dequant_kernel<<<dequant_grid(M * K), 256, 0, s>>>(q, d, w, M, K);
+    return cudaGetLastError();
+}
+
+}  // namespace bqd

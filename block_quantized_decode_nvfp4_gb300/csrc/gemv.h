@@ -1,0 +1,46 @@
+// gemv.h -- internal launchers behind the C ABI (not part of the public API).
+// Each enqueues work on `s` and returns the launch status; none allocates,
+// synchronises or validates arguments (the C ABI layer does that first).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace bqd {
+
+cudaError_t launch_nvfp4_gemv_cuda_core(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                        float* y, int64_t M, int64_t K, int N, cudaStream_t s);
+cudaError_t launch_q8_0_gemv_cuda_core(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
+                                       int64_t K, int N, cudaStream_t s);
+cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float ts, float* w, int64_t M,
+                                 int64_t K, cudaStream_t s);
+cudaError_t launch_q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t s);
+
+// MoE (moe.cu). Limits checked by the ABI layer: E <= 1024, topk <= 32,
+// T * topk <= 8192.
+constexpr int kMoeMaxExperts = 1024;
+constexpr int kMoeMaxTopk = 32;
+constexpr int kMoeMaxPairs = 8192;
+
+cudaError_t launch_moe_route(const float* logits, int T, int E, int topk, int32_t* offsets, int32_t* pair_token,
+                             float* pair_weight, int32_t* pair_slot, cudaStream_t s);
+
+struct MoeWorkspace {
+    int32_t* status;  // device error bits (see bqd.h)
+    int32_t* count;   // [T*topk] times each (token, slot) was produced
+    float* wts;       // [T*topk] routing weight of (token, slot)
+    float* h;         // [T*topk][I] SiLU(gate) * up, pair (expert-major) order
+    float* part;      // [T*topk][H] down projection of (token, slot)
+};
+size_t moe_workspace_size(int T, int topk, int H, int I);
+MoeWorkspace moe_workspace_carve(void* base, int T, int topk, int H, int I);
+
+cudaError_t launch_moe_grouped(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
+                               const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts,
+                               const uint16_t* x, const int32_t* offsets, const int32_t* pair_token,
+                               const float* pair_weight, const int32_t* pair_slot, float* y,
+                               const MoeWorkspace& ws, int E, int H, int I, int T, int topk, cudaStream_t s);
+
+}  // namespace bqd

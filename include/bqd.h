@@ -1,0 +1,185 @@
+/*
+ * bqd.h -- C ABI of libbqd.so, the GB300 (sm_103a) block-quantized decode
+ * matvec library: y = W . x with NVFP4 or Q8_0 weights, for N = 1 token
+ * (plain decode) up to N = 16 (speculative verify), and a top-k routed MoE
+ * layer whose experts are NVFP4.
+ *
+ * Sources (what each call computes):
+ *  - "Vemloir/LumenLLM" README, Quantization and Kernels bullets: weights in
+ *    NVFP4, a block-scaled 4-bit floating-point format; decode runs GEMVs
+ *    reduced with warp shuffles.
+ *  - "robertbfuentes7-cloud/bw24" README, feature list: the NVFP4 (W4) decode
+ *    path is a block-scaled FP4 matvec; speculative decoding verifies K+1
+ *    draft tokens in one batched target forward (a matvec with N = K+1
+ *    columns); MoE batches routed tokens expert-major and decodes each
+ *    selected expert's weights once.
+ *  - "avifenesh/memra" README, Decode kernels bullet: NVFP4 and Q8_0 matvecs.
+ * The pages do not print the formats' bit layouts. Elements follow the
+ * public closed forms (E2M1 per OCP MX v1.0, E4M3 per OCP OFP8 v1.0, fp16
+ * per IEEE 754 binary16, bf16 = upper half of binary32); the block structure
+ * is the workload's: NVFP4 has one E4M3 scale per 16 consecutive k of a row
+ * plus one FP32 tensor scale, two E2M1 codes per byte with the low nibble
+ * holding the lower k; Q8_0 has one fp16 scale per 32 consecutive k.
+ *
+ * Conventions for every call:
+ *  - All array pointers are DEVICE pointers owned by the caller. The library
+ *    never allocates, frees or prints, and never synchronises except in
+ *    bqd_moe_read_status. Work is enqueued on `stream` (0 = legacy default
+ *    stream) in stream order; calls return before the GPU finishes.
+ *  - Arrays are dense, row-major, innermost index contiguous, and every base
+ *    pointer must be 16-byte aligned.
+ *  - Activations are bf16 bit patterns, token-major: x[n][k], row pitch K.
+ *    Outputs are fp32, token-major: y[n][m], row pitch M.
+ *  - Argument errors are detected on the host before any CUDA call and
+ *    return BQD_ERR_NULL / BQD_ERR_SHAPE / BQD_ERR_ALIGN / BQD_ERR_WORKSPACE
+ *    / BQD_ERR_PATH without enqueueing anything. BQD_ERR_ARCH means the
+ *    current device is not compute capability 10.3. BQD_ERR_LAUNCH reports a
+ *    CUDA error from the launch itself (cudaGetLastError).
+ *  - Results are deterministic: the same inputs give bit-identical outputs.
+ *  - Accuracy: fp32 accumulation; |y - y_exact| <= 1e-3 * sum_k |w x| + 1e-6
+ *    per output, where y_exact is the real-valued definition. Dequantised
+ *    weights are bit-exact.
+ */
+#ifndef BQD_H
+#define BQD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int bqd_status;
+
+enum {
+    BQD_OK = 0,
+    BQD_ERR_NULL = 1,      /* a required pointer is NULL */
+    BQD_ERR_SHAPE = 2,     /* a size is out of range or breaks a divisibility rule */
+    BQD_ERR_ALIGN = 3,     /* a base pointer is not 16-byte aligned */
+    BQD_ERR_ARCH = 4,      /* no current CUDA device, or it is not sm_103 */
+    BQD_ERR_LAUNCH = 5,    /* the CUDA launch failed */
+    BQD_ERR_WORKSPACE = 6, /* MoE workspace missing or smaller than moe_workspace_bytes() */
+    BQD_ERR_PATH = 7,      /* unknown path, or the path does not support these arguments */
+    BQD_ERR_DEVICE = 8     /* bqd_moe_read_status found device-side error bits */
+};
+
+/* Compute paths of the NVFP4 GEMV (nvfp4_gemv_path). */
+enum {
+    BQD_PATH_AUTO = 0,      /* the library's choice for the shape (what nvfp4_gemv uses) */
+    BQD_PATH_CUDA_CORE = 1  /* in-register decode + fp32 FMA on the CUDA cores */
+};
+
+/* Device-side status bits written by moe_grouped_gemv into its workspace. */
+enum {
+    BQD_MOE_BAD_OFFSETS = 1, /* expert_offsets is not a CSR of T*topk pairs */
+    BQD_MOE_BAD_PAIR = 2,    /* a pair_token or pair_slot is out of range */
+    BQD_MOE_COVERAGE = 4     /* some (token, slot) appears zero or several times */
+};
+
+/* Text of a status code (static storage; never NULL). */
+const char* bqd_status_string(bqd_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int bqd_version(void);
+
+/*
+ * nvfp4_gemv -- y[n][m] = ts * sum_k e2m1(c[m][k]) * e4m3(s[m][k/16]) * x[n][k]
+ * ("robertbfuentes7-cloud/bw24" README, NVFP4 (W4) decode path; the N > 1
+ * case is the speculative verify of K+1 tokens).
+ *   codes   u8 [M][K/2]: two E2M1 codes per byte, low nibble = even k.
+ *   scales  u8 [M][K/16]: E4M3 block scales (signed; NaN codes give NaN).
+ *   tensor_scale: the FP32 tensor scale ts.
+ *   x       bf16 bits [N][K];   y  fp32 [N][M] (written, never read).
+ *   M >= 0, K >= 0 with K % 16 == 0, 1 <= N <= 16, M * K < 2^62.
+ *   M == 0: returns BQD_OK without touching the GPU (pointers may be NULL).
+ *   K == 0: y is set to zero (codes, scales and x may be NULL).
+ */
+bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x, float* y,
+                      int64_t M, int64_t K, int N, cudaStream_t stream);
+
+/* nvfp4_gemv with an explicit compute path (BQD_PATH_*), to compare paths. */
+bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
+                           float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream);
+
+/*
+ * q8_0_gemv -- y[n][m] = sum_k fp16(d[m][k/32]) * q[m][k] * x[n][k]
+ * ("avifenesh/memra" README, Decode kernels bullet: Q8_0 matvec).
+ *   q  int8 [M][K] (any value, -128 included);  d  fp16 bits [M][K/32].
+ *   The planes are separate (planar), not GGUF's interleaved 34-byte blocks.
+ *   x bf16 bits [N][K]; y fp32 [N][M]. K % 32 == 0, 1 <= N <= 16; M == 0 and
+ *   K == 0 behave as in nvfp4_gemv.
+ */
+bqd_status q8_0_gemv(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K, int N,
+                     cudaStream_t stream);
+
+/*
+ * nvfp4_dequant -- w[m][k] = fl32(e2m1(c[m][k]) * e4m3(s[m][k/16]) * ts),
+ * the dequantised weight rounded once to fp32 (bit-exact). Uses the same
+ * device decoders as the GEMV. w fp32 [M][K]. Shape rules as nvfp4_gemv.
+ */
+bqd_status nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, float* w, int64_t M,
+                         int64_t K, cudaStream_t stream);
+
+/* q8_0_dequant -- w[m][k] = fp16(d[m][k/32]) * q[m][k] (exact in fp32). */
+bqd_status q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t stream);
+
+/*
+ * moe_route_topk -- router and expert-major list of a top-k routed MoE layer
+ * ("robertbfuentes7-cloud/bw24" README, MoE bullet: expert-major batching).
+ *   logits fp32 [T][E]. For each token: softmax over the E logits, keep the
+ *   topk largest (equal logits: lower expert index first), renormalise the
+ *   kept probabilities to sum to 1. Slot s of a token is its s-th largest.
+ *   Outputs, P = T * topk pairs grouped by expert (a CSR):
+ *     expert_offsets int32 [E+1]: expert e owns pairs [off[e], off[e+1]).
+ *     pair_token  int32 [P], pair_slot int32 [P], pair_weight fp32 [P];
+ *     inside an expert's segment tokens are in increasing order.
+ *   1 <= T, 1 <= topk <= min(E, 32), E <= 1024, T * topk <= 8192.
+ *   NaN logits are outside the contract (they are selected last).
+ */
+bqd_status moe_route_topk(const float* logits, int T, int E, int topk, int32_t* expert_offsets, int32_t* pair_token,
+                          float* pair_weight, int32_t* pair_slot, cudaStream_t stream);
+
+/* Bytes of device workspace moe_grouped_gemv needs for these sizes. */
+size_t moe_workspace_bytes(int T, int topk, int H, int I);
+
+/*
+ * moe_grouped_gemv -- one routed MoE FFN layer over T tokens, given the
+ * expert-major list (from moe_route_topk or the caller):
+ *   g = W_gu[e][0:I] . x_t,  u = W_gu[e][I:2I] . x_t,  h = SiLU(g) * u,
+ *   y_t = sum_{s = 0..topk-1, in order} w_{t,s} * (W_dn[e_{t,s}] . h)
+ * Each active expert's weights are streamed once for all of its tokens.
+ *   gu_codes u8 [E][2I][H/2], gu_scales u8 [E][2I][H/16], gu_ts fp32 [E]
+ *     (rows 0..I-1 of an expert are the gate projection, I..2I-1 the up one);
+ *   dn_codes u8 [E][H][I/2], dn_scales u8 [E][H][I/16], dn_ts fp32 [E];
+ *   x bf16 bits [T][H]; y fp32 [T][H];
+ *   workspace: device memory of at least moe_workspace_bytes(T, topk, H, I)
+ *   bytes, 256-byte aligned, owned by the caller, not shared by calls that
+ *   may overlap. Its first int32 is the status word (BQD_MOE_* bits, cleared
+ *   at the start of each call); h (fp32 [T*topk][I], pair order) starts at
+ *   byte 256 + 2 * align256(4 * T * topk).
+ *   H % 32 == 0, I % 32 == 0, 32 <= H <= 8192, 32 <= I <= 4096,
+ *   1 <= topk <= min(E, 32), E <= 1024, T * topk <= 8192.
+ *   Malformed lists never fault: the status word records them (read it with
+ *   bqd_moe_read_status) and the affected outputs are unspecified.
+ */
+bqd_status moe_grouped_gemv(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
+                            const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts, const uint16_t* x,
+                            const int32_t* expert_offsets, const int32_t* pair_token, const float* pair_weight,
+                            const int32_t* pair_slot, float* y, void* workspace, size_t workspace_bytes, int E,
+                            int H, int I, int T, int topk, cudaStream_t stream);
+
+/*
+ * bqd_moe_read_status -- waits for `stream`, copies the workspace's status
+ * word to *status_out and returns BQD_ERR_DEVICE if it is non-zero, else
+ * BQD_OK. Synchronising: do not call it inside a stream capture.
+ */
+bqd_status bqd_moe_read_status(const void* workspace, int32_t* status_out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BQD_H */

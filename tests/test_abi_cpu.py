@@ -1,0 +1,112 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+declared in include/bqd.h, and rejects bad arguments on the host before any
+CUDA call (the documented status codes)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from block_quantized_decode_nvfp4_gb300 import build
+    build.build()
+    import block_quantized_decode_nvfp4_gb300 as bqd
+    return bqd.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "bqd.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("nvfp4_gemv", "q8_0_gemv", "moe_grouped_gemv", "moe_route_topk", "nvfp4_dequant",
+                     "q8_0_dequant", "moe_workspace_bytes", "bqd_status_string", "bqd_moe_read_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import block_quantized_decode_nvfp4_gb300._binding as b
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+        assert name in b.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(L):
+    for code in range(9):
+        assert L.bqd_status_string(code)
+    assert L.bqd_status_string(99) == b"unknown status"
+    assert L.bqd_version() >= 100
+
+
+A = 0x10000  # a 16-byte aligned fake address: never dereferenced (every call below fails validation first)
+U = 0x10008  # misaligned
+
+
+def test_nvfp4_gemv_validation(L):
+    s = None
+    assert L.nvfp4_gemv(None, A, 1.0, A, A, 4, 32, 1, s) == 1          # NULL codes
+    assert L.nvfp4_gemv(A, A, 1.0, A, None, 4, 32, 1, s) == 1          # NULL y
+    assert L.nvfp4_gemv(A, A, 1.0, A, A, 4, 24, 1, s) == 2             # K % 16
+    assert L.nvfp4_gemv(A, A, 1.0, A, A, -1, 32, 1, s) == 2            # M < 0
+    assert L.nvfp4_gemv(A, A, 1.0, A, A, 4, 32, 0, s) == 2             # N < 1
+    assert L.nvfp4_gemv(A, A, 1.0, A, A, 4, 32, 17, s) == 2            # N > 16
+    assert L.nvfp4_gemv(U, A, 1.0, A, A, 4, 32, 1, s) == 3             # misaligned codes
+    assert L.nvfp4_gemv(A, A, 1.0, U, A, 4, 32, 1, s) == 3             # misaligned x
+    assert L.nvfp4_gemv(A, A, 1.0, A, U, 4, 32, 1, s) == 3             # misaligned y
+    assert L.nvfp4_gemv(None, None, 1.0, None, None, 0, 32, 1, s) == 0  # M == 0: no work, no CUDA call
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 4, 32, 1, 99, s) == 7    # unknown path
+    assert L.nvfp4_gemv(A, A, 1.0, A, A, 1 << 40, 1 << 30, 1, s) == 2  # M * K overflow
+
+
+def test_q8_0_and_dequant_validation(L):
+    s = None
+    assert L.q8_0_gemv(A, A, A, A, 4, 48, 1, s) == 2                   # K % 32
+    assert L.q8_0_gemv(A, None, A, A, 4, 64, 1, s) == 1
+    assert L.q8_0_gemv(A, A, A, A, 4, 64, 17, s) == 2
+    assert L.q8_0_gemv(A, U, A, A, 4, 64, 1, s) == 3
+    assert L.nvfp4_dequant(A, A, 1.0, None, 4, 32, s) == 1
+    assert L.nvfp4_dequant(A, A, 1.0, A, 4, 8, s) == 2
+    assert L.q8_0_dequant(A, A, U, 4, 32, s) == 3
+    assert L.q8_0_dequant(None, None, None, 0, 32, s) == 0
+
+
+def test_moe_validation(L):
+    s = None
+    assert L.moe_route_topk(A, 1, 8, 9, A, A, A, A, s) == 2            # topk > E
+    assert L.moe_route_topk(A, 1, 2000, 8, A, A, A, A, s) == 2         # E too large
+    assert L.moe_route_topk(A, 2000, 256, 8, A, A, A, A, s) == 2       # T * topk > 8192
+    assert L.moe_route_topk(A, 1, 256, 33, A, A, A, A, s) == 2         # topk > 32
+    assert L.moe_route_topk(None, 1, 256, 8, A, A, A, A, s) == 1
+    assert L.moe_route_topk(A, 1, 256, 8, A, U, A, A, s) == 3
+    ws = L.moe_workspace_bytes(16, 8, 2048, 512)
+    P = 128
+    align = lambda n: (n + 255) // 256 * 256
+    assert ws == 256 + 2 * align(4 * P) + align(4 * P * 512) + align(4 * P * 2048)
+    args = [A] * 12
+    assert L.moe_grouped_gemv(*args, None, ws, 256, 2048, 512, 16, 8, s) == 6      # no workspace
+    assert L.moe_grouped_gemv(*args, A, ws - 1, 256, 2048, 512, 16, 8, s) == 6     # too small
+    assert L.moe_grouped_gemv(*args, A + 16, ws, 256, 2048, 512, 16, 8, s) == 6    # not 256-aligned
+    assert L.moe_grouped_gemv(*args, A, ws, 256, 2047, 512, 16, 8, s) == 2         # H % 32
+    assert L.moe_grouped_gemv(*args, A, ws, 256, 2048, 500, 16, 8, s) == 2         # I % 32
+    bad = list(args)
+    bad[7] = None
+    assert L.moe_grouped_gemv(*bad, A, ws, 256, 2048, 512, 16, 8, s) == 1
+    bad[7] = U
+    assert L.moe_grouped_gemv(*bad, A, ws, 256, 2048, 512, 16, 8, s) == 3
+    out = C.c_int32(0)
+    assert L.bqd_moe_read_status(None, C.byref(out), s) == 1
+
+
+def test_binding_raises_on_error():
+    import block_quantized_decode_nvfp4_gb300 as bqd
+    with pytest.raises(bqd.BqdError) as ei:
+        bqd.nvfp4_gemv(None, A, 1.0, A, A, 4, 32, 1, stream=0)
+    assert ei.value.status == 1
