@@ -26,6 +26,8 @@ class BqdError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         msg = lib().bqd_status_string(status).decode() if _lib is not None else "?"
+        if status == 5 and _lib is not None:
+            msg += ": " + lib().bqd_last_cuda_error().decode()
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({msg})")
 
 
@@ -33,6 +35,7 @@ _vp, _i64, _i32, _f32, _sz = C.c_void_p, C.c_int64, C.c_int, C.c_float, C.c_size
 SIGNATURES = {
     "bqd_status_string": (C.c_char_p, [_i32]),
     "bqd_version": (_i32, []),
+    "bqd_last_cuda_error": (C.c_char_p, []),
     "nvfp4_gemv": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nvfp4_gemv_path": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),

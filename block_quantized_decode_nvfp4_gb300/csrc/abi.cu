@@ -39,7 +39,14 @@ bqd_status check_arch()
     return state[dev] == 1 ? BQD_OK : BQD_ERR_ARCH;
 }
 
-bqd_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BQD_OK : BQD_ERR_LAUNCH; }
+thread_local const char* t_last_cuda_error = "cudaSuccess";
+
+bqd_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return BQD_OK;
+    t_last_cuda_error = cudaGetErrorName(e);
+    return BQD_ERR_LAUNCH;
+}
 
 bqd_status zero_output(float* y, int64_t count, cudaStream_t s)
 {
@@ -84,6 +91,8 @@ const char* bqd_status_string(bqd_status s)
 }
 
 int bqd_version(void) { return 100; }
+
+const char* bqd_last_cuda_error(void) { return t_last_cuda_error; }
 
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream)

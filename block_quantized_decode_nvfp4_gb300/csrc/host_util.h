@@ -41,13 +41,23 @@ inline int blocks_per_sm(OccCache& c, const void* kern, int dev, int threads, si
     std::lock_guard<std::mutex> g(c.mu);
     if (dev < 0 || dev >= 64) return 1;
     if (!c.attr_set[dev]) {
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dev_info(dev).max_smem_optin);
+        // Allow dynamic shared memory up to the opt-in limit minus the
+        // kernel's static shared memory. Errors of these calls are consumed
+        // here so that they cannot surface as a launch error later.
+        cudaFuncAttributes fa{};
+        size_t static_smem = 0;
+        if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess) static_smem = fa.sharedSizeBytes;
+        const int optin = dev_info(dev).max_smem_optin;
+        if (optin > static_cast<int>(static_smem))
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - static_cast<int>(static_smem));
+        cudaGetLastError();
         c.attr_set[dev] = true;
     }
     for (int i = 0; i < 4; ++i)
         if (c.val[dev][i] && c.smem[dev][i] == smem) return c.val[dev][i];
     int n = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) cudaGetLastError();
     if (n < 1) n = 1;
     for (int i = 0; i < 4; ++i)
         if (!c.val[dev][i]) {

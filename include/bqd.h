@@ -85,6 +85,10 @@ const char* bqd_status_string(bqd_status s);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int bqd_version(void);
 
+/* Name of the CUDA error behind the calling thread's last BQD_ERR_LAUNCH
+ * (static storage; "cudaSuccess" if there was none). */
+const char* bqd_last_cuda_error(void);
+
 /*
  * nvfp4_gemv -- y[n][m] = ts * sum_k e2m1(c[m][k]) * e4m3(s[m][k/16]) * x[n][k]
  * ("robertbfuentes7-cloud/bw24" README, NVFP4 (W4) decode path; the N > 1
