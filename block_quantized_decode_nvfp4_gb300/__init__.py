@@ -9,6 +9,11 @@ generator.
 from ._binding import (  # noqa: F401
     BQD_PATH_AUTO,
     BQD_PATH_CUDA_CORE,
+    BQD_LAUNCH_PDL,
+    BQD_PATH_STREAM,
+    get_launch_flags,
+    set_launch_flags,
+    bqd_device_error,
     BqdError,
     bqd_moe_read_status,
     lib,
@@ -20,5 +25,6 @@ from ._binding import (  # noqa: F401
     nvfp4_gemv_path,
     q8_0_dequant,
     q8_0_gemv,
+    q8_0_gemv_path,
     version,
 )

@@ -18,6 +18,8 @@ STATUS_NAMES = {0: "BQD_OK", 1: "BQD_ERR_NULL", 2: "BQD_ERR_SHAPE", 3: "BQD_ERR_
                 5: "BQD_ERR_LAUNCH", 6: "BQD_ERR_WORKSPACE", 7: "BQD_ERR_PATH", 8: "BQD_ERR_DEVICE"}
 BQD_PATH_AUTO = 0
 BQD_PATH_CUDA_CORE = 1
+BQD_PATH_STREAM = 2
+BQD_LAUNCH_PDL = 1
 
 _lib = None
 
@@ -36,9 +38,13 @@ SIGNATURES = {
     "bqd_status_string": (C.c_char_p, [_i32]),
     "bqd_version": (_i32, []),
     "bqd_last_cuda_error": (C.c_char_p, []),
+    "bqd_set_launch_flags": (C.c_uint, [C.c_uint]),
+    "bqd_get_launch_flags": (C.c_uint, []),
     "nvfp4_gemv": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nvfp4_gemv_path": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "bqd_device_error": (_i32, [C.POINTER(C.c_uint)]),
     "nvfp4_dequant": (_i32, [_vp, _vp, _f32, _vp, _i64, _i64, _vp]),
     "q8_0_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
     "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -90,6 +96,15 @@ def version() -> int:
     return lib().bqd_version()
 
 
+def set_launch_flags(flags: int) -> int:
+    """Process-wide launch options (BQD_LAUNCH_*); returns the previous value."""
+    return lib().bqd_set_launch_flags(flags)
+
+
+def get_launch_flags() -> int:
+    return lib().bqd_get_launch_flags()
+
+
 def nvfp4_gemv(codes, scales, tensor_scale, x, y, M, K, N, stream=None):
     _check(lib().nvfp4_gemv(_ptr(codes), _ptr(scales), tensor_scale, _ptr(x), _ptr(y), M, K, N, _stream(stream)),
            "nvfp4_gemv")
@@ -102,6 +117,20 @@ def nvfp4_gemv_path(codes, scales, tensor_scale, x, y, M, K, N, path, stream=Non
 
 def q8_0_gemv(q, d, x, y, M, K, N, stream=None):
     _check(lib().q8_0_gemv(_ptr(q), _ptr(d), _ptr(x), _ptr(y), M, K, N, _stream(stream)), "q8_0_gemv")
+
+
+def q8_0_gemv_path(q, d, x, y, M, K, N, path, stream=None):
+    _check(lib().q8_0_gemv_path(_ptr(q), _ptr(d), _ptr(x), _ptr(y), M, K, N, path, _stream(stream)),
+           "q8_0_gemv_path")
+
+
+def bqd_device_error() -> int:
+    """Device error bits of the streaming kernels (synchronising; clears them)."""
+    out = C.c_uint(0)
+    st = lib().bqd_device_error(C.byref(out))
+    if st not in (BQD_OK, 8):
+        raise BqdError(st, "bqd_device_error")
+    return out.value
 
 
 def nvfp4_dequant(codes, scales, tensor_scale, w, M, K, stream=None):

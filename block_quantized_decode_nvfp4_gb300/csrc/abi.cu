@@ -8,6 +8,7 @@
 
 #include "bqd.h"
 #include "gemv.h"
+#include "host_util.h"
 
 namespace {
 
@@ -94,14 +95,24 @@ int bqd_version(void) { return 100; }
 
 const char* bqd_last_cuda_error(void) { return t_last_cuda_error; }
 
+unsigned int bqd_set_launch_flags(unsigned int flags)
+{
+    return bqd::launch_flags_ref().exchange(flags & BQD_LAUNCH_PDL);
+}
+
+unsigned int bqd_get_launch_flags(void) { return bqd::launch_flags(); }
+
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream)
 {
-    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE) return BQD_ERR_PATH;
+    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM) return BQD_ERR_PATH;
     bqd_status st = check_dense(codes, scales, x, y, M, K, N, 16, true);
     if (st != BQD_OK || M == 0) return st;
+    if (path == BQD_PATH_STREAM && !bqd::stream_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if ((st = check_arch()) != BQD_OK) return st;
     if (K == 0) return zero_output(y, M * N, stream);
+    if (path != BQD_PATH_CUDA_CORE && bqd::stream_gemv_supported(M, K, N))
+        return from_cuda(bqd::launch_nvfp4_gemv_stream(codes, scales, tensor_scale, x, y, M, K, stream));
     return from_cuda(bqd::launch_nvfp4_gemv_cuda_core(codes, scales, tensor_scale, x, y, M, K, N, stream));
 }
 
@@ -111,14 +122,35 @@ bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_
     return nvfp4_gemv_path(codes, scales, tensor_scale, x, y, M, K, N, BQD_PATH_AUTO, stream);
 }
 
+bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K,
+                          int N, int path, cudaStream_t stream)
+{
+    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM) return BQD_ERR_PATH;
+    bqd_status st = check_dense(q, d, x, y, M, K, N, 32, true);
+    if (st != BQD_OK || M == 0) return st;
+    if (path == BQD_PATH_STREAM && !bqd::stream_gemv_supported(M, K, N)) return BQD_ERR_PATH;
+    if ((st = check_arch()) != BQD_OK) return st;
+    if (K == 0) return zero_output(y, M * N, stream);
+    if (path != BQD_PATH_CUDA_CORE && bqd::stream_gemv_supported(M, K, N))
+        return from_cuda(bqd::launch_q8_0_gemv_stream(q, d, x, y, M, K, stream));
+    return from_cuda(bqd::launch_q8_0_gemv_cuda_core(q, d, x, y, M, K, N, stream));
+}
+
 bqd_status q8_0_gemv(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K, int N,
                      cudaStream_t stream)
 {
-    bqd_status st = check_dense(q, d, x, y, M, K, N, 32, true);
-    if (st != BQD_OK || M == 0) return st;
-    if ((st = check_arch()) != BQD_OK) return st;
-    if (K == 0) return zero_output(y, M * N, stream);
-    return from_cuda(bqd::launch_q8_0_gemv_cuda_core(q, d, x, y, M, K, N, stream));
+    return q8_0_gemv_path(q, d, x, y, M, K, N, BQD_PATH_AUTO, stream);
+}
+
+bqd_status bqd_device_error(unsigned int* bits_out)
+{
+    if (!bits_out) return BQD_ERR_NULL;
+    bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    unsigned int v = 0;
+    if (bqd::read_and_clear_stream_error(&v) != cudaSuccess) return BQD_ERR_LAUNCH;
+    *bits_out = v;
+    return v ? BQD_ERR_DEVICE : BQD_OK;
 }
 
 bqd_status nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, float* w, int64_t M,

@@ -146,7 +146,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
 // With kScaled the block scale is already folded into the elements.
 template <int RPW, int NC>
 __device__ __forceinline__ void nvfp4_word(const uint32_t (&w)[RPW], const uint32_t (&s2)[RPW], const float* xs,
-                                           int xstride, int k, float2 (&acc)[RPW][NC])
+                                           int xstride, int piece, int sw, float2 (&acc)[RPW][NC])
 {
     float2 wf[RPW][4];
 #pragma unroll
@@ -158,8 +158,8 @@ __device__ __forceinline__ void nvfp4_word(const uint32_t (&w)[RPW], const uint3
     }
 #pragma unroll
     for (int n = 0; n < NC; ++n) {
-        const float4 xa = *reinterpret_cast<const float4*>(xs + n * xstride + k);
-        const float4 xb = *reinterpret_cast<const float4*>(xs + n * xstride + k + 4);
+        const float4 xa = *reinterpret_cast<const float4*>(xs + n * xstride + ((piece ^ sw) << 2));
+        const float4 xb = *reinterpret_cast<const float4*>(xs + n * xstride + (((piece + 1) ^ sw) << 2));
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             acc[r][n] = __ffma2_rn(wf[r][0], make_float2(xa.x, xa.y), acc[r][n]);
@@ -174,7 +174,7 @@ __device__ __forceinline__ void nvfp4_word(const uint32_t (&w)[RPW], const uint3
 // (cheaper than scaling every element when there is a single column).
 template <int RPW>
 __device__ __forceinline__ void nvfp4_block_n1(const uint32_t (&w0)[RPW], const uint32_t (&w1)[RPW],
-                                               const float (&s)[RPW], const float* xs, int k,
+                                               const float (&s)[RPW], const float* xs, int piece, int sw,
                                                float2 (&acc)[RPW][1])
 {
     float2 part[RPW];
@@ -182,8 +182,8 @@ __device__ __forceinline__ void nvfp4_block_n1(const uint32_t (&w0)[RPW], const 
     for (int r = 0; r < RPW; ++r) part[r] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const float4 xa = *reinterpret_cast<const float4*>(xs + k + 8 * j);
-        const float4 xb = *reinterpret_cast<const float4*>(xs + k + 8 * j + 4);
+        const float4 xa = *reinterpret_cast<const float4*>(xs + (((piece + 2 * j) ^ sw) << 2));
+        const float4 xb = *reinterpret_cast<const float4*>(xs + (((piece + 2 * j + 1) ^ sw) << 2));
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             uint32_t h[4];
@@ -198,8 +198,13 @@ __device__ __forceinline__ void nvfp4_block_n1(const uint32_t (&w0)[RPW], const 
     for (int r = 0; r < RPW; ++r) acc[r][0].x = fmaf(s[r], part[r].x + part[r].y, acc[r][0].x);
 }
 
+// Activations are staged in shared memory chunk by chunk (kElems fp32 per
+// chunk), the 16-byte pieces of chunk c permuted by XOR with swz(c), so that
+// the 32 lanes of a warp, which read the same piece of 32 consecutive
+// chunks, hit distinct banks.
 struct Nvfp4Vec {
     static constexpr int kElems = 32;
+    __device__ static __forceinline__ int swz(int c) { return c & 7; }
     struct Chunk {
         uint4 c;
         uint32_t s;
@@ -212,7 +217,7 @@ struct Nvfp4Vec {
         return ch;
     }
     template <int RPW, int NC>
-    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride,
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride, int sw,
                                                float2 (&acc)[RPW][NC])
     {
         if constexpr (NC == 1) {
@@ -228,7 +233,7 @@ struct Nvfp4Vec {
                     const float2 sc = e4m3x2_to_float2(ch[r].s);
                     s[r] = b ? sc.y : sc.x;
                 }
-                nvfp4_block_n1<RPW>(w0, w1, s, xs, 16 * b, acc);
+                nvfp4_block_n1<RPW>(w0, w1, s, xs, 4 * b, sw, acc);
             }
         } else {
             uint32_t sb[2][RPW];
@@ -246,7 +251,7 @@ struct Nvfp4Vec {
                     const uint32_t words[4] = {ch[r].c.x, ch[r].c.y, ch[r].c.z, ch[r].c.w};
                     w[r] = words[j];
                 }
-                nvfp4_word<RPW, NC>(w, sb[j / 2], xs, xstride, 8 * j, acc);
+                nvfp4_word<RPW, NC>(w, sb[j / 2], xs, xstride, 2 * j, sw, acc);
             }
         }
     }
@@ -254,6 +259,7 @@ struct Nvfp4Vec {
 
 struct Nvfp4Narrow {
     static constexpr int kElems = 16;
+    __device__ static __forceinline__ int swz(int c) { return (c >> 1) & 3; }
     struct Chunk {
         uint2 c;
         uint32_t s;
@@ -266,7 +272,7 @@ struct Nvfp4Narrow {
         return ch;
     }
     template <int RPW, int NC>
-    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride,
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride, int sw,
                                                float2 (&acc)[RPW][NC])
     {
         uint32_t sb[RPW];
@@ -277,13 +283,14 @@ struct Nvfp4Narrow {
             uint32_t w[RPW];
 #pragma unroll
             for (int r = 0; r < RPW; ++r) w[r] = j ? ch[r].c.y : ch[r].c.x;
-            nvfp4_word<RPW, NC>(w, sb, xs, xstride, 8 * j, acc);
+            nvfp4_word<RPW, NC>(w, sb, xs, xstride, 2 * j, sw, acc);
         }
     }
 };
 
 struct Q8_0Fmt {
     static constexpr int kElems = 32;
+    __device__ static __forceinline__ int swz(int c) { return c & 7; }
     struct Chunk {
         uint4 a, b;
         uint32_t d;
@@ -298,7 +305,7 @@ struct Q8_0Fmt {
         return ch;
     }
     template <int RPW, int NC>
-    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride,
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride, int sw,
                                                float2 (&acc)[RPW][NC])
     {
         float2 part[RPW][NC];
@@ -317,7 +324,7 @@ struct Q8_0Fmt {
             }
 #pragma unroll
             for (int n = 0; n < NC; ++n) {
-                const float4 xv = *reinterpret_cast<const float4*>(xs + n * xstride + 4 * j);
+                const float4 xv = *reinterpret_cast<const float4*>(xs + n * xstride + ((j ^ sw) << 2));
 #pragma unroll
                 for (int r = 0; r < RPW; ++r) {
                     part[r][n] = __ffma2_rn(lo[r], make_float2(xv.x, xv.y), part[r][n]);
@@ -354,40 +361,70 @@ struct RowPitch<Q8_0Fmt> {
 };
 
 // ------------------------------------------------------------------ rows
-// Dot products of RPW weight rows with NC activation columns over chunks
-// [c_begin, c_end) of the rows, spread over a group of LG lanes (lane g of
-// the group takes chunks c_begin + g, c_begin + g + LG, ...). Every row
-// pointer must address a valid row (callers repeat a valid row for the
-// unused slots of a partial group). The next chunk of every row is loaded
-// before the current one is multiplied, so each lane keeps 2 * RPW chunks in
-// flight. xs points at the activation of chunk c_begin. acc[r][n] receives
-// this lane's partial sums (not yet reduced).
-template <class F, int RPW, int NC, int LG = kWarp>
-__device__ __forceinline__ void dot_rows(const uint8_t* const (&codes_row)[RPW],
-                                         const uint8_t* const (&scales_row)[RPW], int c_begin, int c_end,
-                                         const float* xs, int xstride, int g, float2 (&acc)[RPW][NC])
-{
+// A stream of chunk loads for RPW weight rows over chunks [c_begin, c_end),
+// spread over a group of LG lanes (lane g of the group takes chunks
+// c_begin + g, c_begin + g + LG, ...), keeping D chunks of every row in
+// flight in a register ring. start() issues the first D loads and may be
+// called long before run() (e.g. before the activations are staged), so
+// the HBM latency of the first loads overlaps that work.
+// Every row pointer must address a valid row (callers repeat a valid row for
+// the unused slots of a partial group).
+template <class F, int RPW, int D, int LG = kWarp>
+struct RowStream {
     using Chunk = typename F::Chunk;
-    int c = c_begin + g;
-    if (c >= c_end) return;
-    Chunk cur[RPW];
+    Chunk buf[D][RPW];
+    const uint8_t* crow[RPW];
+    const uint8_t* srow[RPW];
+    int c0, c_end, g;
+
+    __device__ __forceinline__ void start(const uint8_t* const (&codes_row)[RPW],
+                                          const uint8_t* const (&scales_row)[RPW], int c_begin, int c_stop,
+                                          int lane_in_group)
+    {
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) cur[r] = F::load(codes_row[r], scales_row[r], c);
-    for (;;) {
-        const int cn = c + LG;
-        const bool more = cn < c_end;
-        Chunk nxt[RPW];
-        if (more) {
-#pragma unroll
-            for (int r = 0; r < RPW; ++r) nxt[r] = F::load(codes_row[r], scales_row[r], cn);
+        for (int r = 0; r < RPW; ++r) {
+            crow[r] = codes_row[r];
+            srow[r] = scales_row[r];
         }
-        F::template dot<RPW, NC>(cur, xs + (c - c_begin) * F::kElems, xstride, acc);
-        if (!more) break;
+        c0 = c_begin;
+        c_end = c_stop;
+        g = lane_in_group;
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) cur[r] = nxt[r];
-        c = cn;
+        for (int i = 0; i < D; ++i) {
+            const int c = c0 + g + i * LG;
+            if (c < c_end) {
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) buf[i][r] = F::load(crow[r], srow[r], c);
+            }
+        }
     }
-}
+
+    // acc[r][n] += this lane's partial sums over its chunks; xs points at the
+    // activation of chunk c_begin (column n at xs + n * xstride).
+    template <int NC>
+    __device__ __forceinline__ void run(const float* xs, int xstride, float2 (&acc)[RPW][NC])
+    {
+        for (int base = c0 + g; base < c_end; base += D * LG) {
+#pragma unroll
+            for (int i = 0; i < D; ++i) {
+                const int c = base + i * LG;
+                if (c < c_end) {
+                    const int cn = c + D * LG;
+                    Chunk nxt[RPW];
+                    if (cn < c_end) {
+#pragma unroll
+                        for (int r = 0; r < RPW; ++r) nxt[r] = F::load(crow[r], srow[r], cn);
+                    }
+                    F::template dot<RPW, NC>(buf[i], xs + (c - c0) * F::kElems, xstride, F::swz(c - c0), acc);
+                    if (cn < c_end) {
+#pragma unroll
+                        for (int r = 0; r < RPW; ++r) buf[i][r] = nxt[r];
+                    }
+                }
+            }
+        }
+    }
+};
 
 // Sum over aligned groups of LG lanes (every lane of the group gets the sum).
 template <int LG = kWarp>
@@ -400,17 +437,34 @@ __device__ __forceinline__ float group_sum(float v)
 
 __device__ __forceinline__ float warp_sum(float v) { return group_sum<kWarp>(v); }
 
-// Stage NC bf16 activation columns x[n][k0 .. k0+len) (row pitch K) into
-// shared memory as fp32, column n at xs + n * len. len and k0 are even.
+// Stage ncols bf16 activation columns x[n][k0 .. k0+len) (row pitch K) into
+// shared memory as fp32 in the swizzled chunk layout of format F, column n
+// at xs + n * len. Needs len % F::kElems == 0, k0 % 4 == 0, K % 4 == 0 and
+// an 8-byte aligned x.
+template <class F>
 __device__ __forceinline__ void stage_x_bf16(const uint16_t* x, int64_t K, int ncols, int k0, int len, float* xs)
 {
-    const int pairs = len / 2;
-    for (int i = threadIdx.x; i < ncols * pairs; i += blockDim.x) {
-        const int n = i / pairs, p = i - n * pairs;
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(x + n * K + k0 + 2 * p);
-        xs[n * len + 2 * p] = bf16_lo(v);
-        xs[n * len + 2 * p + 1] = bf16_hi(v);
+    constexpr int P = F::kElems / 4;  // 16-byte pieces per chunk
+    const int pieces = len / 4;
+    const int total = ncols * pieces;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int n = i / pieces, q = i - n * pieces;
+        const uint2 u = *reinterpret_cast<const uint2*>(x + n * K + k0 + 4 * q);
+        const int c = q / P, j = q % P;
+        *reinterpret_cast<float4*>(xs + n * len + c * F::kElems + ((j ^ F::swz(c)) << 2)) =
+            make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
     }
+}
+
+// Put one 16-byte piece (4 fp32, global piece index q of a column) at its
+// swizzled place in the chunk layout of format F.
+template <class F>
+__device__ __forceinline__ void put_piece(float* col, int q, float4 v)
+{
+    constexpr int P = F::kElems / 4;
+    const int c = q / P, j = q % P;
+    *reinterpret_cast<float4*>(col + c * F::kElems + ((j ^ F::swz(c)) << 2)) = v;
 }
 
 }  // namespace bqd

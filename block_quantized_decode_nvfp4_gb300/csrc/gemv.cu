@@ -33,18 +33,29 @@ constexpr int kWarps = kThreads / kWarp;
 // Shared memory for the fp32 activations of one segment of K.
 constexpr int kXsBudgetBytes = 96 * 1024;
 
-template <int NC>
-struct Rpw {
-    static constexpr int value = NC <= 4 ? 4 : 2;
-};
-
-// One launch computes NC columns. When NC * K fp32 activations fit in
-// shared memory (seg_len == K) every warp owns a contiguous, balanced range
-// of rows and never synchronises. Otherwise K is processed in segments of
+// One launch computes NC columns for groups of RPW rows, keeping D chunks of
+// each row in flight. When NC * K fp32 activations fit in shared memory
+// (seg_len == K) every warp owns a contiguous, balanced range of rows; it
+// issues its first weight loads before the CTA stages the activations, and
+// never synchronises afterwards. Otherwise K is processed in segments of
 // seg_len elements: the CTA owns a balanced row range, walks it in batches of
 // kWarps * RPW rows and restages the activations for each segment.
-template <class F, int RPW, int NC>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const uint8_t* __restrict__ codes,
+// Row pointers of the group starting at r0 (rows past r_end repeat r0).
+template <int RPW>
+__device__ __forceinline__ void group_rows(const uint8_t* codes, const uint8_t* scales, int64_t cpitch,
+                                           int64_t spitch, int64_t r0, int64_t r_end, const uint8_t* (&crow)[RPW],
+                                           const uint8_t* (&srow)[RPW])
+{
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        const int64_t m = r0 + r < r_end ? r0 + r : r0;
+        crow[r] = codes + m * cpitch;
+        srow[r] = scales + m * spitch;
+    }
+}
+
+template <class F, int RPW, int NC, int D>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const uint8_t* __restrict__ codes,
                                                         const uint8_t* __restrict__ scales, float ts,
                                                         const uint16_t* __restrict__ x, float* __restrict__ y,
                                                         int64_t M, int64_t K, int seg_len)
@@ -55,29 +66,30 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint8_t* __restric
     const int64_t cpitch = RowPitch<F>::codes(K);
     const int64_t spitch = RowPitch<F>::scales(K);
     const int chunks = static_cast<int>(K / F::kElems);
+    RowStream<F, RPW, D> rs;
 
     if (seg_len == K) {
-        stage_x_bf16(x, K, NC, 0, static_cast<int>(K), xs);
-        __syncthreads();
         const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
         const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
         const int64_t r_lo = M * gw / nw, r_hi = M * (gw + 1) / nw;
+        const uint8_t* crow[RPW];
+        const uint8_t* srow[RPW];
+        group_rows(codes, scales, cpitch, spitch, r_lo, r_hi, crow, srow);
+        if (r_lo < r_hi) rs.start(crow, srow, 0, chunks, lane);
+        stage_x_bf16<F>(x, K, NC, 0, static_cast<int>(K), xs);
+        __syncthreads();
         for (int64_t r0 = r_lo; r0 < r_hi; r0 += RPW) {
-            const int nrows = static_cast<int>(r_hi - r0 < RPW ? r_hi - r0 : RPW);
-            const uint8_t* crow[RPW];
-            const uint8_t* srow[RPW];
-#pragma unroll
-            for (int r = 0; r < RPW; ++r) {
-                const int64_t m = r0 + (r < nrows ? r : 0);
-                crow[r] = codes + m * cpitch;
-                srow[r] = scales + m * spitch;
+            if (r0 != r_lo) {
+                group_rows(codes, scales, cpitch, spitch, r0, r_hi, crow, srow);
+                rs.start(crow, srow, 0, chunks, lane);
             }
+            const int nrows = static_cast<int>(r_hi - r0 < RPW ? r_hi - r0 : RPW);
             float2 acc[RPW][NC];
 #pragma unroll
             for (int r = 0; r < RPW; ++r)
 #pragma unroll
                 for (int n = 0; n < NC; ++n) acc[r][n] = make_float2(0.f, 0.f);
-            dot_rows<F, RPW, NC>(crow, srow, 0, chunks, xs, static_cast<int>(K), lane, acc);
+            rs.template run<NC>(xs, static_cast<int>(K), acc);
 #pragma unroll
             for (int r = 0; r < RPW; ++r)
 #pragma unroll
@@ -112,10 +124,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const uint8_t* __restric
         for (int c0 = 0; c0 < chunks; c0 += seg_chunks) {
             const int c1 = c0 + seg_chunks < chunks ? c0 + seg_chunks : chunks;
             const int len = (c1 - c0) * F::kElems;
+            if (nrows > 0) rs.start(crow, srow, c0, c1, lane);
             __syncthreads();
-            stage_x_bf16(x, K, NC, c0 * F::kElems, len, xs);
+            stage_x_bf16<F>(x, K, NC, c0 * F::kElems, len, xs);
             __syncthreads();
-            if (nrows > 0) dot_rows<F, RPW, NC>(crow, srow, c0, c1, xs, len, lane, acc);
+            if (nrows > 0) rs.template run<NC>(xs, len, acc);
         }
 #pragma unroll
         for (int r = 0; r < RPW; ++r)
@@ -159,28 +172,50 @@ __global__ void q8_0_dequant_kernel(const int8_t* __restrict__ q, const uint16_t
 }
 
 // ------------------------------------------------------------------ host
+// Launch one (RPW, D) instantiation over a balanced grid filling every SM.
+template <class F, int RPW, int NC, int D>
+cudaError_t launch_cfg(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y, int64_t M,
+                       int64_t K, int seg, cudaStream_t stream, int dev, int64_t* grid_out, bool dry)
+{
+    auto kern = gemv_kernel<F, RPW, NC, D>;
+    static OccCache occ;
+    const size_t smem = static_cast<size_t>(NC) * seg * sizeof(float);
+    const int bps = blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, kThreads, smem);
+    int64_t grid = static_cast<int64_t>(dev_info(dev).sms) * bps;
+    const int64_t need = (seg == K) ? (M + kWarps - 1) / kWarps : (M + kWarps * RPW - 1) / (kWarps * RPW);
+    if (grid > need) grid = need;
+    if (grid < 1) grid = 1;
+    *grid_out = grid;
+    if (dry) return cudaSuccess;
+    kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(codes, scales, ts, x, y, M, K, seg);
+    return cudaGetLastError();
+}
+
 template <class F, int NC>
 cudaError_t launch_nc(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
                       int64_t M, int64_t K, cudaStream_t stream)
 {
-    constexpr int RPW = Rpw<NC>::value;
-    auto kern = gemv_kernel<F, RPW, NC>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const DevInfo di = dev_info(dev);
     const int64_t budget = kXsBudgetBytes / 4 / NC;  // fp32 elements per column
     int seg = static_cast<int>(K);
     if (K > budget) seg = static_cast<int>(budget / F::kElems) * F::kElems;
-    const size_t smem = static_cast<size_t>(NC) * seg * sizeof(float);
-    static OccCache occ;
-    const int bps = blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, kThreads, smem);
-    int64_t grid = static_cast<int64_t>(di.sms) * bps;
-    const int64_t need = (seg == K) ? (M + kWarps - 1) / kWarps : (M + kWarps * RPW - 1) / (kWarps * RPW);
-    if (grid > need) grid = need;
-    if (grid < 1) grid = 1;
-    kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(codes, scales, ts, x, y, M, K, seg);
-    return cudaGetLastError();
+    int64_t grid = 0;
+    if constexpr (NC == 1) {
+        // Rows per warp decide the group size: fewer rows -> smaller groups
+        // with a deeper per-row prefetch, so no warp loads duplicate rows.
+        launch_cfg<F, 4, 1, 2>(codes, scales, ts, x, y, M, K, seg, stream, dev, &grid, true);
+        const int64_t rows_per_warp = M / (grid * kWarps);
+        if (rows_per_warp >= 4 || seg != K)
+            return launch_cfg<F, 4, 1, 2>(codes, scales, ts, x, y, M, K, seg, stream, dev, &grid, false);
+        if (rows_per_warp >= 2)
+            return launch_cfg<F, 2, 1, 4>(codes, scales, ts, x, y, M, K, seg, stream, dev, &grid, false);
+        return launch_cfg<F, 1, 1, 8>(codes, scales, ts, x, y, M, K, seg, stream, dev, &grid, false);
+    } else {
+        constexpr int RPW = NC <= 4 ? 4 : 2;
+        return launch_cfg<F, RPW, NC, 2>(codes, scales, ts, x, y, M, K, seg, stream, dev, &grid, false);
+    }
 }
 
 template <class F>

@@ -18,6 +18,15 @@ cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, fl
                                  int64_t K, cudaStream_t s);
 cudaError_t launch_q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t s);
 
+// Bulk-copy streaming GEMV (gemv_stream.cu): N == 1, K % 256 == 0.
+bool stream_gemv_supported(int64_t M, int64_t K, int N);
+cudaError_t launch_nvfp4_gemv_stream(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                     float* y, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_q8_0_gemv_stream(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
+                                    int64_t K, cudaStream_t s);
+// Reads and clears the device error word of the streaming kernels (synchronous).
+cudaError_t read_and_clear_stream_error(unsigned int* out);
+
 // MoE (moe.cu). Limits checked by the ABI layer: E <= 1024, topk <= 32,
 // T * topk <= 8192.
 constexpr int kMoeMaxExperts = 1024;

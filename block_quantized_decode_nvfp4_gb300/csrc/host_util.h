@@ -4,10 +4,20 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstddef>
 #include <mutex>
 
 namespace bqd {
+
+// Process-wide launch options (bqd_set_launch_flags).
+constexpr unsigned kLaunchPdl = 1u;
+inline std::atomic<unsigned>& launch_flags_ref()
+{
+    static std::atomic<unsigned> flags{0};
+    return flags;
+}
+inline unsigned launch_flags() { return launch_flags_ref().load(std::memory_order_relaxed); }
 
 struct DevInfo {
     int sms = 0;

@@ -230,9 +230,48 @@ __device__ void moe_validate_and_clear(const int32_t* __restrict__ offsets, int 
 }
 
 // ------------------------------------------------------------------ gate_up
-template <int LG, int NC>
+// Row pointers of PAIRS (gate, up) pairs starting at pair ib of an expert's
+// gate_up weight: slots (2p, 2p+1) = rows (ib+p, I+ib+p). Returns the number
+// of valid pairs; unused slots repeat a valid row.
+template <int PAIRS>
+__device__ __forceinline__ int pair_rows(const uint8_t* codes_e, const uint8_t* scales_e, int64_t cpitch,
+                                         int64_t spitch, int I, int ib, int i_hi, const uint8_t* (&crow)[2 * PAIRS],
+                                         const uint8_t* (&srow)[2 * PAIRS])
+{
+    const int npairs = ib >= i_hi ? 0 : (i_hi - ib >= PAIRS ? PAIRS : i_hi - ib);
+#pragma unroll
+    for (int r = 0; r < 2 * PAIRS; ++r) {
+        const int pr = r / 2 < npairs ? r / 2 : 0;
+        const int64_t row = (r % 2 == 0 ? 0 : I) + (npairs ? ib + pr : 0);
+        crow[r] = codes_e + row * cpitch;
+        srow[r] = scales_e + row * spitch;
+    }
+    return npairs;
+}
+
+// Row pointers of RPW consecutive rows starting at jb (< j_hi valid).
+template <int RPW>
+__device__ __forceinline__ int block_rows(const uint8_t* codes_e, const uint8_t* scales_e, int64_t cpitch,
+                                          int64_t spitch, int jb, int j_hi, const uint8_t* (&crow)[RPW],
+                                          const uint8_t* (&srow)[RPW])
+{
+    const int nrows = jb >= j_hi ? 0 : (j_hi - jb >= RPW ? RPW : j_hi - jb);
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        const int64_t row = nrows ? jb + (r < nrows ? r : 0) : 0;
+        crow[r] = codes_e + row * cpitch;
+        srow[r] = scales_e + row * spitch;
+    }
+    return nrows;
+}
+
+// Rows of one expert's gate_up weight against NC staged token columns. The
+// first row group's loads are issued before `stage` fills the activations
+// (CTA-wide, followed by a barrier), so that staging hides under HBM latency.
+template <int LG, int NC, class Stage>
 __device__ __forceinline__ void gate_up_rows(const uint8_t* codes_e, const uint8_t* scales_e, float ts, int H, int I,
-                                             int i_lo, int i_hi, const float* xs, int g0, int ng, float* h_ws)
+                                             int i_lo, int i_hi, const float* xs, int g0, int ng, float* h_ws,
+                                             Stage stage)
 {
     constexpr int PAIRS = NC <= 4 ? 2 : 1;      // (gate, up) row pairs per lane group
     constexpr int RPW = 2 * PAIRS;
@@ -243,23 +282,24 @@ __device__ __forceinline__ void gate_up_rows(const uint8_t* codes_e, const uint8
     const int chunks = H / Nvfp4Vec::kElems;
     const int mine = (warp * kGroups + grp) * PAIRS;
     const int step = kWarps * kGroups * PAIRS;
+    RowStream<Nvfp4Vec, RPW, 2, LG> rs;
+    const uint8_t* crow[RPW];
+    const uint8_t* srow[RPW];
+    int npairs = pair_rows<PAIRS>(codes_e, scales_e, cpitch, spitch, I, i_lo + mine, i_hi, crow, srow);
+    if (npairs) rs.start(crow, srow, 0, chunks, g);
+    stage();
+    __syncthreads();
     for (int ib = i_lo + mine; ib - mine < i_hi; ib += step) {
-        const int npairs = ib >= i_hi ? 0 : (i_hi - ib >= PAIRS ? PAIRS : i_hi - ib);
-        const uint8_t* crow[RPW];
-        const uint8_t* srow[RPW];
-#pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            const int pr = r / 2 < npairs ? r / 2 : 0;
-            const int64_t row = (r % 2 == 0 ? 0 : I) + (npairs ? ib + pr : 0);
-            crow[r] = codes_e + row * cpitch;
-            srow[r] = scales_e + row * spitch;
+        if (ib != i_lo + mine) {
+            npairs = pair_rows<PAIRS>(codes_e, scales_e, cpitch, spitch, I, ib, i_hi, crow, srow);
+            if (npairs) rs.start(crow, srow, 0, chunks, g);
         }
         float2 acc[RPW][NC];
 #pragma unroll
         for (int r = 0; r < RPW; ++r)
 #pragma unroll
             for (int n = 0; n < NC; ++n) acc[r][n] = make_float2(0.f, 0.f);
-        if (npairs) dot_rows<Nvfp4Vec, RPW, NC, LG>(crow, srow, 0, chunks, xs, H, g, acc);
+        if (npairs) rs.template run<NC>(xs, H, acc);
 #pragma unroll
         for (int p = 0; p < PAIRS; ++p)
 #pragma unroll
@@ -275,7 +315,7 @@ __device__ __forceinline__ void gate_up_rows(const uint8_t* codes_e, const uint8
 }
 
 template <int LG, int NCG>
-__global__ void __launch_bounds__(kThreads) moe_gate_up_kernel(
+__global__ void __launch_bounds__(kThreads, 1) moe_gate_up_kernel(
     const uint8_t* __restrict__ gu_codes, const uint8_t* __restrict__ gu_scales, const float* __restrict__ gu_ts,
     const uint16_t* __restrict__ x, const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_token,
     MoeWorkspace ws, int E, int H, int I, int T, int topk)
@@ -299,39 +339,39 @@ __global__ void __launch_bounds__(kThreads) moe_gate_up_kernel(
     for (int g0 = p0; g0 < p1; g0 += NCG) {
         const int ng = p1 - g0 < NCG ? p1 - g0 : NCG;
         __syncthreads();
-        for (int i = threadIdx.x; i < NCG * (H / 2); i += kThreads) {
-            const int n = i / (H / 2), k2 = i - n * (H / 2);
-            float lo = 0.f, hi = 0.f;
-            if (n < ng) {
+        auto stage = [&]() {
+            // the ng token columns, 8 bf16 per 16-byte load; columns past ng
+            // are never written back, so they are left unstaged
+            const int vecs = H / 8;
+            for (int i = threadIdx.x; i < ng * vecs; i += kThreads) {
+                const int n = i / vecs, v = i - n * vecs;
                 const int t = pair_token[g0 + n];
-                if (t >= 0 && t < T) {
-                    const uint32_t v = *reinterpret_cast<const uint32_t*>(x + static_cast<int64_t>(t) * H + 2 * k2);
-                    lo = bf16_lo(v);
-                    hi = bf16_hi(v);
-                } else if (k2 == 0) {
+                uint4 u = make_uint4(0, 0, 0, 0);
+                if (t >= 0 && t < T)
+                    u = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H + 8 * v);
+                else if (v == 0)
                     atomicOr(ws.status, kStatusBadPair);
-                }
+                put_piece<Nvfp4Vec>(xs + n * H, 2 * v, make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)));
+                put_piece<Nvfp4Vec>(xs + n * H, 2 * v + 1,
+                                    make_float4(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)));
             }
-            xs[n * H + 2 * k2] = lo;
-            xs[n * H + 2 * k2 + 1] = hi;
-        }
-        __syncthreads();
+        };
         if (ng == 1)
-            gate_up_rows<LG, 1>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h);
+            gate_up_rows<LG, 1>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h, stage);
         else if (ng == 2)
-            gate_up_rows<LG, 2>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h);
+            gate_up_rows<LG, 2>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h, stage);
         else if (ng <= 4)
-            gate_up_rows<LG, 4>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h);
+            gate_up_rows<LG, 4>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h, stage);
         else
-            gate_up_rows<LG, NCG>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h);
+            gate_up_rows<LG, NCG>(codes_e, scales_e, ts, H, I, i_lo, i_hi, xs, g0, ng, ws.h, stage);
     }
 }
 
 // ------------------------------------------------------------------ down
-template <int LG, int NC>
+template <int LG, int NC, class Stage>
 __device__ __forceinline__ void down_rows(const uint8_t* codes_e, const uint8_t* scales_e, float ts, int H, int I,
                                           int j_lo, int j_hi, const float* xs, const int* slot_of, int ng,
-                                          float* part)
+                                          float* part, Stage stage)
 {
     constexpr int RPW = NC <= 4 ? 4 : 2;
     constexpr int kGroups = kWarp / LG;
@@ -341,22 +381,24 @@ __device__ __forceinline__ void down_rows(const uint8_t* codes_e, const uint8_t*
     const int chunks = I / Nvfp4Vec::kElems;
     const int mine = (warp * kGroups + grp) * RPW;
     const int step = kWarps * kGroups * RPW;
+    RowStream<Nvfp4Vec, RPW, 2, LG> rs;
+    const uint8_t* crow[RPW];
+    const uint8_t* srow[RPW];
+    int nrows = block_rows<RPW>(codes_e, scales_e, cpitch, spitch, j_lo + mine, j_hi, crow, srow);
+    if (nrows) rs.start(crow, srow, 0, chunks, g);
+    stage();
+    __syncthreads();
     for (int jb = j_lo + mine; jb - mine < j_hi; jb += step) {
-        const int nrows = jb >= j_hi ? 0 : (j_hi - jb >= RPW ? RPW : j_hi - jb);
-        const uint8_t* crow[RPW];
-        const uint8_t* srow[RPW];
-#pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            const int64_t row = nrows ? jb + (r < nrows ? r : 0) : 0;
-            crow[r] = codes_e + row * cpitch;
-            srow[r] = scales_e + row * spitch;
+        if (jb != j_lo + mine) {
+            nrows = block_rows<RPW>(codes_e, scales_e, cpitch, spitch, jb, j_hi, crow, srow);
+            if (nrows) rs.start(crow, srow, 0, chunks, g);
         }
         float2 acc[RPW][NC];
 #pragma unroll
         for (int r = 0; r < RPW; ++r)
 #pragma unroll
             for (int n = 0; n < NC; ++n) acc[r][n] = make_float2(0.f, 0.f);
-        if (nrows) dot_rows<Nvfp4Vec, RPW, NC, LG>(crow, srow, 0, chunks, xs, I, g, acc);
+        if (nrows) rs.template run<NC>(xs, I, acc);
 #pragma unroll
         for (int r = 0; r < RPW; ++r)
 #pragma unroll
@@ -369,7 +411,7 @@ __device__ __forceinline__ void down_rows(const uint8_t* codes_e, const uint8_t*
 }
 
 template <int LG>
-__global__ void __launch_bounds__(kThreads) moe_down_kernel(
+__global__ void __launch_bounds__(kThreads, 1) moe_down_kernel(
     const uint8_t* __restrict__ dn_codes, const uint8_t* __restrict__ dn_scales, const float* __restrict__ dn_ts,
     const int32_t* __restrict__ offsets, const int32_t* __restrict__ pair_token,
     const float* __restrict__ pair_weight, const int32_t* __restrict__ pair_slot, MoeWorkspace ws, int E, int H,
@@ -392,35 +434,38 @@ __global__ void __launch_bounds__(kThreads) moe_down_kernel(
     for (int g0 = p0; g0 < p1; g0 += NCG) {
         const int ng = p1 - g0 < NCG ? p1 - g0 : NCG;
         __syncthreads();
-        if (threadIdx.x < NCG) {
-            int flat = -1;
-            if (static_cast<int>(threadIdx.x) < ng) {
-                const int t = pair_token[g0 + threadIdx.x], s = pair_slot[g0 + threadIdx.x];
-                if (t >= 0 && t < T && s >= 0 && s < topk) {
-                    flat = t * topk + s;
-                    if (blockIdx.y == 0) {
-                        ws.wts[flat] = pair_weight[g0 + threadIdx.x];
-                        atomicAdd(ws.count + flat, 1);
+        auto stage = [&]() {
+            if (threadIdx.x < NCG) {
+                int flat = -1;
+                if (static_cast<int>(threadIdx.x) < ng) {
+                    const int t = pair_token[g0 + threadIdx.x], s = pair_slot[g0 + threadIdx.x];
+                    if (t >= 0 && t < T && s >= 0 && s < topk) {
+                        flat = t * topk + s;
+                        if (blockIdx.y == 0) {
+                            ws.wts[flat] = pair_weight[g0 + threadIdx.x];
+                            atomicAdd(ws.count + flat, 1);
+                        }
+                    } else {
+                        atomicOr(ws.status, kStatusBadPair);
                     }
-                } else {
-                    atomicOr(ws.status, kStatusBadPair);
                 }
+                slot_of[threadIdx.x] = flat;
             }
-            slot_of[threadIdx.x] = flat;
-        }
-        for (int i = threadIdx.x; i < NCG * I; i += kThreads) {
-            const int n = i / I, k = i - n * I;
-            xs[i] = n < ng ? ws.h[static_cast<int64_t>(g0 + n) * I + k] : 0.f;
-        }
-        __syncthreads();
+            const int vecs = I / 4;
+            for (int i = threadIdx.x; i < ng * vecs; i += kThreads) {
+                const int n = i / vecs, v = i - n * vecs;
+                put_piece<Nvfp4Vec>(xs + n * I, v,
+                                    reinterpret_cast<const float4*>(ws.h + static_cast<int64_t>(g0 + n) * I)[v]);
+            }
+        };
         if (ng == 1)
-            down_rows<LG, 1>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part);
+            down_rows<LG, 1>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part, stage);
         else if (ng == 2)
-            down_rows<LG, 2>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part);
+            down_rows<LG, 2>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part, stage);
         else if (ng <= 4)
-            down_rows<LG, 4>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part);
+            down_rows<LG, 4>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part, stage);
         else
-            down_rows<LG, 8>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part);
+            down_rows<LG, 8>(codes_e, scales_e, ts, H, I, j_lo, j_hi, xs, slot_of, ng, ws.part, stage);
     }
 }
 

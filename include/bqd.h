@@ -66,11 +66,30 @@ enum {
     BQD_ERR_DEVICE = 8     /* bqd_moe_read_status found device-side error bits */
 };
 
-/* Compute paths of the NVFP4 GEMV (nvfp4_gemv_path). */
+/* Compute paths of the GEMVs (nvfp4_gemv_path, q8_0_gemv_path). */
 enum {
-    BQD_PATH_AUTO = 0,      /* the library's choice for the shape (what nvfp4_gemv uses) */
-    BQD_PATH_CUDA_CORE = 1  /* in-register decode + fp32 FMA on the CUDA cores */
+    BQD_PATH_AUTO = 0,      /* the library's choice for the shape (what nvfp4_gemv / q8_0_gemv use) */
+    BQD_PATH_CUDA_CORE = 1, /* register-prefetch loads, in-register decode, fp32 FMA; any shape */
+    BQD_PATH_STREAM = 2     /* bulk-copy (TMA) stream into a shared-memory ring, decode on the CUDA
+                               cores; N == 1 and K % 256 == 0 (K <= 16384) only, else BQD_ERR_PATH */
 };
+
+/* Launch options (bqd_set_launch_flags). */
+enum {
+    /* Programmatic dependent launch for the streaming GEMV (BQD_PATH_STREAM):
+     * a call may start, and begin reading its WEIGHTS (codes, scales, q, d),
+     * while the previous streaming call in the same stream is still
+     * finishing. Its activations are read, and its output written, only
+     * after that previous call has completed, so chaining layers is safe.
+     * Do not enable it if a call's weights can be written by the kernel
+     * immediately before it in the stream. Off by default. */
+    BQD_LAUNCH_PDL = 1
+};
+
+/* Sets the process-wide launch options (BQD_LAUNCH_* bits); returns the
+ * previous value. Thread-safe; affects calls made after it returns. */
+unsigned int bqd_set_launch_flags(unsigned int flags);
+unsigned int bqd_get_launch_flags(void);
 
 /* Device-side status bits written by moe_grouped_gemv into its workspace. */
 enum {
@@ -104,7 +123,8 @@ const char* bqd_last_cuda_error(void);
 bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x, float* y,
                       int64_t M, int64_t K, int N, cudaStream_t stream);
 
-/* nvfp4_gemv with an explicit compute path (BQD_PATH_*), to compare paths. */
+/* nvfp4_gemv with an explicit compute path (BQD_PATH_*), to compare paths.
+ * AUTO takes BQD_PATH_STREAM where it applies, else BQD_PATH_CUDA_CORE. */
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream);
 
@@ -118,6 +138,19 @@ bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float te
  */
 bqd_status q8_0_gemv(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K, int N,
                      cudaStream_t stream);
+
+/* q8_0_gemv with an explicit compute path (BQD_PATH_*). */
+bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K,
+                          int N, int path, cudaStream_t stream);
+
+/*
+ * bqd_device_error -- waits for the device, copies the device error word of
+ * the streaming kernels to *bits_out and clears it. Bit 0: a shared-memory
+ * pipeline wait ran out (the kernel gave up instead of hanging; its outputs
+ * are unspecified). Returns BQD_ERR_DEVICE if any bit was set. Synchronising:
+ * do not call it inside a stream capture.
+ */
+bqd_status bqd_device_error(unsigned int* bits_out);
 
 /*
  * nvfp4_dequant -- w[m][k] = fl32(e2m1(c[m][k]) * e4m3(s[m][k/16]) * ts),

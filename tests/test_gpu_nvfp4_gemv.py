@@ -7,6 +7,7 @@ import torch
 import oracle
 import block_quantized_decode_nvfp4_gb300 as bqd
 from block_quantized_decode_nvfp4_gb300 import synthetic as syn
+from tests import pins
 from tests.gpu_util import Guarded, assert_within, dev, need_gpu
 
 pytestmark = pytest.mark.gpu
@@ -114,3 +115,111 @@ def test_empty_shapes():
     assert np.all(out.get() == 0)
     bqd.nvfp4_gemv(None, None, 1.0, None, None, 0, 64, 1)  # M == 0: nothing
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- compute paths
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    yield
+    assert bqd.bqd_device_error() == 0, "a pipeline wait ran out"
+
+
+@pytest.mark.parametrize("M,K", syn.NVFP4_SHAPES + [(1, 256), (7, 512), (200, 2304), (3000, 16384)])
+def test_stream_and_cuda_core_paths_match_oracle(M, K):
+    w = syn.dense_nvfp4(M, K, N=1, seed=K + M)
+    ref, a = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], w["x"], M, K)
+    for path in (bqd.BQD_PATH_STREAM, bqd.BQD_PATH_CUDA_CORE):
+        y = run(w, path=path)
+        assert_within(y, ref, a, f"{M}x{K} path {path}")
+
+
+def test_stream_path_rejects_unsupported_shapes():
+    w = syn.dense_nvfp4(8, 4112, N=1, seed=1)
+    with pytest.raises(bqd.BqdError):
+        run(w, path=bqd.BQD_PATH_STREAM)
+    w = syn.dense_nvfp4(8, 1024, N=2, seed=1)
+    with pytest.raises(bqd.BqdError):
+        run(w, path=bqd.BQD_PATH_STREAM)
+
+
+def _bf16(vals):
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("case", ["wide_range", "subnormal", "huge", "tiny", "zeros"])
+def test_stream_activation_range_cases(case):
+    M, K = 300, 4096
+    w = syn.dense_nvfp4(M, K, N=1, seed=77)
+    xf = torch.from_numpy(pins.bf16_lib(w["x"])[0].astype(np.float32))
+    if case == "wide_range":      # 2^40 .. 2^-40: beyond f16's exact range -> exact fp32 path
+        xf[5], xf[100] = 2.0 ** 40, 2.0 ** -40
+    elif case == "subnormal":     # a bf16 subnormal -> exact fp32 path
+        xf[7] = 2.0 ** -130
+    elif case == "huge":          # everything large: f16 path with a large power-of-two prescale
+        xf = xf * 2.0 ** 100
+    elif case == "tiny":          # everything small: f16 path with a large power-of-two upscale
+        xf = xf * 2.0 ** -120
+    elif case == "zeros":
+        xf = xf * 0
+    w["x"] = _bf16(xf.numpy())[None]
+    y = run(w, path=bqd.BQD_PATH_STREAM)
+    ref, a = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], w["x"], M, K)
+    assert_within(y, ref, a, case, absol=0.0 if case != "zeros" else 0.0)
+    if case == "zeros":
+        assert np.all(y == 0)
+
+
+def test_stream_nonfinite_activation_pattern():
+    M, K = 64, 512
+    w = syn.dense_nvfp4(M, K, N=1, seed=78)
+    x = w["x"].copy()
+    x[0, 3] = 0x7F80  # +inf
+    w["x"] = x
+    y = run(w, path=bqd.BQD_PATH_STREAM)
+    ref, _ = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], w["x"], M, K)
+    assert np.array_equal(np.isnan(y[0]), np.isnan(ref[0]))
+    assert np.array_equal(np.isinf(y[0]), np.isinf(ref[0]))
+    fin = np.isfinite(ref[0])
+    assert np.array_equal(np.sign(y[0][~fin & ~np.isnan(ref[0])]), np.sign(ref[0][~fin & ~np.isnan(ref[0])]))
+
+
+# ---------------------------------------------------------------- dependent launch
+@pytest.fixture
+def pdl_on():
+    prev = bqd.set_launch_flags(bqd.BQD_LAUNCH_PDL)
+    yield
+    bqd.set_launch_flags(prev)
+
+
+def test_pdl_chain_is_bit_identical(pdl_on):
+    ws = [syn.dense_nvfp4(M, K, N=1, seed=i) for i, (M, K) in enumerate(syn.NVFP4_SHAPES * 2)]
+    dw = [(dev(w["codes"]), dev(w["scales"]), dev(w["x"])) for w in ws]
+    outs = [torch.empty(w["M"], dtype=torch.float32, device="cuda") for w in ws]
+
+    def chain():
+        for w, (c, s, x), y in zip(ws, dw, outs):
+            bqd.nvfp4_gemv(c, s, w["ts"], x, y, w["M"], w["K"], 1)
+        torch.cuda.synchronize()
+        return [y.cpu().numpy().copy() for y in outs]
+
+    with_pdl = chain()
+    bqd.set_launch_flags(0)
+    without = chain()
+    for a, b in zip(with_pdl, without):
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_pdl_output_may_overwrite_previous_input(pdl_on):
+    # call A reads x_a; call B, launched right after it, writes its output over
+    # x_a's memory: B must not write before A has finished reading
+    K = 8192
+    wa = syn.dense_nvfp4(12288, K, N=1, seed=31)
+    wb = syn.dense_nvfp4(K // 2, 4096, N=1, seed=32)
+    ref_a, a_a = oracle.nvfp4_gemv(wa["codes"], wa["scales"], wa["ts"], wa["x"], 12288, K)
+    for _ in range(3):
+        shared = dev(wa["x"]).view(torch.uint8)  # K bf16 = 2K bytes, later K/2 fp32
+        ya = torch.empty(12288, dtype=torch.float32, device="cuda")
+        bqd.nvfp4_gemv(dev(wa["codes"]), dev(wa["scales"]), wa["ts"], shared, ya, 12288, K, 1)
+        bqd.nvfp4_gemv(dev(wb["codes"]), dev(wb["scales"]), wb["ts"], dev(wb["x"]), shared, K // 2, 4096, 1)
+        torch.cuda.synchronize()
+        assert_within(ya.cpu().numpy()[None], ref_a, a_a, "A under PDL")

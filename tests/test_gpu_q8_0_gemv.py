@@ -100,3 +100,19 @@ def test_empty_shapes():
     bqd.q8_0_gemv(None, None, None, out.ptr, 3, 0, 2)
     assert np.all(out.get() == 0)
     torch.cuda.synchronize()
+
+
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    yield
+    assert bqd.bqd_device_error() == 0, "a pipeline wait ran out"
+
+
+@pytest.mark.parametrize("M,K", syn.Q8_0_SHAPES[:2] + [(1, 256), (33, 768), (500, 16384)])
+def test_stream_and_cuda_core_paths_match_oracle(M, K):
+    w = syn.dense_q8_0(M, K, N=1, seed=M + K)
+    ref, a = oracle.q8_0_gemv(w["q"], w["d"], w["x"], M, K)
+    for path in (bqd.BQD_PATH_STREAM, bqd.BQD_PATH_CUDA_CORE):
+        out = Guarded(M)
+        bqd.q8_0_gemv_path(dev(w["q"]), dev(w["d"]), dev(w["x"]), out.ptr, M, K, 1, path)
+        assert_within(out.get()[None], ref, a, f"{M}x{K} path {path}")
