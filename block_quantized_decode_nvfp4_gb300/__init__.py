@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     bqd_moe_read_status,
     lib,
     moe_grouped_gemv,
+    moe_grouped_gemv_noalloc,
     moe_route_topk,
     moe_workspace_bytes,
     nvfp4_dequant,

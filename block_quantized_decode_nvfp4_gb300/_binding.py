@@ -51,6 +51,7 @@ SIGNATURES = {
     "moe_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32]),
     "moe_grouped_gemv": (_i32, [_vp] * 13 + [_sz, _i32, _i32, _i32, _i32, _i32, _vp]),
     "bqd_moe_read_status": (_i32, [_vp, C.POINTER(C.c_int32), _vp]),
+    "moe_grouped_gemv_noalloc": (_i32, [_vp] * 12 + [_i32, _i32, _i32, _i32, _i32, _vp]),
 }
 
 
@@ -157,6 +158,15 @@ def moe_grouped_gemv(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, 
                                   _ptr(dn_ts), _ptr(x), _ptr(expert_offsets), _ptr(pair_token), _ptr(pair_weight),
                                   _ptr(pair_slot), _ptr(y), _ptr(workspace), workspace_bytes, E, H, I, T, topk,
                                   _stream(stream)), "moe_grouped_gemv")
+
+
+def moe_grouped_gemv_noalloc(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, expert_offsets,
+                             pair_token, pair_weight, pair_slot, y, E, H, I, T, topk, stream=None):
+    """moe_grouped_gemv without a caller workspace (scratch inside the library)."""
+    _check(lib().moe_grouped_gemv_noalloc(_ptr(gu_codes), _ptr(gu_scales), _ptr(gu_ts), _ptr(dn_codes),
+                                          _ptr(dn_scales), _ptr(dn_ts), _ptr(x), _ptr(expert_offsets),
+                                          _ptr(pair_token), _ptr(pair_weight), _ptr(pair_slot), _ptr(y), E, H, I, T,
+                                          topk, _stream(stream)), "moe_grouped_gemv_noalloc")
 
 
 def bqd_moe_read_status(workspace, stream=None) -> int:

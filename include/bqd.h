@@ -209,6 +209,30 @@ bqd_status moe_grouped_gemv(const uint8_t* gu_codes, const uint8_t* gu_scales, c
                             int H, int I, int T, int topk, cudaStream_t stream);
 
 /*
+ * moe_grouped_gemv_noalloc -- moe_grouped_gemv for callers that cannot
+ * allocate device memory (no counterpart on the source pages; it exists for
+ * programs whose host owns every device allocation and gives plug-ins no
+ * allocator, and for loops that must not allocate once running).
+ * Same arguments and results as moe_grouped_gemv, without the workspace:
+ * the scratch is a 4 MiB array inside libbqd.so, held on every GPU that
+ * loads the library until the process exits. Calls whose
+ * moe_workspace_bytes(T, topk, H, I) exceeds 4 MiB return BQD_ERR_WORKSPACE
+ * before touching the GPU. The library allocates nothing on this path.
+ * The first call on each device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Every call shares the one array: calls that may run at the same time on
+ * the GPU (other streams, other threads) race and give unspecified results.
+ * The array keeps the last call's contents; whatever a call needs zeroed it
+ * clears itself. Device-side list checks still run, but their status word
+ * lives in the shared array and is not reported.
+ */
+bqd_status moe_grouped_gemv_noalloc(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
+                                    const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts,
+                                    const uint16_t* x, const int32_t* expert_offsets, const int32_t* pair_token,
+                                    const float* pair_weight, const int32_t* pair_slot, float* y, int E, int H,
+                                    int I, int T, int topk, cudaStream_t stream);
+
+/*
  * bqd_moe_read_status -- waits for `stream`, copies the workspace's status
  * word to *status_out and returns BQD_ERR_DEVICE if it is non-zero, else
  * BQD_OK. Synchronising: do not call it inside a stream capture.
