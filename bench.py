@@ -267,22 +267,32 @@ def cpu_units(rows):
 
 
 def cpu_baseline_sample(units, budget_s):
-    """The same leading fraction of every row's units, sized to ~budget_s."""
-    t0 = time.perf_counter()
-    units[0][1][0][0]()
-    per_unit = max(time.perf_counter() - t0, 1e-4)
-    n_total = sum(len(u) for _, u in units)
-    frac = min(1.0, budget_s / (per_unit * n_total))
+    """The same leading fraction of every row's units, sized to ~budget_s
+    from a timing of each row's first unit (which is part of the sample)."""
     done_b, secs = 0, 0.0
+    cost = []
     for _, u in units:
-        take = max(1, int(math.ceil(len(u) * frac)))
-        for f, nb in u[:take]:
+        f, nb = u[0]
+        t0 = time.perf_counter()
+        f()
+        dt = time.perf_counter() - t0
+        secs += dt
+        done_b += nb
+        cost.append(max(dt, 1e-5))
+    rest = sum(c * (len(u) - 1) for c, (_, u) in zip(cost, units))
+    frac = 0.0 if rest <= 0 else max(0.0, min(1.0, (budget_s - secs) / rest))
+    taken = []
+    for _, u in units:
+        take = 1 + int(math.floor((len(u) - 1) * frac))
+        taken.append(take)
+        for f, nb in u[1:take]:
             t0 = time.perf_counter()
             f()
             secs += time.perf_counter() - t0
             done_b += nb
-    desc = (f"fp64 C oracle on 1 host core: the first {frac:.4f} of every row's work units "
-            f"(GEMV: blocks of 64 weight rows; MoE: routed (token, slot) pairs), at least one per row")
+    desc = (f"fp64 C oracle on 1 host core: the first unit of every row plus the first {frac:.4f} of the "
+            f"remaining work units of every row (GEMV unit: 64 weight rows; MoE unit: one routed (token, slot) "
+            f"pair); {sum(taken)} of {sum(len(u) for _, u in units)} units")
     return done_b, secs, desc
 
 
@@ -483,6 +493,24 @@ def run_ours(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_row(args):
+    """Call one row of the step a few times and nothing else (for ncu)."""
+    import torch
+
+    import block_quantized_decode_nvfp4_gb300 as bqd
+    from block_quantized_decode_nvfp4_gb300 import build as _build
+
+    _build.build()
+    spec = {n: (k, p) for n, k, p in rows_spec()}
+    if args.profile_row not in spec:
+        raise SystemExit(f"unknown row {args.profile_row!r}; rows: {sorted(spec)}")
+    kind, p = spec[args.profile_row]
+    row = Row(args.profile_row, kind, p, host_inputs(kind, p), torch, bqd)
+    for _ in range(args.profile_calls):
+        row.run()
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -491,11 +519,18 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile-row", default=None,
+                    help="only call this row of the step (e.g. 'q8_0 151936x4096 N=1') --profile-calls times, "
+                         "for profilers; prints no JSON line")
+    ap.add_argument("--profile-calls", type=int, default=3)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.profile_row is not None:
+        run_profile_row(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank)
         return
