@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     BQD_PATH_CUDA_CORE,
     BQD_LAUNCH_PDL,
     BQD_PATH_STREAM,
+    BQD_PATH_MMA,
     get_launch_flags,
     set_launch_flags,
     bqd_device_error,

@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "BQD_OK", 1: "BQD_ERR_NULL", 2: "BQD_ERR_SHAPE", 3: "BQD_ERR_
 BQD_PATH_AUTO = 0
 BQD_PATH_CUDA_CORE = 1
 BQD_PATH_STREAM = 2
+BQD_PATH_MMA = 3
 BQD_LAUNCH_PDL = 1
 
 _lib = None

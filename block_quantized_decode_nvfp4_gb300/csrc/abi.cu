@@ -105,14 +105,19 @@ unsigned int bqd_get_launch_flags(void) { return bqd::launch_flags(); }
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream)
 {
-    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM) return BQD_ERR_PATH;
+    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM && path != BQD_PATH_MMA)
+        return BQD_ERR_PATH;
     bqd_status st = check_dense(codes, scales, x, y, M, K, N, 16, true);
     if (st != BQD_OK || M == 0) return st;
     if (path == BQD_PATH_STREAM && !bqd::stream_gemv_supported(M, K, N)) return BQD_ERR_PATH;
+    if (path == BQD_PATH_MMA && !bqd::mma_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if ((st = check_arch()) != BQD_OK) return st;
     if (K == 0) return zero_output(y, M * N, stream);
-    if (path != BQD_PATH_CUDA_CORE && bqd::stream_gemv_supported(M, K, N))
+    const bool use_stream = path == BQD_PATH_STREAM || (path == BQD_PATH_AUTO && bqd::stream_gemv_supported(M, K, N));
+    const bool use_mma = path == BQD_PATH_MMA || (path == BQD_PATH_AUTO && N >= 2 && bqd::mma_gemv_supported(M, K, N));
+    if (use_stream)
         return from_cuda(bqd::launch_nvfp4_gemv_stream(codes, scales, tensor_scale, x, y, M, K, stream));
+    if (use_mma) return from_cuda(bqd::launch_nvfp4_gemv_mma(codes, scales, tensor_scale, x, y, M, K, N, stream));
     return from_cuda(bqd::launch_nvfp4_gemv_cuda_core(codes, scales, tensor_scale, x, y, M, K, N, stream));
 }
 
@@ -147,8 +152,10 @@ bqd_status bqd_device_error(unsigned int* bits_out)
     if (!bits_out) return BQD_ERR_NULL;
     bqd_status st = check_arch();
     if (st != BQD_OK) return st;
-    unsigned int v = 0;
-    if (bqd::read_and_clear_stream_error(&v) != cudaSuccess) return BQD_ERR_LAUNCH;
+    unsigned int v = 0, w = 0;
+    if (bqd::read_and_clear_stream_error(&v) != cudaSuccess || bqd::read_and_clear_mma_error(&w) != cudaSuccess)
+        return BQD_ERR_LAUNCH;
+    v |= w;
     *bits_out = v;
     return v ? BQD_ERR_DEVICE : BQD_OK;
 }

@@ -27,6 +27,12 @@ cudaError_t launch_q8_0_gemv_stream(const int8_t* q, const uint16_t* d, const ui
 // Reads and clears the device error word of the streaming kernels (synchronous).
 cudaError_t read_and_clear_stream_error(unsigned int* out);
 
+// Tensor-core GEMV (gemv_mma.cu): NVFP4, 1 <= N <= 16, K % 256 == 0.
+bool mma_gemv_supported(int64_t M, int64_t K, int N);
+cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                  float* y, int64_t M, int64_t K, int N, cudaStream_t s);
+cudaError_t read_and_clear_mma_error(unsigned int* out);
+
 // MoE (moe.cu). Limits checked by the ABI layer: E <= 1024, topk <= 32,
 // T * topk <= 8192.
 constexpr int kMoeMaxExperts = 1024;

@@ -1,0 +1,720 @@
+// gemv_mma.cu -- tensor-core (tcgen05) GEMV for a few tokens (N <= 16), NVFP4.
+//
+// Y[n][m] = ts * sum_b scale[m][b] * sum_{k in b} e2m1[m][k] * X[n][k]: the
+// multi-token form of the NVFP4 matvec that checks K+1 drafted tokens in one
+// batched target forward ("robertbfuentes7-cloud/bw24" README, NVFP4 (W4)
+// decode path and speculative decoding bullets).
+//
+// Every product is exact: an E2M1 element times its E4M3 block scale has at
+// most 6 significant bits and lies in [2^-10, 2688], so it is an f16 value,
+// and the activations are staged as f16 after an exact power-of-two scaling
+// (or, when their range does not allow that, both operands are bf16, which
+// also holds every such product). The tensor cores accumulate in fp32.
+//
+// Work split. A CTA owns a 128-row tile (the MMA's M) and a contiguous range
+// of k; the k ranges of one tile are the CTAs of a thread-block cluster
+// (up to 8), whose fp32 partial sums are added in rank order through
+// distributed shared memory, so results are deterministic. Roles per CTA:
+//  * warp 0, lane 0: producer. 2-D tensor copies (TMA) bring 128 rows x
+//    256 k of codes (16 KiB, 128-byte swizzle) and their scales (2 KiB) into
+//    a 3-stage shared-memory ring.
+//  * warps 2..5: decoders, one thread per row (TMEM lane). Each decodes 64 k
+//    of its row per step into f16 pairs and writes them to tensor memory
+//    (tcgen05.st), which is the A operand of the MMA: the decoded weights
+//    never pass through shared memory.
+//  * warp 1: allocates 256 TMEM columns; lane 0 issues the MMAs
+//    (M = 128, N = 16, K = 16 each; B = the staged activations in shared
+//    memory) into one fp32 accumulator of 16 columns and frees A slots with
+//    tcgen05.commit.
+// Every wait is bounded; one that runs out sets a bit in the device error
+// word and the kernel runs to its end without waiting again.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemv.h"
+#include "host_util.h"
+#include "stream.cuh"
+
+namespace bqd {
+
+// Device error word of the tensor-core kernel (kErrWaitTimeout).
+__device__ unsigned int g_mma_error = 0;
+
+namespace {
+
+constexpr int kTileM = 128;                   // rows per CTA = MMA M
+constexpr int kNPad = 16;                     // MMA N: tokens padded to 16
+constexpr int kStageK = 256;                  // k per ring stage
+constexpr int kChunkK = 64;                   // k per decode step / A slot
+constexpr int kChunksPerStage = kStageK / kChunkK;
+constexpr int kStages = 3;
+constexpr int kASlots = 7;                    // A slots in TMEM, 32 columns each
+constexpr int kTmemCols = 256;                // D: columns [0, 16); A: [32, 256)
+constexpr int kACol0 = 32;
+constexpr int kDecGroups = 2;                 // decoder groups, taking alternate chunks
+constexpr int kDecWarps = 4 * kDecGroups;     // one warp per TMEM lane quarter per group
+constexpr int kThreads = (2 + kDecWarps) * kWarp;
+constexpr int kCodesStage = kTileM * (kStageK / 2);  // 16 KiB
+constexpr int kScalesStage = kTileM * (kStageK / 16);  // 2 KiB
+constexpr int kStageBytes = kCodesStage + kScalesStage;
+constexpr int kBBytesPerK = kNPad * 2;        // staged activations: 32 bytes per k
+constexpr int kMaxCluster = 8;
+constexpr int kLoadsInFlight = 8;             // activation loads per thread in flight
+// A kernel that allocates tensor memory runs one CTA per SM. Half of TMEM
+// (256 columns) is enough, and leaves room for a CTA of a second launch on
+// another stream: an allocation never waits for a CTA that may itself be
+// waiting on a cluster peer.
+static_assert(4 % kDecGroups == 0, "each decoder group takes the same chunks of every stage");
+constexpr int kSmemLimit = 226 * 1024;  // dynamic part; static shared memory stays below 1 KiB
+
+static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled codes");
+static_assert(kACol0 + kASlots * 32 <= kTmemCols, "TMEM layout");
+static_assert(kASlots >= kDecGroups, "slot bookkeeping");
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major, no swizzle: start address, the
+// byte distance between core matrices (8 rows x 16 bytes) adjacent in k
+// (lbo) and adjacent in rows (sbo), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+
+// D[tmem_d] (+)= A[tmem_a] * B[desc]^T, M = 128, N = 16, K = 16, f16 or bf16
+// operands (as idesc says), fp32 accumulation.
+__device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 columns of this warp's 32 TMEM lanes from 32 registers per thread.
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+        "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// One lane of the (converged) warp; the same lane every time.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+    return pred != 0;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank)
+{
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------------ decode
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h)
+{
+    const float2 f = f16x2_to_float2(h);
+    __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);  // exact: the products fit in bf16
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// 64 consecutive k of one row (32 code bytes c0, c1 and the 4 block scales in
+// s4) to 32 pairs, pair j = elements 2j (low half) and 2j+1, scaled exactly
+// by the block scale; f16 pairs, or bf16 pairs when !F16.
+template <bool F16>
+__device__ __forceinline__ void decode_chunk(const uint4& c0, const uint4& c1, uint32_t s4, uint32_t (&a)[32])
+{
+    const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu), s23 = e4m3x2_to_f16x2(s4 >> 16);
+    const uint32_t sb[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232), __byte_perm(s23, 0, 0x1010),
+                            __byte_perm(s23, 0, 0x3232)};
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // word i = k 8i..8i+7 of the chunk, block i / 2
+        uint32_t h[4];
+        e2m1x8_to_f16x2(w[i], h);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t p = hmul2_bits(h[j], sb[i >> 1]);
+            a[4 * i + j] = F16 ? p : f16x2_to_bf16x2(p);
+        }
+    }
+}
+
+// ------------------------------------------------------------ kernel
+// Dynamic shared memory (1024-byte aligned): ring [kStages][codes 16 KiB |
+// scales 2 KiB], then the activations B: krange/8 groups of [16 tokens][8 k]
+// as f16 (or bf16), 256 bytes per group, which is the K-major core-matrix
+// layout with 256 bytes between k-adjacent and 128 bytes between
+// row-adjacent core matrices. After the last MMA the ring is reused for the
+// fp32 partial sums [16][128].
+__global__ void __launch_bounds__(kThreads, 1)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
+                    const uint16_t* __restrict__ x, float* __restrict__ y, float ts, int M, int K, int N, int ks)
+{
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[kASlots], aempty[kASlots], dfull;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_emax[kNPad], s_emin[kNPad], s_bad[kNPad];
+
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    unsigned char* ring = smem;
+    unsigned char* bsm = smem + kStages * kStageBytes;
+
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int rank = ks > 1 ? static_cast<int>(cluster_rank()) : 0;
+    const int tile = blockIdx.x / ks;
+    const int m0 = tile * kTileM;
+    const int nst_all = K / kStageK;
+    const int st_lo = nst_all * rank / ks, st_hi = nst_all * (rank + 1) / ks;
+    const int nst = st_hi - st_lo;
+    const int k0 = st_lo * kStageK, krange = nst * kStageK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kDecWarps);
+        }
+        for (int s = 0; s < kASlots; ++s) {
+            mbar_init(&afull[s], 4);  // the four warps of the group that owns the chunk
+            mbar_init(&aempty[s], 1);
+        }
+        mbar_init(&dfull, 1);
+        fence_barrier_init();
+    }
+    if (threadIdx.x < kNPad) {
+        s_emax[threadIdx.x] = 0;
+        s_emin[threadIdx.x] = INT_MAX;
+        s_bad[threadIdx.x] = 0;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    pdl_trigger();
+
+    // The first stages need no wait: start the weight stream before staging
+    // the activations.
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&map_codes);
+        prefetch_map(&map_scales);
+        for (int t = 0; t < nst && t < kStages; ++t) {
+            mbar_arrive_expect_tx(&full[t], kStageBytes);
+            tma_load_2d(ring + t * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[t]);
+            tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16), m0,
+                        &full[t]);
+        }
+    }
+
+    // ---- activations, pass 1 (all threads): B = f16(x * 2^4) written while
+    // each token's exponent range is scanned. Each thread keeps one token,
+    // with eight 16-byte loads in flight. The 2^4 prescale is exact for
+    // 2^-21 <= |x| < 2^11; a token outside that window takes pass 2.
+    pdl_wait();  // the activations may come from the previous kernel in the stream
+    const int groups = krange / 8;  // 8 k = one 16-byte piece
+    {
+        const int active = (kThreads / N) * N, gstep = kThreads / N;
+        if (threadIdx.x < active) {
+            const int n = threadIdx.x % N;
+            const uint16_t* xn = x + static_cast<int64_t>(n) * K + k0;
+            int emax = 0, emin = INT_MAX, bad = 0;
+            for (int g0 = threadIdx.x / N; g0 < groups; g0 += kLoadsInFlight * gstep) {
+                uint4 u[kLoadsInFlight];
+#pragma unroll
+                for (int j = 0; j < kLoadsInFlight; ++j) {
+                    const int g = g0 + j * gstep;
+                    u[j] = g < groups ? *reinterpret_cast<const uint4*>(xn + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < kLoadsInFlight; ++j) {
+                    const int g = g0 + j * gstep;
+                    if (g >= groups) break;
+                    const uint32_t wv[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int e2 = 0; e2 < 4; ++e2) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t b = (wv[e2] >> (16 * h)) & 0x7FFFu;
+                            const int e = static_cast<int>(b >> 7);
+                            if (b != 0) {
+                                if (e == 0 || e == 255) bad = 1;  // subnormal, inf or NaN
+                                emax = max(emax, e);
+                                emin = min(emin, e);
+                            }
+                        }
+                        __half2 hv = __floats2half2_rn(bf16_lo(wv[e2]) * 16.f, bf16_hi(wv[e2]) * 16.f);
+                        o[e2] = *reinterpret_cast<uint32_t*>(&hv);
+                    }
+                    *reinterpret_cast<uint4*>(bsm + g * 256 + n * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            if (bad) atomicOr(&s_bad[n], 1);
+            atomicMax(&s_emax[n], emax);
+            atomicMin(&s_emin[n], emin);
+        }
+    }
+    __syncthreads();
+    // Staging mode of the CTA: 0 = f16 with the fixed 2^4 prescale (pass 1
+    // is final); 1 = f16 with a per-token prescale 2^-sexp that puts the
+    // token's largest |x| in [2^14, 2^15), exact when every nonzero |x| of
+    // the token lies within 31 binades of the largest; 2 = bf16 operands.
+    int mode = 0;
+    for (int n = 0; n < N; ++n) {
+        const bool none = s_emin[n] == INT_MAX;
+        if (s_bad[n] || (!none && s_emax[n] - s_emin[n] > 31))
+            mode = 2;
+        else if (!none && (s_emin[n] < 127 - 21 || s_emax[n] > 127 + 10) && mode < 1)
+            mode = 1;
+    }
+    const bool f16 = mode != 2;
+    auto token_sexp = [&](int n) {
+        if (mode == 0) return -4;
+        if (mode == 2 || n >= N || s_emin[n] == INT_MAX) return 0;
+        return s_emax[n] - 127 - 14;
+    };
+    if (mode != 0) {
+        // ---- pass 2 (all threads, only for activations outside the window)
+        for (int i = threadIdx.x; i < groups * N; i += kThreads) {
+            const int n = i % N, g = i / N;
+            uint4 u = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + 8 * g);
+            if (f16) {
+                // 2^-sexp as two exact factors (it can exceed the fp32 range)
+                const int e = -token_sexp(n), e1 = e / 2, e2 = e - e1;
+                const float f1 = __int_as_float((e1 + 127) << 23), f2 = __int_as_float((e2 + 127) << 23);
+                const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    __half2 hv = __floats2half2_rn(bf16_lo(wv[j]) * f1 * f2, bf16_hi(wv[j]) * f1 * f2);
+                    o[j] = *reinterpret_cast<uint32_t*>(&hv);
+                }
+                u = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            *reinterpret_cast<uint4*>(bsm + g * 256 + n * 16) = u;
+        }
+        __syncthreads();
+    }
+    // Tokens N..15 of B are not written: they only feed accumulator
+    // columns that are never read.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // B is read by the tensor cores
+    __syncthreads();
+
+    const int nchunks = nst * kChunksPerStage;  // even
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t slot = 0, phase = 0;
+            for (int t = 0; t < nst; ++t) {
+                if (t >= kStages) {
+                    if (ok) ok = mbar_wait(&empty[slot], phase ^ 1u, &g_mma_error);
+                    mbar_arrive_expect_tx(&full[slot], kStageBytes);
+                    tma_load_2d(ring + slot * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[slot]);
+                    tma_load_2d(ring + slot * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16),
+                                m0, &full[slot]);
+                }
+                if (++slot == kStages) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+            // Every copy has landed before the CTA can exit: the decoders
+            // waited for all of them, and the last wait below covers a
+            // decoder that gave up.
+            if (ok) {
+                const int first = nst > kStages ? nst - kStages : 0;
+                for (int t = first; t < nst && ok; ++t)
+                    ok = mbar_wait(&full[t % kStages], static_cast<uint32_t>((t / kStages) & 1), &g_mma_error);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issue
+        // The whole warp runs the loop on warp-uniform values and one
+        // elected lane issues: about 33 cycles per MMA, against 50+ when a
+        // single lane runs the loop on per-thread values.
+        const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
+        const uint64_t bdesc0 = __shfl_sync(0xFFFFFFFFu, smem_desc(smem_u32(bsm), 256, 128), 0);
+        const uint32_t idesc = __shfl_sync(0xFFFFFFFFu,
+                                           (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) |
+                                               (static_cast<uint32_t>(kNPad >> 3) << 17) |
+                                               (static_cast<uint32_t>(kTileM >> 4) << 24),
+                                           0);
+        bool ok = true;
+        uint32_t slot = 0, phase = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            if (ok) ok = mbar_wait(&afull[slot], phase, &g_mma_error);
+            tc_fence_after();
+            const uint32_t a_col = tm + kACol0 + slot * 32;
+            if (elect_one()) {
+#pragma unroll
+                for (int j = 0; j < kChunkK / 16; ++j) {
+                    // 16 k = two 256-byte groups of B
+                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((c * (kChunkK / 8) + 2 * j) * (256 >> 4));
+                    mma_tmem_a(tm, a_col + 8 * j, bdesc, idesc, (c | j) != 0 ? 1u : 0u);
+                }
+                mma_commit(&aempty[slot]);
+            }
+            __syncwarp();
+            if (++slot == kASlots) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        }
+        if (elect_one()) mma_commit(&dfull);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ decoders
+        // Group g takes chunks g, g + G, g + 2G, ... (G = kDecGroups), so it
+        // reads every stage; the warps of a group cover the four TMEM lane
+        // quarters (one row per thread).
+        const int grp = (warp - 2) / 4;
+        const int q = warp & 3;  // TMEM lane quarter of this warp
+        const int row = q * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        const int swz = row & 7;
+        bool ok = true;
+        uint32_t sslot = 0, sphase = 0;
+        uint32_t aslot = grp, aphase = 0;
+        const unsigned char* st = ring;
+        uint4 srow = make_uint4(0u, 0u, 0u, 0u);
+        // Chunk c (64 k) of this row: shared memory -> decoded pairs in a.
+        auto fetch = [&](int c, uint32_t(&a)[32]) {
+            const int sub = c & (kChunksPerStage - 1);
+            if (sub == grp) {  // the group's first chunk of the stage
+                if (ok) ok = mbar_wait(&full[sslot], sphase, &g_mma_error);
+                st = ring + sslot * kStageBytes;
+                srow = *reinterpret_cast<const uint4*>(st + kCodesStage + row * 16);
+            }
+            const unsigned char* rp = st + row * 128;
+            const uint4 c0 = *reinterpret_cast<const uint4*>(rp + (((2 * sub) ^ swz) << 4));
+            const uint4 c1 = *reinterpret_cast<const uint4*>(rp + (((2 * sub + 1) ^ swz) << 4));
+            const uint32_t s4 = sub == 0 ? srow.x : sub == 1 ? srow.y : sub == 2 ? srow.z : srow.w;
+            if (f16)
+                decode_chunk<true>(c0, c1, s4, a);
+            else
+                decode_chunk<false>(c0, c1, s4, a);
+            if (sub == grp + kChunksPerStage - kDecGroups) {  // the group's last chunk: release the stage
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[sslot]);
+                if (++sslot == kStages) {
+                    sslot = 0;
+                    sphase ^= 1u;
+                }
+            }
+        };
+        // Chunk c (in a) to its TMEM slot c % kASlots; `next` decodes the
+        // group's following chunk while the store drains.
+        auto publish = [&](int c, const uint32_t(&a)[32], auto&& next) {
+            if (ok && c >= kASlots) ok = mbar_wait(&aempty[aslot], aphase ^ 1u, &g_mma_error);
+            tmem_st_x32(tmem + lane_base + kACol0 + aslot * 32, a);
+            next();
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[aslot]);
+            aslot += kDecGroups;
+            if (aslot >= kASlots) {
+                aslot -= kASlots;
+                aphase ^= 1u;
+            }
+        };
+        constexpr int G = kDecGroups;
+        uint32_t a0[32], a1[32];
+        fetch(grp, a0);
+        for (int c = grp; c < nchunks; c += 2 * G) {
+            publish(c, a0, [&] {
+                if (c + G < nchunks) fetch(c + G, a1);
+            });
+            if (c + G < nchunks)
+                publish(c + G, a1, [&] {
+                    if (c + 2 * G < nchunks) fetch(c + 2 * G, a0);
+                });
+        }
+        // ---- epilogue: this row's 16 accumulators
+        if (ok) ok = mbar_wait(&dfull, 0, &g_mma_error);
+        tc_fence_after();
+        uint32_t v[16];
+        tmem_ld_x16(tmem + lane_base, v);
+        if (ks == 1) {
+            if (m0 + row < M) {
+#pragma unroll
+                for (int n = 0; n < kNPad; ++n)
+                    if (n < N)
+                        y[static_cast<int64_t>(n) * M + m0 + row] = ldexpf(__uint_as_float(v[n]), token_sexp(n)) * ts;
+            }
+        } else {
+            float* part = reinterpret_cast<float*>(ring);  // every copy into the ring has been consumed
+#pragma unroll
+            for (int n = 0; n < kNPad; ++n) part[n * kTileM + row] = ldexpf(__uint_as_float(v[n]), token_sexp(n));
+        }
+        tc_fence_before();
+    }
+
+    if (ks > 1) {
+        // ---- cluster reduction in rank order: this CTA writes rows
+        // [128 * rank / ks, 128 * (rank + 1) / ks) of the tile
+        cluster_sync();
+        const float* part = reinterpret_cast<const float*>(ring);
+        const int r_lo = kTileM * rank / ks, r_hi = kTileM * (rank + 1) / ks, nr = r_hi - r_lo;
+        for (int i = threadIdx.x; i < nr * N; i += kThreads) {
+            const int n = i / nr, r = r_lo + i % nr;
+            float pv[kMaxCluster];
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j)
+                pv[j] = j < ks ? ld_cluster_f32(part + n * kTileM + r, static_cast<uint32_t>(j)) : 0.f;
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxCluster; ++j)
+                if (j < ks) s += pv[j];  // rank order
+            if (m0 + r < M) y[static_cast<int64_t>(n) * M + m0 + r] = s * ts;
+        }
+        cluster_sync();  // peers' shared memory stays alive until every read is done
+    } else {
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D map of a row-major byte matrix [rows][cols] read in boxes of
+// box_cols x 128 rows; rows past the end read as zero.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_cols, bool swizzle128)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(kTileM)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t smem_bytes(int stages_per_cta)
+{
+    return 1024 + static_cast<size_t>(kStages) * kStageBytes +
+           static_cast<size_t>(stages_per_cta) * kStageK * kBBytesPerK;
+}
+
+// Clusters of `ks` CTAs that fit on the device at once (cached per device).
+int active_clusters(int dev, int sms, int ks, size_t smem)
+{
+    static std::mutex mu;
+    static int cache[64][kMaxCluster + 1] = {};
+    static size_t cache_smem[64][kMaxCluster + 1] = {};
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 0 && dev < 64 && cache[dev][ks] && cache_smem[dev][ks] == smem) return cache[dev][ks];
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ks * sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(ks);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemv_mma_kernel, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = sms / ks;
+        if (n < 1) n = 1;
+    }
+    if (dev >= 0 && dev < 64) {
+        cache[dev][ks] = n;
+        cache_smem[dev][ks] = smem;
+    }
+    return n;
+}
+
+}  // namespace
+
+bool mma_gemv_supported(int64_t M, int64_t K, int N)
+{
+    if (N < 1 || N > kNPad || M < 1 || M > (int64_t(1) << 30) || K < kStageK || K % kStageK != 0 ||
+        K > (int64_t(1) << 20))
+        return false;
+    const int64_t per_cta = (K / kStageK + kMaxCluster - 1) / kMaxCluster;
+    return smem_bytes(static_cast<int>(per_cta)) <= static_cast<size_t>(kSmemLimit);
+}
+
+cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                  float* y, int64_t M, int64_t K, int N, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const DevInfo di = dev_info(dev);
+    const int limit = di.max_smem_optin < kSmemLimit ? di.max_smem_optin : kSmemLimit;
+    static OccCache occ;
+    blocks_per_sm(occ, reinterpret_cast<const void*>(gemv_mma_kernel), dev, kThreads,
+                  smem_bytes(1));  // sets the shared-memory opt-in
+
+    const int tiles = static_cast<int>((M + kTileM - 1) / kTileM);
+    const int nst_all = static_cast<int>(K / kStageK);
+    // Cluster size: fewest waves x stages per CTA (plus ~2 stages of fixed
+    // cost per wave); ties go to the smaller cluster.
+    int best_ks = 0;
+    int64_t best_cost = INT64_MAX;
+    for (int ks = 1; ks <= kMaxCluster && ks <= nst_all; ++ks) {
+        const int per_cta = (nst_all + ks - 1) / ks;
+        const size_t smem = smem_bytes(per_cta);
+        if (smem > static_cast<size_t>(limit)) continue;
+        const int act = active_clusters(dev, di.sms, ks, smem);
+        const int64_t waves = (tiles + act - 1) / act;
+        const int64_t cost = waves * (per_cta + 2);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best_ks = ks;
+        }
+    }
+    if (best_ks == 0) return cudaErrorInvalidValue;
+    const int ks = best_ks;
+    const size_t smem = smem_bytes((nst_all + ks - 1) / ks);
+
+    CUtensorMap map_codes, map_scales;
+    if (!make_map(&map_codes, codes, M, K / 2, kStageK / 2, true) ||
+        !make_map(&map_scales, scales, M, K / 16, kStageK / 16, false))
+        return cudaErrorInvalidValue;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * ks));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (ks > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = static_cast<unsigned>(ks);
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (launch_flags() & kLaunchPdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, gemv_mma_kernel, map_codes, map_scales, x, y, ts, static_cast<int>(M),
+                              static_cast<int>(K), N, ks);
+}
+
+cudaError_t read_and_clear_mma_error(unsigned int* out)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_mma_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    *out = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_mma_error, &zero, sizeof(zero));
+    }
+    return e;
+}
+
+}  // namespace bqd

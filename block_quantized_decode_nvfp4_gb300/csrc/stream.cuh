@@ -11,8 +11,9 @@ namespace bqd {
 
 // Error bit set in a kernel's device error word when a wait runs out.
 constexpr unsigned int kErrWaitTimeout = 1u;
-// ~2^22 polls with backoff: far beyond any legitimate wait (microseconds).
-constexpr int kWaitPolls = 1 << 22;
+// 2^31 SM cycles (about one second): far beyond any legitimate wait
+// (microseconds), short enough to give the GPU back.
+constexpr long long kWaitCycles = 1ll << 31;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
@@ -55,13 +56,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 }
 
 // Bounded wait for the phase with the given parity; false if it ran out,
-// after setting kErrWaitTimeout in *err.
+// after setting kErrWaitTimeout in *err. try_wait itself suspends the thread
+// until the phase completes or a short hardware time limit passes, so the
+// loop needs no sleep of its own (a sleep only delays the wake-up).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err)
 {
-    for (int i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    do {
         if (mbar_try_wait(bar, parity)) return true;
-        if (i > 16) __nanosleep(64);
-    }
+    } while (clock64() - t0 < kWaitCycles);
     atomicOr(err, kErrWaitTimeout);
     return false;
 }

@@ -70,8 +70,13 @@ enum {
 enum {
     BQD_PATH_AUTO = 0,      /* the library's choice for the shape (what nvfp4_gemv / q8_0_gemv use) */
     BQD_PATH_CUDA_CORE = 1, /* register-prefetch loads, in-register decode, fp32 FMA; any shape */
-    BQD_PATH_STREAM = 2     /* bulk-copy (TMA) stream into a shared-memory ring, decode on the CUDA
+    BQD_PATH_STREAM = 2,    /* bulk-copy (TMA) stream into a shared-memory ring, decode on the CUDA
                                cores; N == 1 and K % 256 == 0 (K <= 16384) only, else BQD_ERR_PATH */
+    BQD_PATH_MMA = 3        /* NVFP4 only: weights decoded exactly to f16 (or bf16) in tensor memory and
+                               multiplied on the tensor cores (tcgen05.mma, fp32 accumulation), k split
+                               over a thread-block cluster with a fixed-order sum; 1 <= N <= 16,
+                               K % 256 == 0, M < 2^30, K <= 2^20 (smaller if shared memory runs
+                               short), else BQD_ERR_PATH. q8_0_gemv_path returns BQD_ERR_PATH */
 };
 
 /* Launch options (bqd_set_launch_flags). */
@@ -124,7 +129,8 @@ bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_
                       int64_t M, int64_t K, int N, cudaStream_t stream);
 
 /* nvfp4_gemv with an explicit compute path (BQD_PATH_*), to compare paths.
- * AUTO takes BQD_PATH_STREAM where it applies, else BQD_PATH_CUDA_CORE. */
+ * AUTO takes BQD_PATH_STREAM for N == 1 and BQD_PATH_MMA for N >= 2 where
+ * they apply, else BQD_PATH_CUDA_CORE. */
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream);
 
@@ -144,11 +150,12 @@ bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x,
                           int N, int path, cudaStream_t stream);
 
 /*
- * bqd_device_error -- waits for the device, copies the device error word of
- * the streaming kernels to *bits_out and clears it. Bit 0: a shared-memory
- * pipeline wait ran out (the kernel gave up instead of hanging; its outputs
- * are unspecified). Returns BQD_ERR_DEVICE if any bit was set. Synchronising:
- * do not call it inside a stream capture.
+ * bqd_device_error -- waits for the device, copies the device error words of
+ * the streaming and tensor-core kernels (BQD_PATH_STREAM, BQD_PATH_MMA) to
+ * *bits_out (OR of the two) and clears them. Bit 0: a pipeline wait ran out
+ * (the kernel gave up instead of hanging; its outputs are unspecified).
+ * Returns BQD_ERR_DEVICE if any bit was set. Synchronising: do not call it
+ * inside a stream capture.
  */
 bqd_status bqd_device_error(unsigned int* bits_out);
 
