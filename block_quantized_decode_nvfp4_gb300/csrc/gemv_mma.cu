@@ -54,24 +54,24 @@ constexpr int kNPad = 16;                     // MMA N: tokens padded to 16
 constexpr int kStageK = 256;                  // k per ring stage
 constexpr int kChunkK = 64;                   // k per decode step / A slot
 constexpr int kChunksPerStage = kStageK / kChunkK;
-constexpr int kStages = 3;
-constexpr int kASlots = 7;                    // A slots in TMEM, 32 columns each
-constexpr int kTmemCols = 256;                // D: columns [0, 16); A: [32, 256)
+constexpr int kMaxStages = 8;                 // ring stages: as many as shared memory allows, 3..8
+constexpr int kASlots = 15;                   // A slots in TMEM, 32 columns each
+constexpr int kTmemCols = 512;                // D: columns [0, 16); A: [32, 512)
 constexpr int kACol0 = 32;
-constexpr int kDecGroups = 2;                 // decoder groups, taking alternate chunks
+constexpr int kDecGroups = 4;                 // decoder groups: group g takes chunk g of every stage
 constexpr int kDecWarps = 4 * kDecGroups;     // one warp per TMEM lane quarter per group
 constexpr int kThreads = (2 + kDecWarps) * kWarp;
 constexpr int kCodesStage = kTileM * (kStageK / 2);  // 16 KiB
 constexpr int kScalesStage = kTileM * (kStageK / 16);  // 2 KiB
 constexpr int kStageBytes = kCodesStage + kScalesStage;
-constexpr int kBBytesPerK = kNPad * 2;        // staged activations: 32 bytes per k
 constexpr int kMaxCluster = 8;
 constexpr int kLoadsInFlight = 8;             // activation loads per thread in flight
-// A kernel that allocates tensor memory runs one CTA per SM. Half of TMEM
-// (256 columns) is enough, and leaves room for a CTA of a second launch on
-// another stream: an allocation never waits for a CTA that may itself be
-// waiting on a cluster peer.
-static_assert(4 % kDecGroups == 0, "each decoder group takes the same chunks of every stage");
+// The CTA takes all of TMEM (512 columns). At least 116 KiB of shared
+// memory per CTA keeps two CTAs of this kernel (from any launches, on any
+// streams) off the same SM, so a TMEM allocation here never waits for a CTA
+// that may itself be waiting on a cluster peer.
+constexpr int kMinSmem = 116 * 1024;
+static_assert(kDecGroups == kChunksPerStage, "one chunk of every stage per decoder group");
 constexpr int kSmemLimit = 226 * 1024;  // dynamic part; static shared memory stays below 1 KiB
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled codes");
@@ -211,25 +211,29 @@ __device__ __forceinline__ void decode_chunk(const uint4& c0, const uint4& c1, u
 }
 
 // ------------------------------------------------------------ kernel
-// Dynamic shared memory (1024-byte aligned): ring [kStages][codes 16 KiB |
-// scales 2 KiB], then the activations B: krange/8 groups of [16 tokens][8 k]
-// as f16 (or bf16), 256 bytes per group, which is the K-major core-matrix
-// layout with 256 bytes between k-adjacent and 128 bytes between
-// row-adjacent core matrices. After the last MMA the ring is reused for the
-// fp32 partial sums [16][128].
+// Dynamic shared memory (1024-byte aligned): ring [ns][codes 16 KiB |
+// scales 2 KiB], then the activations B: krange/8 groups of [brows tokens]
+// [8 k] as f16 (or bf16), brows * 16 bytes per group: the K-major core-matrix
+// layout with brows * 16 bytes between k-adjacent core matrices. With
+// brows = 16 the second 8-token core matrix follows at +128 bytes; with
+// brows = 8 (N <= 8) the descriptor's row-group stride is 0, so MMA columns
+// 8..15 repeat columns 0..7 and are never read. After the last MMA the ring
+// is reused for the fp32 partial sums [16][128].
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
-                    const uint16_t* __restrict__ x, float* __restrict__ y, float ts, int M, int K, int N, int ks)
+                    const uint16_t* __restrict__ x, float* __restrict__ y, float ts, int M, int K, int N, int ks, int ns,
+                    int brows)
 {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[kASlots], aempty[kASlots], dfull;
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], afull[kASlots], aempty[kASlots], dfull;
     __shared__ uint32_t s_tmem;
     __shared__ int s_emax[kNPad], s_emin[kNPad], s_bad[kNPad];
 
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     unsigned char* ring = smem;
-    unsigned char* bsm = smem + kStages * kStageBytes;
+    unsigned char* bsm = smem + ns * kStageBytes;
+    const int gbytes = brows * 16;  // bytes of B per 8 k
 
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int rank = ks > 1 ? static_cast<int>(cluster_rank()) : 0;
@@ -241,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k0 = st_lo * kStageK, krange = nst * kStageK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < ns; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kDecWarps);
         }
@@ -269,18 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     pdl_trigger();
 
-    // The first stages need no wait: start the weight stream before staging
-    // the activations.
-    if (warp == 0 && lane == 0) {
-        prefetch_map(&map_codes);
-        prefetch_map(&map_scales);
-        for (int t = 0; t < nst && t < kStages; ++t) {
-            mbar_arrive_expect_tx(&full[t], kStageBytes);
-            tma_load_2d(ring + t * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[t]);
-            tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16), m0,
-                        &full[t]);
+    // The first ns stages need no wait; they are issued right after this
+    // thread's first activation loads (so those are not queued behind them).
+    auto start_weight_stream = [&] {
+        if (warp == 0 && lane == 0) {
+            prefetch_map(&map_codes);
+            prefetch_map(&map_scales);
+            for (int t = 0; t < nst && t < ns; ++t) {
+                mbar_arrive_expect_tx(&full[t], kStageBytes);
+                tma_load_2d(ring + t * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[t]);
+                tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16), m0,
+                            &full[t]);
+            }
         }
-    }
+    };
 
     // ---- activations, pass 1 (all threads): B = f16(x * 2^4) written while
     // each token's exponent range is scanned. Each thread keeps one token,
@@ -290,6 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int groups = krange / 8;  // 8 k = one 16-byte piece
     {
         const int active = (kThreads / N) * N, gstep = kThreads / N;
+        // Every CTA reads the same activations: each starts at its own place
+        // so that the CTAs do not all ask for the same lines at once.
+        const int rot = static_cast<int>((blockIdx.x * 97u) % static_cast<unsigned>(groups));
         if (threadIdx.x < active) {
             const int n = threadIdx.x % N;
             const uint16_t* xn = x + static_cast<int64_t>(n) * K + k0;
@@ -298,13 +307,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint4 u[kLoadsInFlight];
 #pragma unroll
                 for (int j = 0; j < kLoadsInFlight; ++j) {
-                    const int g = g0 + j * gstep;
-                    u[j] = g < groups ? *reinterpret_cast<const uint4*>(xn + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
+                    int g = g0 + j * gstep + rot;
+                    if (g >= groups) g -= groups;
+                    u[j] = g0 + j * gstep < groups ? *reinterpret_cast<const uint4*>(xn + 8 * g)
+                                                   : make_uint4(0u, 0u, 0u, 0u);
                 }
+                if (g0 == static_cast<int>(threadIdx.x) / N) start_weight_stream();  // thread 0: first round
 #pragma unroll
                 for (int j = 0; j < kLoadsInFlight; ++j) {
-                    const int g = g0 + j * gstep;
-                    if (g >= groups) break;
+                    if (g0 + j * gstep >= groups) break;
+                    int g = g0 + j * gstep + rot;
+                    if (g >= groups) g -= groups;
                     const uint32_t wv[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
                     uint32_t o[4];
 #pragma unroll
@@ -322,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __half2 hv = __floats2half2_rn(bf16_lo(wv[e2]) * 16.f, bf16_hi(wv[e2]) * 16.f);
                         o[e2] = *reinterpret_cast<uint32_t*>(&hv);
                     }
-                    *reinterpret_cast<uint4*>(bsm + g * 256 + n * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(bsm + g * gbytes + n * 16) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
             if (bad) atomicOr(&s_bad[n], 1);
@@ -367,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 u = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            *reinterpret_cast<uint4*>(bsm + g * 256 + n * 16) = u;
+            *reinterpret_cast<uint4*>(bsm + g * gbytes + n * 16) = u;
         }
         __syncthreads();
     }
@@ -383,14 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             uint32_t slot = 0, phase = 0;
             for (int t = 0; t < nst; ++t) {
-                if (t >= kStages) {
+                if (t >= ns) {
                     if (ok) ok = mbar_wait(&empty[slot], phase ^ 1u, &g_mma_error);
                     mbar_arrive_expect_tx(&full[slot], kStageBytes);
                     tma_load_2d(ring + slot * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[slot]);
                     tma_load_2d(ring + slot * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16),
                                 m0, &full[slot]);
                 }
-                if (++slot == kStages) {
+                if (++slot == ns) {
                     slot = 0;
                     phase ^= 1u;
                 }
@@ -399,9 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // waited for all of them, and the last wait below covers a
             // decoder that gave up.
             if (ok) {
-                const int first = nst > kStages ? nst - kStages : 0;
+                const int first = nst > ns ? nst - ns : 0;
                 for (int t = first; t < nst && ok; ++t)
-                    ok = mbar_wait(&full[t % kStages], static_cast<uint32_t>((t / kStages) & 1), &g_mma_error);
+                    ok = mbar_wait(&full[t % ns], static_cast<uint32_t>((t / ns) & 1), &g_mma_error);
             }
         }
     } else if (warp == 1) {
@@ -410,30 +423,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         // elected lane issues: about 33 cycles per MMA, against 50+ when a
         // single lane runs the loop on per-thread values.
         const uint32_t tm = __shfl_sync(0xFFFFFFFFu, tmem, 0);
-        const uint64_t bdesc0 = __shfl_sync(0xFFFFFFFFu, smem_desc(smem_u32(bsm), 256, 128), 0);
+        const uint64_t bdesc0 =
+            __shfl_sync(0xFFFFFFFFu, smem_desc(smem_u32(bsm), gbytes, brows == 16 ? 128 : 0), 0);
+        const uint32_t bstep = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(gbytes >> 4), 0);  // per 8 k
         const uint32_t idesc = __shfl_sync(0xFFFFFFFFu,
                                            (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) |
                                                (static_cast<uint32_t>(kNPad >> 3) << 17) |
                                                (static_cast<uint32_t>(kTileM >> 4) << 24),
                                            0);
+        // Chunks go in fours (nchunks is a multiple of 4): lanes 0..3 wait
+        // for the four chunks' A slots with one instruction, so each barrier
+        // round trip (~150 cycles) is paid once per 16 MMAs and overlaps the
+        // previous batch's work.
+        constexpr int kBatch = 4;
+        static_assert(kASlots >= 2 * kBatch, "decoders must be able to run a batch ahead");
         bool ok = true;
         uint32_t slot = 0, phase = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            if (ok) ok = mbar_wait(&afull[slot], phase, &g_mma_error);
+        for (int c = 0; c < nchunks; c += kBatch) {
+            uint32_t ws = slot + (lane & (kBatch - 1)), wp = phase;
+            if (ws >= kASlots) {
+                ws -= kASlots;
+                wp ^= 1u;
+            }
+            if (ok && lane < kBatch) ok = mbar_wait(&afull[ws], wp, &g_mma_error);
+            __syncwarp();
             tc_fence_after();
-            const uint32_t a_col = tm + kACol0 + slot * 32;
             if (elect_one()) {
 #pragma unroll
-                for (int j = 0; j < kChunkK / 16; ++j) {
-                    // 16 k = two 256-byte groups of B
-                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>((c * (kChunkK / 8) + 2 * j) * (256 >> 4));
-                    mma_tmem_a(tm, a_col + 8 * j, bdesc, idesc, (c | j) != 0 ? 1u : 0u);
+                for (int h = 0; h < kBatch; ++h) {
+                    uint32_t sl = slot + h;
+                    if (sl >= kASlots) sl -= kASlots;
+                    const uint32_t a_col = tm + kACol0 + sl * 32;
+#pragma unroll
+                    for (int j = 0; j < kChunkK / 16; ++j) {
+                        // 16 k = two groups of B
+                        const uint64_t bdesc =
+                            bdesc0 + static_cast<uint64_t>(((c + h) * (kChunkK / 8) + 2 * j) * bstep);
+                        mma_tmem_a(tm, a_col + 8 * j, bdesc, idesc, ((c + h) | j) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&aempty[sl]);
                 }
-                mma_commit(&aempty[slot]);
             }
             __syncwarp();
-            if (++slot == kASlots) {
-                slot = 0;
+            slot += kBatch;
+            if (slot >= kASlots) {
+                slot -= kASlots;
                 phase ^= 1u;
             }
         }
@@ -441,9 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------ decoders
-        // Group g takes chunks g, g + G, g + 2G, ... (G = kDecGroups), so it
-        // reads every stage; the warps of a group cover the four TMEM lane
-        // quarters (one row per thread).
+        // Group g decodes chunk g (k 64g .. 64g+63) of every stage; the four
+        // warps of a group cover the four TMEM lane quarters (one row per
+        // thread). Four warps per scheduler hide each other's latencies.
         const int grp = (warp - 2) / 4;
         const int q = warp & 3;  // TMEM lane quarter of this warp
         const int row = q * 32 + lane;
@@ -452,63 +486,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         uint32_t sslot = 0, sphase = 0;
         uint32_t aslot = grp, aphase = 0;
-        const unsigned char* st = ring;
-        uint4 srow = make_uint4(0u, 0u, 0u, 0u);
-        // Chunk c (64 k) of this row: shared memory -> decoded pairs in a.
-        auto fetch = [&](int c, uint32_t(&a)[32]) {
-            const int sub = c & (kChunksPerStage - 1);
-            if (sub == grp) {  // the group's first chunk of the stage
-                if (ok) ok = mbar_wait(&full[sslot], sphase, &g_mma_error);
-                st = ring + sslot * kStageBytes;
-                srow = *reinterpret_cast<const uint4*>(st + kCodesStage + row * 16);
-            }
+        for (int t = 0; t < nst; ++t) {
+            const int c = t * kChunksPerStage + grp;
+            if (ok) ok = mbar_wait_warp(&full[sslot], sphase, &g_mma_error);
+            const unsigned char* st = ring + sslot * kStageBytes;
+            const uint4 srow = *reinterpret_cast<const uint4*>(st + kCodesStage + row * 16);
             const unsigned char* rp = st + row * 128;
-            const uint4 c0 = *reinterpret_cast<const uint4*>(rp + (((2 * sub) ^ swz) << 4));
-            const uint4 c1 = *reinterpret_cast<const uint4*>(rp + (((2 * sub + 1) ^ swz) << 4));
-            const uint32_t s4 = sub == 0 ? srow.x : sub == 1 ? srow.y : sub == 2 ? srow.z : srow.w;
+            const uint4 c0 = *reinterpret_cast<const uint4*>(rp + (((2 * grp) ^ swz) << 4));
+            const uint4 c1 = *reinterpret_cast<const uint4*>(rp + (((2 * grp + 1) ^ swz) << 4));
+            const uint32_t s4 = grp == 0 ? srow.x : grp == 1 ? srow.y : grp == 2 ? srow.z : srow.w;
+            uint32_t a[32];
             if (f16)
                 decode_chunk<true>(c0, c1, s4, a);
             else
                 decode_chunk<false>(c0, c1, s4, a);
-            if (sub == grp + kChunksPerStage - kDecGroups) {  // the group's last chunk: release the stage
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[sslot]);
-                if (++sslot == kStages) {
-                    sslot = 0;
-                    sphase ^= 1u;
-                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[sslot]);  // this warp no longer reads the stage
+            if (++sslot == ns) {
+                sslot = 0;
+                sphase ^= 1u;
             }
-        };
-        // Chunk c (in a) to its TMEM slot c % kASlots; `next` decodes the
-        // group's following chunk while the store drains.
-        auto publish = [&](int c, const uint32_t(&a)[32], auto&& next) {
-            if (ok && c >= kASlots) ok = mbar_wait(&aempty[aslot], aphase ^ 1u, &g_mma_error);
+            if (ok && c >= kASlots) ok = mbar_wait_warp(&aempty[aslot], aphase ^ 1u, &g_mma_error);
             tmem_st_x32(tmem + lane_base + kACol0 + aslot * 32, a);
-            next();
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[aslot]);
-            aslot += kDecGroups;
+            aslot += kDecGroups;  // chunk c + kDecGroups
             if (aslot >= kASlots) {
                 aslot -= kASlots;
                 aphase ^= 1u;
             }
-        };
-        constexpr int G = kDecGroups;
-        uint32_t a0[32], a1[32];
-        fetch(grp, a0);
-        for (int c = grp; c < nchunks; c += 2 * G) {
-            publish(c, a0, [&] {
-                if (c + G < nchunks) fetch(c + G, a1);
-            });
-            if (c + G < nchunks)
-                publish(c + G, a1, [&] {
-                    if (c + 2 * G < nchunks) fetch(c + 2 * G, a0);
-                });
         }
         // ---- epilogue: this row's 16 accumulators
-        if (ok) ok = mbar_wait(&dfull, 0, &g_mma_error);
+        if (ok) ok = mbar_wait_warp(&dfull, 0, &g_mma_error);
         tc_fence_after();
         uint32_t v[16];
         tmem_ld_x16(tmem + lane_base, v);
@@ -591,10 +602,13 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t smem_bytes(int stages_per_cta)
+// Shared memory of a CTA with `stages_per_cta` stages of k, B rows of
+// `brows` tokens and a ring of `ns` stages.
+size_t smem_bytes(int stages_per_cta, int brows, int ns)
 {
-    return 1024 + static_cast<size_t>(kStages) * kStageBytes +
-           static_cast<size_t>(stages_per_cta) * kStageK * kBBytesPerK;
+    const size_t s =
+        1024 + static_cast<size_t>(ns) * kStageBytes + static_cast<size_t>(stages_per_cta) * kStageK * brows * 2;
+    return s < static_cast<size_t>(kMinSmem) ? static_cast<size_t>(kMinSmem) : s;
 }
 
 // Clusters of `ks` CTAs that fit on the device at once (cached per device).
@@ -637,7 +651,7 @@ bool mma_gemv_supported(int64_t M, int64_t K, int N)
         K > (int64_t(1) << 20))
         return false;
     const int64_t per_cta = (K / kStageK + kMaxCluster - 1) / kMaxCluster;
-    return smem_bytes(static_cast<int>(per_cta)) <= static_cast<size_t>(kSmemLimit);
+    return smem_bytes(static_cast<int>(per_cta), N <= 8 ? 8 : 16, 3) <= static_cast<size_t>(kSmemLimit);
 }
 
 cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
@@ -650,17 +664,18 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
     const int limit = di.max_smem_optin < kSmemLimit ? di.max_smem_optin : kSmemLimit;
     static OccCache occ;
     blocks_per_sm(occ, reinterpret_cast<const void*>(gemv_mma_kernel), dev, kThreads,
-                  smem_bytes(1));  // sets the shared-memory opt-in
+                  smem_bytes(1, 8, 3));  // sets the shared-memory opt-in
 
     const int tiles = static_cast<int>((M + kTileM - 1) / kTileM);
     const int nst_all = static_cast<int>(K / kStageK);
+    const int brows = N <= 8 ? 8 : 16;
     // Cluster size: fewest waves x stages per CTA (plus ~2 stages of fixed
     // cost per wave); ties go to the smaller cluster.
     int best_ks = 0;
     int64_t best_cost = INT64_MAX;
     for (int ks = 1; ks <= kMaxCluster && ks <= nst_all; ++ks) {
         const int per_cta = (nst_all + ks - 1) / ks;
-        const size_t smem = smem_bytes(per_cta);
+        const size_t smem = smem_bytes(per_cta, brows, 3);
         if (smem > static_cast<size_t>(limit)) continue;
         const int act = active_clusters(dev, di.sms, ks, smem);
         const int64_t waves = (tiles + act - 1) / act;
@@ -672,7 +687,13 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
     }
     if (best_ks == 0) return cudaErrorInvalidValue;
     const int ks = best_ks;
-    const size_t smem = smem_bytes((nst_all + ks - 1) / ks);
+    const int per_cta = (nst_all + ks - 1) / ks;
+    // Ring: as many stages as shared memory holds (up to 8, no more than the
+    // CTA's stages); at least 3 fit by the choice of ks.
+    int ns = static_cast<int>((limit - 1024 - static_cast<int64_t>(per_cta) * kStageK * brows * 2) / kStageBytes);
+    if (ns > kMaxStages) ns = kMaxStages;
+    if (ns > per_cta) ns = per_cta;
+    const size_t smem = smem_bytes(per_cta, brows, ns);
 
     CUtensorMap map_codes, map_scales;
     if (!make_map(&map_codes, codes, M, K / 2, kStageK / 2, true) ||
@@ -701,7 +722,7 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
     cfg.attrs = attr;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, gemv_mma_kernel, map_codes, map_scales, x, y, ts, static_cast<int>(M),
-                              static_cast<int>(K), N, ks);
+                              static_cast<int>(K), N, ks, ns, brows);
 }
 
 cudaError_t read_and_clear_mma_error(unsigned int* out)

@@ -70,6 +70,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     return false;
 }
 
+// The same wait for a whole (converged) warp: lane 0 polls, the other lanes
+// wait at the warp barrier, which also orders their later memory accesses
+// after lane 0's acquire. Keeps polling traffic to one thread per warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned int* err)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, err);
+    __syncwarp();
+    return __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+}
+
 // 1-D bulk copy global -> shared of `bytes` (multiple of 16, both addresses
 // 16-byte aligned); completion is counted on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
