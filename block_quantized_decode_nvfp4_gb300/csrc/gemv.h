@@ -52,6 +52,16 @@ struct MoeWorkspace {
 size_t moe_workspace_size(int T, int topk, int H, int I);
 MoeWorkspace moe_workspace_carve(void* base, int T, int topk, int H, int I);
 
+// Streaming gate_up and down kernels (moe_stream.cu) for H % 256 == 0 and
+// I % 256 == 0; the combine kernel of moe.cu runs after them.
+bool moe_stream_supported(int E, int H, int I);
+cudaError_t launch_moe_stream_layer(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
+                                    const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts,
+                                    const uint16_t* x, const int32_t* offsets, const int32_t* pair_token,
+                                    const float* pair_weight, const int32_t* pair_slot, const MoeWorkspace& ws, int E,
+                                    int H, int I, int T, int topk, cudaStream_t stream);
+cudaError_t read_and_clear_moe_stream_error(unsigned int* out);
+
 cudaError_t launch_moe_grouped(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
                                const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts,
                                const uint16_t* x, const int32_t* offsets, const int32_t* pair_token,

@@ -569,6 +569,15 @@ cudaError_t launch_moe_grouped(const uint8_t* gu_codes, const uint8_t* gu_scales
     const int max_active = P < E ? P : E;
     err = cudaMemsetAsync(ws.status, 0, sizeof(int32_t), s);
     if (err != cudaSuccess) return err;
+    const dim3 grid_c((H + kThreads - 1) / kThreads, T);
+
+    if (moe_stream_supported(E, H, I)) {
+        err = launch_moe_stream_layer(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, offsets, pair_token,
+                                      pair_weight, pair_slot, ws, E, H, I, T, topk, s);
+        if (err != cudaSuccess) return err;
+        moe_combine_kernel<<<grid_c, kThreads, 0, s>>>(ws, y, H, topk);
+        return cudaGetLastError();
+    }
 
     // gate_up: one CTA per (active expert, slice of its I row pairs)
     int gy = (2 * sms + max_active - 1) / max_active;
@@ -601,7 +610,6 @@ cudaError_t launch_moe_grouped(const uint8_t* gu_codes, const uint8_t* gu_scales
 #undef BQD_DN
     if (err != cudaSuccess) return err;
 
-    const dim3 grid_c((H + kThreads - 1) / kThreads, T);
     moe_combine_kernel<<<grid_c, kThreads, 0, s>>>(ws, y, H, topk);
     return cudaGetLastError();
 }

@@ -120,8 +120,10 @@ def test_moe_layer_full_size(T):
     assert_within(y, yref, tol_y, f"MoE y T={T}", rel=1.0, absol=0.0)
 
 
-def test_moe_deterministic_and_identical_experts():
-    L = syn.moe_layer(T=4, E=32, H=512, I=128, topk=4, seed=3)
+# I = 128 takes the register-streaming kernels, I = 256 the bulk-copy ones
+@pytest.mark.parametrize("I", [128, 256])
+def test_moe_deterministic_and_identical_experts(I):
+    L = syn.moe_layer(T=4, E=32, H=512, I=I, topk=4, seed=3)
     y1, _, _ = _layer_run(L)
     y2, _, _ = _layer_run(L)
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
@@ -135,19 +137,21 @@ def test_moe_deterministic_and_identical_experts():
     assert_within(y, yref, 3 * scale + 1e-5, "identical experts", rel=1e-3, absol=0.0)
 
 
-def test_moe_small_shapes_and_many_tokens_per_expert():
+@pytest.mark.parametrize("I", [64, 256])
+def test_moe_small_shapes_and_many_tokens_per_expert(I):
     # few experts, many tokens: token groups of 8 and more per expert
-    L = syn.moe_layer(T=40, E=4, H=256, I=64, topk=2, seed=4)
+    L = syn.moe_layer(T=40, E=4, H=256, I=I, topk=2, seed=4)
     y, _, _ = _layer_run(L)
     yref, parts = oracle.moe_layer(L, want_parts=True)
     sel, w = oracle.moe_route(L["logits"], 2)
     scale = np.einsum("ts,tsh->th", w, parts["ad"])
-    assert_within(y, yref, 3 * scale + 1e-5, "T=40 E=4", rel=1e-3, absol=0.0)
+    assert_within(y, yref, 3 * scale + 1e-5, f"T=40 E=4 I={I}", rel=1e-3, absol=0.0)
 
 
-def test_moe_malformed_list_sets_status_without_faulting():
-    L = syn.moe_layer(T=2, E=8, H=128, I=64, topk=2, seed=5)
-    T, E, H, I, topk = 2, 8, 128, 64, 2
+@pytest.mark.parametrize("H,I", [(128, 64), (256, 256)])
+def test_moe_malformed_list_sets_status_without_faulting(H, I):
+    L = syn.moe_layer(T=2, E=8, H=H, I=I, topk=2, seed=5)
+    T, E, topk = 2, 8, 2
     off, ptok, pw, pslot = route(L["logits"], topk)
     wsb = bqd.moe_workspace_bytes(T, topk, H, I)
     ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
