@@ -219,6 +219,11 @@ class Row:
             self.in_bytes = self.x.numel() * 2 + self.logits.numel() * 4
         self.out_bytes = self.y.numel() * 4
 
+    def run_path(self, path):
+        """The NVFP4 GEMV of this row through an explicit compute path."""
+        p = self.p
+        self.bqd.nvfp4_gemv_path(self.w[0], self.w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"], path)
+
     def run(self):
         p, b = self.p, self.bqd
         if self.kind == "nvfp4":
@@ -371,20 +376,29 @@ def run_ours(args, rank, world):
 
     # ---- per-row isolated timings: L2 emptied by a read-only sweep before each call
     flush = torch.empty(int(2.5 * l2) // 4, dtype=torch.float32, device="cuda").fill_(1.0)
-    per_row = []
-    for r in rows:
+
+    def isolated_us(fn):
         ts = []
         for i in range(30):
             flush.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            r.run()
+            fn()
             e1.record(stream)
             e1.synchronize()
             if i >= 5:
                 ts.append(e0.elapsed_time(e1) * 1e3)  # us
-        us = statistics.median(ts)
-        per_row.append((r, us))
+        return statistics.median(ts)
+
+    per_row = [(r, isolated_us(r.run)) for r in rows]
+    # the multi-token (verify) rows through both compute paths
+    verify_paths = {}
+    for r in rows:
+        if r.kind == "nvfp4" and r.p["N"] > 1:
+            cc = isolated_us(lambda r=r: r.run_path(bqd.BQD_PATH_CUDA_CORE))
+            mma = isolated_us(lambda r=r: r.run_path(bqd.BQD_PATH_MMA))
+            verify_paths[r.name] = {"cuda_core_us": round(cc, 3), "mma_us": round(mma, 3),
+                                    "mma_GB_s": round(r.bytes / mma / 1e3, 1), "speedup": round(cc / mma, 3)}
 
     # ---- headline: K full steps, inputs resident in HBM
     peak, peak_kind = measured_peaks()
@@ -482,6 +496,7 @@ def run_ours(args, rank, world):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dominant.bytes},
         "rows": breakdown,
+        "verify_paths": verify_paths,
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": {"value": round(step_bytes * world / e2e_s / 1e9, 2), "unit": "GB/s",
