@@ -357,6 +357,7 @@ def run_ours(args, rank, world):
     if world > 1:
         dist.barrier()
     bqd.lib()
+    bqd.set_launch_flags(bqd.BQD_LAUNCH_PDL if args.launch_pdl == "on" else 0)
     props = torch.cuda.get_device_properties(local)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_FALLBACK
 
@@ -488,7 +489,7 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; the method's workload shapes)",
-        "config": {"workload": WORKLOAD, "step_bytes": step_bytes,
+        "config": {"workload": WORKLOAD, "step_bytes": step_bytes, "launch_pdl": args.launch_pdl,
                    "l2": f"inputs larger than L2: one step streams {step_bytes / 1e9:.2f} GB vs L2 "
                          f"{l2 / 2**20:.0f} MiB; per-row figures flush L2 with a read sweep before each call",
                    "formats": "NVFP4 (E2M1 + E4M3/16 + fp32 ts), Q8_0 (int8 + fp16/32); bf16 x; fp32 accumulate"},
@@ -534,6 +535,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--launch-pdl", choices=["on", "off"], default="on",
+                    help="programmatic dependent launch between the step's kernels (BQD_LAUNCH_PDL)")
     ap.add_argument("--profile-row", default=None,
                     help="only call this row of the step (e.g. 'q8_0 151936x4096 N=1') --profile-calls times, "
                          "for profilers; prints no JSON line")

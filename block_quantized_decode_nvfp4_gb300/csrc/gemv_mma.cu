@@ -273,20 +273,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     pdl_trigger();
 
-    // The first ns stages need no wait; they are issued right after this
-    // thread's first activation loads (so those are not queued behind them).
-    auto start_weight_stream = [&] {
-        if (warp == 0 && lane == 0) {
-            prefetch_map(&map_codes);
-            prefetch_map(&map_scales);
-            for (int t = 0; t < nst && t < ns; ++t) {
-                mbar_arrive_expect_tx(&full[t], kStageBytes);
-                tma_load_2d(ring + t * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[t]);
-                tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16), m0,
-                            &full[t]);
-            }
+    // The first ns stages need no wait. They do not depend on the previous
+    // kernel in the stream either, so they start before the dependent-launch
+    // wait (the weights must not be written by that kernel).
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&map_codes);
+        prefetch_map(&map_scales);
+        for (int t = 0; t < nst && t < ns; ++t) {
+            mbar_arrive_expect_tx(&full[t], kStageBytes);
+            tma_load_2d(ring + t * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[t]);
+            tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16), m0,
+                        &full[t]);
         }
-    };
+    }
 
     // ---- activations, pass 1 (all threads): B = f16(x * 2^4) written while
     // each token's exponent range is scanned. Each thread keeps one token,
@@ -312,7 +311,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     u[j] = g0 + j * gstep < groups ? *reinterpret_cast<const uint4*>(xn + 8 * g)
                                                    : make_uint4(0u, 0u, 0u, 0u);
                 }
-                if (g0 == static_cast<int>(threadIdx.x) / N) start_weight_stream();  // thread 0: first round
 #pragma unroll
                 for (int j = 0; j < kLoadsInFlight; ++j) {
                     if (g0 + j * gstep >= groups) break;

@@ -81,13 +81,15 @@ enum {
 
 /* Launch options (bqd_set_launch_flags). */
 enum {
-    /* Programmatic dependent launch for the streaming GEMV (BQD_PATH_STREAM):
-     * a call may start, and begin reading its WEIGHTS (codes, scales, q, d),
-     * while the previous streaming call in the same stream is still
-     * finishing. Its activations are read, and its output written, only
-     * after that previous call has completed, so chaining layers is safe.
-     * Do not enable it if a call's weights can be written by the kernel
-     * immediately before it in the stream. Off by default. */
+    /* Programmatic dependent launch for the streaming and tensor-core GEMVs
+     * (BQD_PATH_STREAM, BQD_PATH_MMA) and the MoE stream kernels: a call may
+     * start while the previous kernel in the same stream is still finishing.
+     * A GEMV call may begin reading its WEIGHTS (codes, scales, q, d) then;
+     * its activations are read, and its output written, only after that
+     * previous kernel has completed, so chaining layers is safe. The MoE
+     * kernels read nothing before the previous kernel has completed. Do not
+     * enable it if a call's weights can be written by the kernel immediately
+     * before it in the stream. Off by default. */
     BQD_LAUNCH_PDL = 1
 };
 
