@@ -180,9 +180,9 @@ __device__ __forceinline__ void gu_pair(const unsigned char* cg, const unsigned 
         const uint32_t wgv[4] = {wg.x, wg.y, wg.z, wg.w}, wuv[4] = {wu.x, wu.y, wu.z, wu.w};
 #pragma unroll
         for (int b = 0; b < 2; ++b) {  // 16-element blocks of the chunk
-            float2 g2[NT], u2[NT];
+            float2 g2[2][NT], u2[2][NT];  // one accumulator pair per word: two short chains
 #pragma unroll
-            for (int n = 0; n < NT; ++n) g2[n] = u2[n] = make_float2(0.f, 0.f);
+            for (int n = 0; n < NT; ++n) g2[0][n] = g2[1][n] = u2[0][n] = u2[1][n] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int wi = 2 * b + j;  // elements 8wi .. 8wi+7 = activation pieces 2wi, 2wi+1
@@ -203,15 +203,17 @@ __device__ __forceinline__ void gu_pair(const unsigned char* cg, const unsigned 
                                           make_float2(x1.z, x1.w)};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        g2[n] = __ffma2_rn(fg[q], xv[q], g2[n]);
-                        u2[n] = __ffma2_rn(fu[q], xv[q], u2[n]);
+                        g2[j][n] = __ffma2_rn(fg[q], xv[q], g2[j][n]);
+                        u2[j][n] = __ffma2_rn(fu[q], xv[q], u2[j][n]);
                     }
                 }
             }
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                gsum[n] = fmaf(b ? scg.y : scg.x, g2[n].x + g2[n].y, gsum[n]);
-                usum[n] = fmaf(b ? scu.y : scu.x, u2[n].x + u2[n].y, usum[n]);
+                const float gb = (g2[0][n].x + g2[0][n].y) + (g2[1][n].x + g2[1][n].y);
+                const float ub = (u2[0][n].x + u2[0][n].y) + (u2[1][n].x + u2[1][n].y);
+                gsum[n] = fmaf(b ? scg.y : scg.x, gb, gsum[n]);
+                usum[n] = fmaf(b ? scu.y : scu.x, ub, usum[n]);
             }
         }
     }
@@ -231,9 +233,9 @@ __device__ __forceinline__ void dn_row(const unsigned char* cr, const unsigned c
         const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
-            float2 a2[NT];
+            float2 a2[2][NT];  // one accumulator pair per word: two short chains
 #pragma unroll
-            for (int n = 0; n < NT; ++n) a2[n] = make_float2(0.f, 0.f);
+            for (int n = 0; n < NT; ++n) a2[0][n] = a2[1][n] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int wi = 2 * b + j;  // elements 8wi .. 8wi+7 = h pieces 2wi, 2wi+1
@@ -245,14 +247,15 @@ __device__ __forceinline__ void dn_row(const unsigned char* cr, const unsigned c
                 for (int n = 0; n < NT; ++n) {
                     const float4 h0 = *reinterpret_cast<const float4*>(hs + n * I + xf_index(c, 2 * wi));
                     const float4 h1 = *reinterpret_cast<const float4*>(hs + n * I + xf_index(c, 2 * wi + 1));
-                    a2[n] = __ffma2_rn(f0, make_float2(h0.x, h0.y), a2[n]);
-                    a2[n] = __ffma2_rn(f1, make_float2(h0.z, h0.w), a2[n]);
-                    a2[n] = __ffma2_rn(f2, make_float2(h1.x, h1.y), a2[n]);
-                    a2[n] = __ffma2_rn(f3, make_float2(h1.z, h1.w), a2[n]);
+                    a2[j][n] = __ffma2_rn(f0, make_float2(h0.x, h0.y), a2[j][n]);
+                    a2[j][n] = __ffma2_rn(f1, make_float2(h0.z, h0.w), a2[j][n]);
+                    a2[j][n] = __ffma2_rn(f2, make_float2(h1.x, h1.y), a2[j][n]);
+                    a2[j][n] = __ffma2_rn(f3, make_float2(h1.z, h1.w), a2[j][n]);
                 }
             }
 #pragma unroll
-            for (int n = 0; n < NT; ++n) acc[n] = fmaf(b ? sc.y : sc.x, a2[n].x + a2[n].y, acc[n]);
+            for (int n = 0; n < NT; ++n)
+                acc[n] = fmaf(b ? sc.y : sc.x, (a2[0][n].x + a2[0][n].y) + (a2[1][n].x + a2[1][n].y), acc[n]);
         }
     }
 }
@@ -467,8 +470,8 @@ __global__ void __launch_bounds__(kThreadsM, 1)
 
     const int cw = warp - 1, ctid = threadIdx.x - kWarp;
     const int nch = I / 32;  // chunks per row (8 .. 128)
-    int lg = kWarp;          // lanes per row: the largest power of two <= nch, at most 32
-    while (lg > nch) lg >>= 1;
+    int lg = kWarp;          // lanes per row: the largest power of two <= nch / 2, at most 32
+    while (lg > 1 && 2 * lg > nch) lg >>= 1;
     const int rpp = kWarp / lg;                // rows per warp pass
     const int sub = lane / lg, gl = lane % lg;
     int staged_a = -1, staged_g0 = -1;
