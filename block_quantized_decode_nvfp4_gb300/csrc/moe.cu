@@ -102,9 +102,22 @@ __global__ void __launch_bounds__(kThreads) moe_route_kernel(const float* __rest
     unsigned char* tk = taken + warp * E;
     int* cnt = wc + warp * E;
     for (int t = t_lo; t < t_hi; ++t) {
-        for (int e = lane; e < E; e += kWarp) {
-            L[e] = logits[static_cast<int64_t>(t) * E + e];
-            tk[e] = 0;
+        // the token's logits: eight loads in flight per lane, then to shared memory
+        for (int e0 = 0; e0 < E; e0 += 8 * kWarp) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + i * kWarp + lane;
+                v[i] = e < E ? logits[static_cast<int64_t>(t) * E + e] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + i * kWarp + lane;
+                if (e < E) {
+                    L[e] = v[i];
+                    tk[e] = 0;
+                }
+            }
         }
         __syncwarp();
         int my_e = 0;
@@ -478,10 +491,22 @@ __global__ void __launch_bounds__(kThreads) moe_combine_kernel(MoeWorkspace ws, 
     if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < topk && ws.count[t * topk + threadIdx.x] != 1)
         atomicOr(ws.status, kStatusCoverage);
     if (j >= H) return;
+    // slots in order 0..topk-1; loads of up to eight slots in flight at once
     float acc = 0.f;
-    for (int s = 0; s < topk; ++s) {
-        const int f = t * topk + s;
-        if (ws.count[f] > 0) acc = fmaf(ws.wts[f], ws.part[static_cast<int64_t>(f) * H + j], acc);
+    for (int s0 = 0; s0 < topk; s0 += 8) {
+        int cnt[8];
+        float wv[8], pv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int f = t * topk + s0 + i;
+            const bool in = s0 + i < topk;
+            cnt[i] = in ? ws.count[f] : 0;
+            wv[i] = in ? ws.wts[f] : 0.f;
+            pv[i] = in ? ws.part[static_cast<int64_t>(f) * H + j] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (cnt[i] > 0) acc = fmaf(wv[i], pv[i], acc);
     }
     y[static_cast<int64_t>(t) * H + j] = acc;
 }
