@@ -181,6 +181,24 @@ def profiled_traffic(kernel_key):
     return ent.get("dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+def max_over_ranks(seconds: float, world: int, device) -> float:
+    """The slowest rank's time; every rank calls this (a collective)."""
+    if world == 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes: int, world: int, steps: int, seconds: float) -> float:
+    """Weak scaling: each rank streams step_bytes per step; the job's rate is
+    the bytes of all ranks over the slowest rank's time."""
+    return step_bytes * world * steps / seconds / 1e9
+
+
 # ---------------------------------------------------------------- device rows
 class Row:
     """One row of the step with its device buffers and launch closure."""
@@ -428,11 +446,7 @@ def run_ours(args, rank, world):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed_s = t_start.elapsed_time(t_end) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_s = float(t.item())
+    elapsed_s = max_over_ranks(t_start.elapsed_time(t_end) / 1e3, world, "cuda")
     dom_us = statistics.mean(a.elapsed_time(b_) * 1e3 for a, b_ in dom_events)
 
     # ---- e2e: host buffers through the public API, copies inside the timed region
@@ -456,11 +470,7 @@ def run_ours(args, rank, world):
             r.run()
             yo.copy_(r.y, non_blocking=True)
         torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / e2e_steps, world, "cuda")
 
     # ---- CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -472,7 +482,7 @@ def run_ours(args, rank, world):
     if rank != 0:
         return
     ms = elapsed_s / args.steps * 1e3
-    value = step_bytes * world * args.steps / elapsed_s / 1e9
+    value = whole_job_gbs(step_bytes, world, args.steps, elapsed_s)
     traffic = profiled_traffic("q8_0_gemv 151936x4096 N=1")
     breakdown = {}
     for r, us in per_row:
@@ -500,7 +510,7 @@ def run_ours(args, rank, world):
         "verify_paths": verify_paths,
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
-        "e2e": {"value": round(step_bytes * world / e2e_s / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(step_bytes, world, 1, e2e_s), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
                 "note": "weights resident (model parameters); per step: pinned H2D of every row's "
                         "activations and router logits, all calls, D2H of every output, stream sync"},
