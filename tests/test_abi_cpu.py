@@ -19,7 +19,8 @@ def L():
 
 
 def _declared_functions():
-    src = open(os.path.join(ROOT, "include", "bqd.h")).read()
+    with open(os.path.join(ROOT, "include", "bqd.h")) as f:
+        src = f.read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", src, flags=re.M)
     return sorted(set(n for n in names if n not in ("defined",)))

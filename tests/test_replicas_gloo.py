@@ -35,7 +35,7 @@ def _rank(rank, world, port, results):
 def test_two_ranks_agree_on_the_slowest_time_and_the_job_rate():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_rank, args=(world, port, results), nprocs=world, join=True)
         got = dict(results)
