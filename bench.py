@@ -158,10 +158,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_sha():
+def source_sha(files=None):
+    """Hash of the kernel sources: the named files of csrc/ (a kernel, its
+    launcher and the headers they include), or all of csrc/."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_decode_nvfp4_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files else os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -176,7 +178,7 @@ def profiled_traffic(kernel_key):
     with open(path) as f:
         d = json.load(f)
     ent = d.get(kernel_key)
-    if not ent or ent.get("source_sha") != source_sha():
+    if not ent or ent.get("source_sha") != source_sha(ent.get("sources")):
         return None
     return ent.get("dram_bytes_per_launch")
 
