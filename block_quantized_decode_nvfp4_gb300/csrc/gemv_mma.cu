@@ -11,20 +11,27 @@
 // (or, when their range does not allow that, both operands are bf16, which
 // also holds every such product). The tensor cores accumulate in fp32.
 //
-// Work split. A CTA owns a 128-row tile (the MMA's M) and a contiguous range
-// of k; the k ranges of one tile are the CTAs of a thread-block cluster
-// (up to 8), whose fp32 partial sums are added in rank order through
-// distributed shared memory, so results are deterministic. Roles per CTA:
+// Work split. Rows go in 128-row tiles (the MMA's M) and k in 256-k stages.
+// A thread-block cluster of cs CTAs (up to 8) takes tc <= cs consecutive
+// tiles, i.e. tc * K/256 (tile, stage) units in tile-major order, and rank r
+// of the cluster a contiguous 1/cs of them, which touches at most two tiles
+// (one accumulator each). The fp32 partial sums of a tile are added in rank
+// order through distributed shared memory, so results are deterministic.
+// tc > 1 lets a cluster's CTAs cover more SMs than whole tiles would (for
+// 96 tiles: 32 clusters of 4 CTAs, 12 stages each, instead of 96 CTAs of 16
+// stages). Roles per CTA:
 //  * warp 0, lane 0: producer. 2-D tensor copies (TMA) bring 128 rows x
 //    256 k of codes (16 KiB, 128-byte swizzle) and their scales (2 KiB) into
-//    a 3-stage shared-memory ring.
-//  * warps 2..5: decoders, one thread per row (TMEM lane). Each decodes 64 k
-//    of its row per step into f16 pairs and writes them to tensor memory
+//    a ring of up to 8 stages.
+//  * warps 2..17: decoders in four groups of four warps; group g takes the
+//    64-k chunk g of every stage, one row per thread (TMEM lane). A thread
+//    decodes its chunk into f16 pairs and writes them to tensor memory
 //    (tcgen05.st), which is the A operand of the MMA: the decoded weights
 //    never pass through shared memory.
-//  * warp 1: allocates 256 TMEM columns; lane 0 issues the MMAs
-//    (M = 128, N = 16, K = 16 each; B = the staged activations in shared
-//    memory) into one fp32 accumulator of 16 columns and frees A slots with
+//  * warp 1: allocates all 512 TMEM columns (accumulator + 15 A slots of 32
+//    columns); one elected lane issues the MMAs (M = 128, N = 16, K = 16
+//    each; B = the staged activations in shared memory) into one fp32
+//    accumulator of 16 columns per tile touched and frees A slots with
 //    tcgen05.commit.
 // Every wait is bounded; one that runs out sets a bit in the device error
 // word and the kernel runs to its end without waiting again.
@@ -56,7 +63,7 @@ constexpr int kChunkK = 64;                   // k per decode step / A slot
 constexpr int kChunksPerStage = kStageK / kChunkK;
 constexpr int kMaxStages = 8;                 // ring stages: as many as shared memory allows, 3..8
 constexpr int kASlots = 15;                   // A slots in TMEM, 32 columns each
-constexpr int kTmemCols = 512;                // D: columns [0, 16); A: [32, 512)
+constexpr int kTmemCols = 512;                // D: columns [0, 16) and [16, 32); A: [32, 512)
 constexpr int kACol0 = 32;
 constexpr int kDecGroups = 4;                 // decoder groups: group g takes chunk g of every stage
 constexpr int kDecWarps = 4 * kDecGroups;     // one warp per TMEM lane quarter per group
@@ -168,12 +175,26 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank)
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(const void* local, uint32_t rank)
 {
     uint32_t remote;
-    float v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return remote;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// 16 bytes from global memory. A thread's batch of these stays in program
+// order ahead of the code that uses the values, so the batch is in flight
+// at once rather than one load per round trip.
+__device__ __forceinline__ uint4 ld_global_v4(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
 
@@ -212,17 +233,20 @@ __device__ __forceinline__ void decode_chunk(const uint4& c0, const uint4& c1, u
 
 // ------------------------------------------------------------ kernel
 // Dynamic shared memory (1024-byte aligned): ring [ns][codes 16 KiB |
-// scales 2 KiB], then the activations B: krange/8 groups of [brows tokens]
-// [8 k] as f16 (or bf16), brows * 16 bytes per group: the K-major core-matrix
-// layout with brows * 16 bytes between k-adjacent core matrices. With
-// brows = 16 the second 8-token core matrix follows at +128 bytes; with
-// brows = 8 (N <= 8) the descriptor's row-group stride is 0, so MMA columns
-// 8..15 repeat columns 0..7 and are never read. After the last MMA the ring
-// is reused for the fp32 partial sums [16][128].
+// scales 2 KiB], then the activations B of the CTA's units in unit order:
+// 32 groups per unit of [brows tokens][8 k] as f16 (or bf16), brows * 16
+// bytes per group: the K-major core-matrix layout with brows * 16 bytes
+// between k-adjacent core matrices. With brows = 16 the second 8-token core
+// matrix follows at +128 bytes; with brows = 8 (N <= 8) the descriptor's
+// row-group stride is 0, so MMA columns 8..15 repeat columns 0..7 and are
+// never read. With cs > 1, a receive area at recv_off holds the partial sums
+// that the cluster's CTAs push to the rank owning each row: [cs ranks][16
+// tokens][rows_max rows] fp32. It is used for nothing else, so a peer can
+// write it while this CTA still runs its MMAs.
 __global__ void __launch_bounds__(kThreads, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_scales,
-                    const uint16_t* __restrict__ x, float* __restrict__ y, float ts, int M, int K, int N, int ks, int ns,
-                    int brows)
+                    const uint16_t* __restrict__ x, float* __restrict__ y, float ts, int M, int K, int N, int cs, int tc,
+                    int tiles, int ns, int brows, int recv_off)
 {
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], afull[kASlots], aempty[kASlots], dfull;
@@ -236,13 +260,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int gbytes = brows * 16;  // bytes of B per 8 k
 
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int rank = ks > 1 ? static_cast<int>(cluster_rank()) : 0;
-    const int tile = blockIdx.x / ks;
-    const int m0 = tile * kTileM;
+    const int rank = cs > 1 ? static_cast<int>(cluster_rank()) : 0;
     const int nst_all = K / kStageK;
-    const int st_lo = nst_all * rank / ks, st_hi = nst_all * (rank + 1) / ks;
-    const int nst = st_hi - st_lo;
-    const int k0 = st_lo * kStageK, krange = nst * kStageK;
+    // The cluster's tiles [tile0, tile0 + tcl) are U units; this CTA takes
+    // units [u_lo, u_hi): segment 0 = stages [sa, sa + n0) of tile ta, then
+    // segment 1 (when nst > n0) = stages [0, nst - n0) of tile ta + 1.
+    const int tile0 = static_cast<int>(blockIdx.x / cs) * tc;
+    const int tcl = min(tc, tiles - tile0);
+    const int U = tcl * nst_all;
+    const int u_lo = U * rank / cs, u_hi = U * (rank + 1) / cs;
+    const int nst = u_hi - u_lo;
+    const int ta = tile0 + u_lo / nst_all, sa = u_lo % nst_all;
+    const int n0 = min(nst, nst_all - sa);
+    const int g0 = n0 * (kStageK / 8);  // groups of B in segment 0
+    auto unit_stage = [&](int t) { return t < n0 ? sa + t : t - n0; };
+    auto unit_row0 = [&](int t) { return (t < n0 ? ta : ta + 1) * kTileM; };
+    auto group_k = [&](int g) { return g < g0 ? sa * kStageK + 8 * g : 8 * (g - g0); };
+    // Rows of the cluster: rank o owns rows [R o / cs, R (o + 1) / cs).
+    const int R = tcl * kTileM, rows_max = (R + cs - 1) / cs;
+    float* recv = reinterpret_cast<float*>(smem + recv_off);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ns; ++s) {
@@ -276,23 +312,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The first ns stages need no wait. They do not depend on the previous
     // kernel in the stream either, so they start before the dependent-launch
     // wait (the weights must not be written by that kernel).
-    if (warp == 0 && lane == 0) {
+    if (threadIdx.x == 0) {
         prefetch_map(&map_codes);
         prefetch_map(&map_scales);
         for (int t = 0; t < nst && t < ns; ++t) {
             mbar_arrive_expect_tx(&full[t], kStageBytes);
-            tma_load_2d(ring + t * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[t]);
-            tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16), m0,
-                        &full[t]);
+            tma_load_2d(ring + t * kStageBytes, &map_codes, unit_stage(t) * (kStageK / 2), unit_row0(t), &full[t]);
+            tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, unit_stage(t) * (kStageK / 16),
+                        unit_row0(t), &full[t]);
         }
     }
 
     // ---- activations, pass 1 (all threads): B = f16(x * 2^4) written while
     // each token's exponent range is scanned. Each thread keeps one token,
-    // with eight 16-byte loads in flight. The 2^4 prescale is exact for
+    // with up to eight 16-byte loads in flight together. The 2^4 prescale is exact for
     // 2^-21 <= |x| < 2^11; a token outside that window takes pass 2.
     pdl_wait();  // the activations may come from the previous kernel in the stream
-    const int groups = krange / 8;  // 8 k = one 16-byte piece
+    const int groups = nst * (kStageK / 8);  // 8 k = one 16-byte piece
     {
         const int active = (kThreads / N) * N, gstep = kThreads / N;
         // Every CTA reads the same activations: each starts at its own place
@@ -300,21 +336,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rot = static_cast<int>((blockIdx.x * 97u) % static_cast<unsigned>(groups));
         if (threadIdx.x < active) {
             const int n = threadIdx.x % N;
-            const uint16_t* xn = x + static_cast<int64_t>(n) * K + k0;
+            const uint16_t* xn = x + static_cast<int64_t>(n) * K;
             int emax = 0, emin = INT_MAX, bad = 0;
-            for (int g0 = threadIdx.x / N; g0 < groups; g0 += kLoadsInFlight * gstep) {
+            for (int gi = threadIdx.x / N; gi < groups; gi += kLoadsInFlight * gstep) {
                 uint4 u[kLoadsInFlight];
 #pragma unroll
                 for (int j = 0; j < kLoadsInFlight; ++j) {
-                    int g = g0 + j * gstep + rot;
+                    int g = gi + j * gstep + rot;
                     if (g >= groups) g -= groups;
-                    u[j] = g0 + j * gstep < groups ? *reinterpret_cast<const uint4*>(xn + 8 * g)
-                                                   : make_uint4(0u, 0u, 0u, 0u);
+                    u[j] = gi + j * gstep < groups ? ld_global_v4(xn + group_k(g)) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
                 for (int j = 0; j < kLoadsInFlight; ++j) {
-                    if (g0 + j * gstep >= groups) break;
-                    int g = g0 + j * gstep + rot;
+                    if (gi + j * gstep >= groups) break;
+                    int g = gi + j * gstep + rot;
                     if (g >= groups) g -= groups;
                     const uint32_t wv[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
                     uint32_t o[4];
@@ -364,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- pass 2 (all threads, only for activations outside the window)
         for (int i = threadIdx.x; i < groups * N; i += kThreads) {
             const int n = i % N, g = i / N;
-            uint4 u = *reinterpret_cast<const uint4*>(x + static_cast<int64_t>(n) * K + k0 + 8 * g);
+            uint4 u = ld_global_v4(x + static_cast<int64_t>(n) * K + group_k(g));
             if (f16) {
                 // 2^-sexp as two exact factors (it can exceed the fp32 range)
                 const int e = -token_sexp(n), e1 = e / 2, e2 = e - e1;
@@ -397,9 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t >= ns) {
                     if (ok) ok = mbar_wait(&empty[slot], phase ^ 1u, &g_mma_error);
                     mbar_arrive_expect_tx(&full[slot], kStageBytes);
-                    tma_load_2d(ring + slot * kStageBytes, &map_codes, (st_lo + t) * (kStageK / 2), m0, &full[slot]);
-                    tma_load_2d(ring + slot * kStageBytes + kCodesStage, &map_scales, (st_lo + t) * (kStageK / 16),
-                                m0, &full[slot]);
+                    tma_load_2d(ring + slot * kStageBytes, &map_codes, unit_stage(t) * (kStageK / 2), unit_row0(t),
+                                &full[slot]);
+                    tma_load_2d(ring + slot * kStageBytes + kCodesStage, &map_scales, unit_stage(t) * (kStageK / 16),
+                                unit_row0(t), &full[slot]);
                 }
                 if (++slot == ns) {
                     slot = 0;
@@ -435,6 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // previous batch's work.
         constexpr int kBatch = 4;
         static_assert(kASlots >= 2 * kBatch, "decoders must be able to run a batch ahead");
+        static_assert(kBatch == kChunksPerStage, "a batch is one unit (one stage of one tile)");
+        const int c_seg1 = n0 * kChunksPerStage;  // first chunk of segment 1
         bool ok = true;
         uint32_t slot = 0, phase = 0;
         for (int c = 0; c < nchunks; c += kBatch) {
@@ -446,6 +484,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && lane < kBatch) ok = mbar_wait(&afull[ws], wp, &g_mma_error);
             __syncwarp();
             tc_fence_after();
+            // the unit's accumulator, and whether this batch starts it
+            const uint32_t dcol = tm + (c < c_seg1 ? 0u : 16u);
+            const bool first = c == 0 || c == c_seg1;
             if (elect_one()) {
 #pragma unroll
                 for (int h = 0; h < kBatch; ++h) {
@@ -457,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // 16 k = two groups of B
                         const uint64_t bdesc =
                             bdesc0 + static_cast<uint64_t>(((c + h) * (kChunkK / 8) + 2 * j) * bstep);
-                        mma_tmem_a(tm, a_col + 8 * j, bdesc, idesc, ((c + h) | j) != 0 ? 1u : 0u);
+                        mma_tmem_a(dcol, a_col + 8 * j, bdesc, idesc, (first && (h | j) == 0) ? 0u : 1u);
                     }
                     mma_commit(&aempty[sl]);
                 }
@@ -516,45 +557,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 aphase ^= 1u;
             }
         }
-        // ---- epilogue: this row's 16 accumulators
-        if (ok) ok = mbar_wait_warp(&dfull, 0, &g_mma_error);
-        tc_fence_after();
-        uint32_t v[16];
-        tmem_ld_x16(tmem + lane_base, v);
-        if (ks == 1) {
-            if (m0 + row < M) {
+        // ---- epilogue: decoder group g takes this row's 16 accumulators of
+        // segment g (groups past the CTA's segments have nothing to do)
+        const int nseg = nst > n0 ? 2 : 1;
+        if (grp < nseg) {
+            if (ok) ok = mbar_wait_warp(&dfull, 0, &g_mma_error);
+            tc_fence_after();
+            uint32_t v[16];
+            tmem_ld_x16(tmem + lane_base + 16 * grp, v);
+            if (cs == 1) {  // one tile, all of k: the result itself
+                const int64_t m = static_cast<int64_t>(ta) * kTileM + row;
+                if (m < M) {
+#pragma unroll
+                    for (int n = 0; n < kNPad; ++n)
+                        if (n < N) y[static_cast<int64_t>(n) * M + m] = ldexpf(__uint_as_float(v[n]), token_sexp(n)) * ts;
+                }
+            } else {
+                // push the row's partial sums (in x's own scale: the staging
+                // scale is per CTA) into the receive area of its owner
+                const int q = ((grp == 0 ? ta : ta + 1) - tile0) * kTileM + row;
+                const int o = ((q + 1) * cs - 1) / R;  // the rank with R o / cs <= q < R (o + 1) / cs
+                const uint32_t dst =
+                    mapa(recv + (rank * kNPad) * rows_max + (q - R * o / cs), static_cast<uint32_t>(o));
 #pragma unroll
                 for (int n = 0; n < kNPad; ++n)
-                    if (n < N)
-                        y[static_cast<int64_t>(n) * M + m0 + row] = ldexpf(__uint_as_float(v[n]), token_sexp(n)) * ts;
+                    if (n < N) st_cluster_f32(dst + 4u * n * rows_max, ldexpf(__uint_as_float(v[n]), token_sexp(n)));
             }
-        } else {
-            float* part = reinterpret_cast<float*>(ring);  // every copy into the ring has been consumed
-#pragma unroll
-            for (int n = 0; n < kNPad; ++n) part[n * kTileM + row] = ldexpf(__uint_as_float(v[n]), token_sexp(n));
         }
         tc_fence_before();
     }
 
-    if (ks > 1) {
-        // ---- cluster reduction in rank order: this CTA writes rows
-        // [128 * rank / ks, 128 * (rank + 1) / ks) of the tile
+    if (cs > 1) {
+        // ---- cluster reduction: after the barrier (its release / acquire
+        // makes the pushed partials visible) each rank sums its own rows in
+        // rank order from its receive area: a row of local tile j takes the
+        // ranks whose units touch tile j. Nothing is read or written in a
+        // peer's shared memory after the barrier, so CTAs may then exit.
         cluster_sync();
-        const float* part = reinterpret_cast<const float*>(ring);
-        const int r_lo = kTileM * rank / ks, r_hi = kTileM * (rank + 1) / ks, nr = r_hi - r_lo;
-        for (int i = threadIdx.x; i < nr * N; i += kThreads) {
-            const int n = i / nr, r = r_lo + i % nr;
-            float pv[kMaxCluster];
-#pragma unroll
-            for (int j = 0; j < kMaxCluster; ++j)
-                pv[j] = j < ks ? ld_cluster_f32(part + n * kTileM + r, static_cast<uint32_t>(j)) : 0.f;
+        const int q_lo = R * rank / cs, q_hi = R * (rank + 1) / cs, nq = q_hi - q_lo;
+        for (int i = threadIdx.x; i < nq * N; i += kThreads) {
+            const int n = i / nq, qq = i % nq, q = q_lo + qq;
+            const int j = q / kTileM;
             float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxCluster; ++j)
-                if (j < ks) s += pv[j];  // rank order
-            if (m0 + r < M) y[static_cast<int64_t>(n) * M + m0 + r] = s * ts;
+            for (int p = 0; p < kMaxCluster; ++p) {
+                const int plo = U * p / cs, phi = U * (p + 1) / cs;
+                if (p < cs && plo < (j + 1) * nst_all && phi > j * nst_all)
+                    s += recv[(p * kNPad + n) * rows_max + qq];  // rank order
+            }
+            const int64_t m = static_cast<int64_t>(tile0) * kTileM + q;
+            if (m < M) y[static_cast<int64_t>(n) * M + m] = s * ts;
         }
-        cluster_sync();  // peers' shared memory stays alive until every read is done
     } else {
         __syncthreads();
     }
@@ -600,16 +653,23 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, in
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shared memory of a CTA with `stages_per_cta` stages of k, B rows of
-// `brows` tokens and a ring of `ns` stages.
-size_t smem_bytes(int stages_per_cta, int brows, int ns)
+// Receive area of the cluster reduction: [cs][16 tokens][rows per rank].
+size_t recv_bytes(int cs, int tc)
 {
-    const size_t s =
-        1024 + static_cast<size_t>(ns) * kStageBytes + static_cast<size_t>(stages_per_cta) * kStageK * brows * 2;
+    return cs > 1 ? static_cast<size_t>(cs) * kNPad * ((tc * kTileM + cs - 1) / cs) * sizeof(float) : 0;
+}
+
+// Shared memory of a CTA with `stages_per_cta` stages of k, B rows of
+// `brows` tokens, a ring of `ns` stages and `recv` bytes of receive area.
+size_t smem_bytes(int stages_per_cta, int brows, int ns, size_t recv)
+{
+    const size_t s = 1024 + static_cast<size_t>(ns) * kStageBytes +
+                     static_cast<size_t>(stages_per_cta) * kStageK * brows * 2 + recv;
     return s < static_cast<size_t>(kMinSmem) ? static_cast<size_t>(kMinSmem) : s;
 }
 
-// Clusters of `ks` CTAs that fit on the device at once (cached per device).
+// Clusters of `ks` CTAs with `smem` bytes of dynamic shared memory each that
+// fit on the device at once (cached per device and cluster size).
 int active_clusters(int dev, int sms, int ks, size_t smem)
 {
     static std::mutex mu;
@@ -649,7 +709,8 @@ bool mma_gemv_supported(int64_t M, int64_t K, int N)
         K > (int64_t(1) << 20))
         return false;
     const int64_t per_cta = (K / kStageK + kMaxCluster - 1) / kMaxCluster;
-    return smem_bytes(static_cast<int>(per_cta), N <= 8 ? 8 : 16, 3) <= static_cast<size_t>(kSmemLimit);
+    return smem_bytes(static_cast<int>(per_cta), N <= 8 ? 8 : 16, 3, recv_bytes(kMaxCluster, 1)) <=
+           static_cast<size_t>(kSmemLimit);
 }
 
 cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
@@ -662,36 +723,45 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
     const int limit = di.max_smem_optin < kSmemLimit ? di.max_smem_optin : kSmemLimit;
     static OccCache occ;
     blocks_per_sm(occ, reinterpret_cast<const void*>(gemv_mma_kernel), dev, kThreads,
-                  smem_bytes(1, 8, 3));  // sets the shared-memory opt-in
+                  smem_bytes(1, 8, 3, 0));  // sets the shared-memory opt-in
 
     const int tiles = static_cast<int>((M + kTileM - 1) / kTileM);
     const int nst_all = static_cast<int>(K / kStageK);
     const int brows = N <= 8 ? 8 : 16;
-    // Cluster size: fewest waves x stages per CTA (plus ~2 stages of fixed
-    // cost per wave); ties go to the smaller cluster.
-    int best_ks = 0;
+    // Clusters of cs CTAs over tc <= cs tiles: fewest waves x stages per
+    // CTA (plus ~2 stages of fixed cost per wave); ties go to the smaller
+    // cluster, then to fewer tiles per cluster.
+    int cs = 0, tc = 0;
     int64_t best_cost = INT64_MAX;
-    for (int ks = 1; ks <= kMaxCluster && ks <= nst_all; ++ks) {
-        const int per_cta = (nst_all + ks - 1) / ks;
-        const size_t smem = smem_bytes(per_cta, brows, 3);
-        if (smem > static_cast<size_t>(limit)) continue;
-        const int act = active_clusters(dev, di.sms, ks, smem);
-        const int64_t waves = (tiles + act - 1) / act;
-        const int64_t cost = waves * (per_cta + 2);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best_ks = ks;
+    for (int c = 1; c <= kMaxCluster && c <= nst_all; ++c) {
+        for (int t = 1; t <= c && t <= tiles; ++t) {
+            const int per = (t * nst_all + c - 1) / c;
+            const size_t sm = smem_bytes(per, brows, 3, recv_bytes(c, t));
+            if (sm > static_cast<size_t>(limit)) continue;
+            // one CTA per SM whatever its shared memory (see kMinSmem), so
+            // the count depends on c alone; asked once per c at the limit
+            const int act = active_clusters(dev, di.sms, c, static_cast<size_t>(limit));
+            const int64_t clusters = (tiles + t - 1) / t;
+            const int64_t waves = (clusters + act - 1) / act;
+            const int64_t cost = waves * (per + 2);
+            if (cost < best_cost) {
+                best_cost = cost;
+                cs = c;
+                tc = t;
+            }
         }
     }
-    if (best_ks == 0) return cudaErrorInvalidValue;
-    const int ks = best_ks;
-    const int per_cta = (nst_all + ks - 1) / ks;
+    if (cs == 0) return cudaErrorInvalidValue;
+    const int per_cta = (tc * nst_all + cs - 1) / cs;
     // Ring: as many stages as shared memory holds (up to 8, no more than the
-    // CTA's stages); at least 3 fit by the choice of ks.
-    int ns = static_cast<int>((limit - 1024 - static_cast<int64_t>(per_cta) * kStageK * brows * 2) / kStageBytes);
+    // CTA's stages); at least 3 fit by the choice of cs and tc.
+    const size_t recv = recv_bytes(cs, tc);
+    const int64_t bbytes = static_cast<int64_t>(per_cta) * kStageK * brows * 2;
+    int ns = static_cast<int>((limit - 1024 - bbytes - static_cast<int64_t>(recv)) / kStageBytes);
     if (ns > kMaxStages) ns = kMaxStages;
     if (ns > per_cta) ns = per_cta;
-    const size_t smem = smem_bytes(per_cta, brows, ns);
+    const size_t smem = smem_bytes(per_cta, brows, ns, recv);
+    const int recv_off = static_cast<int>(ns * kStageBytes + bbytes);
 
     CUtensorMap map_codes, map_scales;
     if (!make_map(&map_codes, codes, M, K / 2, kStageK / 2, true) ||
@@ -699,15 +769,16 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
         return cudaErrorInvalidValue;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles * ks));
+    const int clusters = (tiles + tc - 1) / tc;
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (ks > 1) {
+    if (cs > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = static_cast<unsigned>(ks);
+        attr[na].val.clusterDim.x = static_cast<unsigned>(cs);
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -720,7 +791,7 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
     cfg.attrs = attr;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, gemv_mma_kernel, map_codes, map_scales, x, y, ts, static_cast<int>(M),
-                              static_cast<int>(K), N, ks, ns, brows);
+                              static_cast<int>(K), N, cs, tc, tiles, ns, brows, recv_off);
 }
 
 cudaError_t read_and_clear_mma_error(unsigned int* out)

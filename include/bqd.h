@@ -73,8 +73,9 @@ enum {
     BQD_PATH_STREAM = 2,    /* bulk-copy (TMA) stream into a shared-memory ring, decode on the CUDA
                                cores; N == 1 and K % 256 == 0 (K <= 16384) only, else BQD_ERR_PATH */
     BQD_PATH_MMA = 3        /* NVFP4 only: weights decoded exactly to f16 (or bf16) in tensor memory and
-                               multiplied on the tensor cores (tcgen05.mma, fp32 accumulation), k split
-                               over a thread-block cluster with a fixed-order sum; 1 <= N <= 16,
+                               multiplied on the tensor cores (tcgen05.mma, fp32 accumulation), the
+                               (row tile, k) work split over thread-block clusters with a fixed-order
+                               sum, so results are deterministic; 1 <= N <= 16,
                                K % 256 == 0, M < 2^30, K <= 2^20 (smaller if shared memory runs
                                short), else BQD_ERR_PATH. q8_0_gemv_path returns BQD_ERR_PATH */
 };

@@ -43,11 +43,14 @@ def check(w, rows=None, what=""):
 
 
 # Several 128-row tiles with a ragged last tile, one to many 256-k stages
-# (so clusters of 1 to 8 CTAs), every token count from 1 to 16.
+# (so clusters of 1 to 8 CTAs), token counts from 1 to 16.
 @pytest.mark.parametrize("M,K,N", [
     (1, 256, 1), (128, 256, 16), (129, 512, 2), (300, 768, 4), (257, 1024, 8), (640, 2304, 3),
     (1000, 4096, 16), (77, 8192, 5), (4096, 256, 2), (383, 3072, 7), (200, 16384, 9), (1, 12288, 16),
     (513, 1536, 11), (64, 2048, 13),
+    # clusters that take 2..5 tiles (3..6 CTAs each on a 152-SM part), so a
+    # CTA's units cross a tile boundary, with a partial last cluster
+    (9819, 768, 3), (11995, 1024, 12), (5979, 3072, 12), (9819, 2048, 3), (13915, 1536, 5), (14427, 1536, 12),
 ])
 def test_mma_matches_oracle(M, K, N):
     check(syn.dense_nvfp4(M, K, N=N, seed=3 * M + K + N), what=f"{M}x{K} N={N}")
