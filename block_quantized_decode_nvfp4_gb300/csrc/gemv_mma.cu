@@ -12,26 +12,29 @@
 // also holds every such product). The tensor cores accumulate in fp32.
 //
 // Work split. Rows go in 128-row tiles (the MMA's M) and k in 256-k stages.
-// A thread-block cluster of cs CTAs (up to 8) takes tc <= cs consecutive
-// tiles, i.e. tc * K/256 (tile, stage) units in tile-major order, and rank r
-// of the cluster a contiguous 1/cs of them, which touches at most two tiles
-// (one accumulator each). The fp32 partial sums of a tile are added in rank
-// order through distributed shared memory, so results are deterministic.
-// tc > 1 lets a cluster's CTAs cover more SMs than whole tiles would (for
-// 96 tiles: 32 clusters of 4 CTAs, 12 stages each, instead of 96 CTAs of 16
-// stages). Roles per CTA:
-//  * warp 0, lane 0: producer. 2-D tensor copies (TMA) bring 128 rows x
-//    256 k of codes (16 KiB, 128-byte swizzle) and their scales (2 KiB) into
-//    a ring of up to 8 stages.
+// A thread-block cluster of cs CTAs (up to 8) takes tc <= 4 consecutive
+// tiles; rank r of the cluster takes the stages [r K/cs, (r + 1) K/cs) of
+// every one of them, so it stages only that slice of the activations and
+// uses it for all tc tiles, each tile in its own TMEM accumulator. The fp32
+// partial sums of a tile are added in rank order through distributed shared
+// memory, so results are deterministic. For 96 tiles of K = 4096 this gives
+// 32 clusters of 4 CTAs with 3 tiles x 4 stages each (128 SMs busy, a
+// quarter of the activations per CTA). Roles per CTA:
+//  * warp 0: producer. 2-D tensor copies (TMA) bring 128 rows x 256 k of
+//    codes (16 KiB, 128-byte swizzle) and their scales (2 KiB) into a ring
+//    of up to 8 stages; the first four are requested by four lanes at the
+//    CTA's start, the rest by lane 0 as the ring turns.
+//  * warps 1..17 stage the activations (f16 after an exact power-of-two
+//    scaling, or bf16) into shared memory once per CTA.
 //  * warps 2..17: decoders in four groups of four warps; group g takes the
 //    64-k chunk g of every stage, one row per thread (TMEM lane). A thread
 //    decodes its chunk into f16 pairs and writes them to tensor memory
 //    (tcgen05.st), which is the A operand of the MMA: the decoded weights
 //    never pass through shared memory.
-//  * warp 1: allocates all 512 TMEM columns (accumulator + 15 A slots of 32
-//    columns); one elected lane issues the MMAs (M = 128, N = 16, K = 16
+//  * warp 1: allocates all 512 TMEM columns (4 accumulators + 14 A slots of
+//    32 columns); one elected lane issues the MMAs (M = 128, N = 16, K = 16
 //    each; B = the staged activations in shared memory) into one fp32
-//    accumulator of 16 columns per tile touched and frees A slots with
+//    accumulator of 16 columns per tile and frees A slots with
 //    tcgen05.commit.
 // Every wait is bounded; one that runs out sets a bit in the device error
 // word and the kernel runs to its end without waiting again.
@@ -62,9 +65,10 @@ constexpr int kStageK = 256;                  // k per ring stage
 constexpr int kChunkK = 64;                   // k per decode step / A slot
 constexpr int kChunksPerStage = kStageK / kChunkK;
 constexpr int kMaxStages = 8;                 // ring stages: as many as shared memory allows, 3..8
-constexpr int kASlots = 15;                   // A slots in TMEM, 32 columns each
-constexpr int kTmemCols = 512;                // D: columns [0, 16) and [16, 32); A: [32, 512)
-constexpr int kACol0 = 32;
+constexpr int kASlots = 14;                   // A slots in TMEM, 32 columns each
+constexpr int kTmemCols = 512;                // D: columns [16 j, 16 j + 16) for tile j < 4; A: [64, 512)
+constexpr int kACol0 = 64;
+constexpr int kMaxTiles = 4;                  // tiles per cluster (accumulators per CTA)
 constexpr int kDecGroups = 4;                 // decoder groups: group g takes chunk g of every stage
 constexpr int kDecWarps = 4 * kDecGroups;     // one warp per TMEM lane quarter per group
 constexpr int kThreads = (2 + kDecWarps) * kWarp;
@@ -73,17 +77,24 @@ constexpr int kScalesStage = kTileM * (kStageK / 16);  // 2 KiB
 constexpr int kStageBytes = kCodesStage + kScalesStage;
 constexpr int kMaxCluster = 8;
 constexpr int kLoadsInFlight = 8;             // activation loads per thread in flight
+// Ring stages requested at the CTA's start; the producer requests the rest
+// once the activations are staged. Requesting all eight at once (about
+// 19 MB from 128 CTAs) delayed everything else the CTAs fetched at start by
+// up to 3 us; four measured best (12288 x 4096, N = 8: 16.6 us back to back
+// against 17.4 us with eight).
+constexpr int kInitStages = 4;
 // The CTA takes all of TMEM (512 columns). At least 116 KiB of shared
 // memory per CTA keeps two CTAs of this kernel (from any launches, on any
 // streams) off the same SM, so a TMEM allocation here never waits for a CTA
 // that may itself be waiting on a cluster peer.
 constexpr int kMinSmem = 116 * 1024;
 static_assert(kDecGroups == kChunksPerStage, "one chunk of every stage per decoder group");
-constexpr int kSmemLimit = 226 * 1024;  // dynamic part; static shared memory stays below 1 KiB
+constexpr int kSmemLimit = 225 * 1024;  // dynamic part; static shared memory stays below 2 KiB
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte alignment of the swizzled codes");
 static_assert(kACol0 + kASlots * 32 <= kTmemCols, "TMEM layout");
 static_assert(kASlots >= kDecGroups, "slot bookkeeping");
+static_assert(kMaxTiles * 16 <= kACol0 && kMaxTiles <= kDecGroups, "one accumulator and one epilogue group per tile");
 
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar)
@@ -251,7 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], afull[kASlots], aempty[kASlots], dfull;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_emax[kNPad], s_emin[kNPad], s_bad[kNPad];
+    // Exponent range of each token's activations per warp (warp 0 stages
+    // none; its row ends up holding the CTA's range): emax | emin << 9 |
+    // bad << 18, emax in [0, 255] (0 = no nonzero value), emin in [0, 256]
+    // (256 = none).
+    __shared__ uint32_t s_range[kThreads / kWarp][kNPad];
 
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
@@ -262,41 +277,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int rank = cs > 1 ? static_cast<int>(cluster_rank()) : 0;
     const int nst_all = K / kStageK;
-    // The cluster's tiles [tile0, tile0 + tcl) are U units; this CTA takes
-    // units [u_lo, u_hi): segment 0 = stages [sa, sa + n0) of tile ta, then
-    // segment 1 (when nst > n0) = stages [0, nst - n0) of tile ta + 1.
+    // The cluster's tiles [tile0, tile0 + tcl); this CTA's stages
+    // [s_lo, s_lo + nsr) of each. Units (tile, stage) go tile-major:
+    // unit t = tile t / nsr, stage s_lo + t % nsr.
     const int tile0 = static_cast<int>(blockIdx.x / cs) * tc;
     const int tcl = min(tc, tiles - tile0);
-    const int U = tcl * nst_all;
-    const int u_lo = U * rank / cs, u_hi = U * (rank + 1) / cs;
-    const int nst = u_hi - u_lo;
-    const int ta = tile0 + u_lo / nst_all, sa = u_lo % nst_all;
-    const int n0 = min(nst, nst_all - sa);
-    const int g0 = n0 * (kStageK / 8);  // groups of B in segment 0
-    auto unit_stage = [&](int t) { return t < n0 ? sa + t : t - n0; };
-    auto unit_row0 = [&](int t) { return (t < n0 ? ta : ta + 1) * kTileM; };
-    auto group_k = [&](int g) { return g < g0 ? sa * kStageK + 8 * g : 8 * (g - g0); };
+    const int s_lo = nst_all * rank / cs, nsr = nst_all * (rank + 1) / cs - s_lo;
+    const int nst = tcl * nsr;
+    auto unit_stage = [&](int t) { return s_lo + t % nsr; };
+    auto unit_row0 = [&](int t) { return (tile0 + t / nsr) * kTileM; };
+    auto group_k = [&](int g) { return s_lo * kStageK + 8 * g; };
     // Rows of the cluster: rank o owns rows [R o / cs, R (o + 1) / cs).
     const int R = tcl * kTileM, rows_max = (R + cs - 1) / cs;
     float* recv = reinterpret_cast<float*>(smem + recv_off);
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < ns; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kDecWarps);
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < ns; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kDecWarps);
+            }
+            for (int s = 0; s < kASlots; ++s) {
+                mbar_init(&afull[s], 4);  // the four warps of the group that owns the chunk
+                mbar_init(&aempty[s], 1);
+            }
+            mbar_init(&dfull, 1);
+            fence_barrier_init();
+            prefetch_map(&map_codes);
+            prefetch_map(&map_scales);
         }
-        for (int s = 0; s < kASlots; ++s) {
-            mbar_init(&afull[s], 4);  // the four warps of the group that owns the chunk
-            mbar_init(&aempty[s], 1);
+        __syncwarp();
+        // The first stages need no wait. They do not depend on the previous
+        // kernel in the stream either, so the first kInitStages of them start
+        // at once, while warp 1 allocates tensor memory and before the
+        // dependent-launch wait (the weights must not be written by that
+        // kernel). Lane t requests stage t.
+        const int t = lane;
+        if (t < nst && t < ns && t < kInitStages) {
+            mbar_arrive_expect_tx(&full[t], kStageBytes);
+            tma_load_2d(ring + t * kStageBytes, &map_codes, unit_stage(t) * (kStageK / 2), unit_row0(t), &full[t]);
+            tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, unit_stage(t) * (kStageK / 16),
+                        unit_row0(t), &full[t]);
         }
-        mbar_init(&dfull, 1);
-        fence_barrier_init();
     }
-    if (threadIdx.x < kNPad) {
-        s_emax[threadIdx.x] = 0;
-        s_emin[threadIdx.x] = INT_MAX;
-        s_bad[threadIdx.x] = 0;
-    }
+    static_assert(kMaxStages <= kWarp, "one lane per initial stage");
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                      "r"(kTmemCols)
@@ -309,36 +333,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     pdl_trigger();
 
-    // The first ns stages need no wait. They do not depend on the previous
-    // kernel in the stream either, so they start before the dependent-launch
-    // wait (the weights must not be written by that kernel).
-    if (threadIdx.x == 0) {
-        prefetch_map(&map_codes);
-        prefetch_map(&map_scales);
-        for (int t = 0; t < nst && t < ns; ++t) {
-            mbar_arrive_expect_tx(&full[t], kStageBytes);
-            tma_load_2d(ring + t * kStageBytes, &map_codes, unit_stage(t) * (kStageK / 2), unit_row0(t), &full[t]);
-            tma_load_2d(ring + t * kStageBytes + kCodesStage, &map_scales, unit_stage(t) * (kStageK / 16),
-                        unit_row0(t), &full[t]);
-        }
-    }
-
-    // ---- activations, pass 1 (all threads): B = f16(x * 2^4) written while
-    // each token's exponent range is scanned. Each thread keeps one token,
-    // with up to eight 16-byte loads in flight together. The 2^4 prescale is exact for
+    // ---- activations, pass 1 (warps 1..; warp 0 has just issued the ring's
+    // first copies, and its shared-memory accesses queue behind them): B = f16(x * 2^4) written while each token's exponent
+    // range is scanned. Each thread keeps one token, with up to eight 16-byte
+    // loads in flight together. The 2^4 prescale is exact for
     // 2^-21 <= |x| < 2^11; a token outside that window takes pass 2.
     pdl_wait();  // the activations may come from the previous kernel in the stream
-    const int groups = nst * (kStageK / 8);  // 8 k = one 16-byte piece
+    const int groups = nsr * (kStageK / 8);  // B covers the CTA's stages once; 8 k = one 16-byte piece
     {
-        const int active = (kThreads / N) * N, gstep = kThreads / N;
+        constexpr int kStagers = kThreads - kWarp;
+        const int xt = threadIdx.x - kWarp;  // < 0 in warp 0
+        const int active = (kStagers / N) * N, gstep = kStagers / N;
         // Every CTA reads the same activations: each starts at its own place
         // so that the CTAs do not all ask for the same lines at once.
         const int rot = static_cast<int>((blockIdx.x * 97u) % static_cast<unsigned>(groups));
-        if (threadIdx.x < active) {
-            const int n = threadIdx.x % N;
+        const int n = (xt + N * kWarp) % N;  // lane l of any warp: token l % N when N divides 32
+        int emax = 0, emin = INT_MAX, bad = 0;
+        if (xt >= 0 && xt < active) {
             const uint16_t* xn = x + static_cast<int64_t>(n) * K;
-            int emax = 0, emin = INT_MAX, bad = 0;
-            for (int gi = threadIdx.x / N; gi < groups; gi += kLoadsInFlight * gstep) {
+            for (int gi = xt / N; gi < groups; gi += kLoadsInFlight * gstep) {
                 uint4 u[kLoadsInFlight];
 #pragma unroll
                 for (int j = 0; j < kLoadsInFlight; ++j) {
@@ -371,29 +384,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4*>(bsm + g * gbytes + n * 16) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
             }
-            if (bad) atomicOr(&s_bad[n], 1);
-            atomicMax(&s_emax[n], emax);
-            atomicMin(&s_emin[n], emin);
         }
+        // Per-token range: reduce over the warp's lanes of each token, then
+        // one plain store per warp and token (shared atomics from every warp
+        // on a few words took over a microsecond to settle)
+        if ((kWarp % N) == 0) {  // lane l holds token l % N
+            for (int off = N; off < kWarp; off <<= 1) {
+                emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, off));
+                emin = min(emin, __shfl_xor_sync(0xFFFFFFFFu, emin, off));
+                bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, off);
+            }
+        } else {
+            for (int t = 0; t < N; ++t) {
+                const int mx = __reduce_max_sync(0xFFFFFFFFu, n == t ? emax : 0);
+                const int mn = __reduce_min_sync(0xFFFFFFFFu, n == t ? emin : INT_MAX);
+                const int bd = static_cast<int>(__reduce_or_sync(0xFFFFFFFFu, n == t ? static_cast<unsigned>(bad) : 0u));
+                if (lane == t) {
+                    emax = mx;
+                    emin = mn;
+                    bad = bd;
+                }
+            }
+        }
+        if (lane < N)  // lane t now holds token t's range over the warp
+            s_range[warp][lane] = static_cast<uint32_t>(emax) | static_cast<uint32_t>(min(emin, 256)) << 9 |
+                                  static_cast<uint32_t>(bad) << 18;
     }
     __syncthreads();
     // Staging mode of the CTA: 0 = f16 with the fixed 2^4 prescale (pass 1
     // is final); 1 = f16 with a per-token prescale 2^-sexp that puts the
     // token's largest |x| in [2^14, 2^15), exact when every nonzero |x| of
     // the token lies within 31 binades of the largest; 2 = bf16 operands.
-    int mode = 0;
-    for (int n = 0; n < N; ++n) {
-        const bool none = s_emin[n] == INT_MAX;
-        if (s_bad[n] || (!none && s_emax[n] - s_emin[n] > 31))
-            mode = 2;
-        else if (!none && (s_emin[n] < 127 - 21 || s_emax[n] > 127 + 10) && mode < 1)
-            mode = 1;
+    // Thread t < N of warp 1 judges token t; the barriers OR the verdicts.
+    int need2 = 0, need1 = 0;
+    if (warp == 1 && lane < N) {
+        const int t = lane;
+        int emax = 0, emin = 256, bad = 0;
+        for (int w = 1; w < kThreads / kWarp; ++w) {
+            const uint32_t r = s_range[w][t];
+            emax = max(emax, static_cast<int>(r & 0x1FFu));
+            emin = min(emin, static_cast<int>((r >> 9) & 0x1FFu));
+            bad |= static_cast<int>(r >> 18);
+        }
+        s_range[0][t] = static_cast<uint32_t>(emax) | static_cast<uint32_t>(emin) << 9;  // read by token_sexp
+        const bool none = emin == 256;
+        need2 = bad || (!none && emax - emin > 31);
+        need1 = !none && (emin < 127 - 21 || emax > 127 + 10);
     }
+    const int any2 = __syncthreads_or(need2), any1 = __syncthreads_or(need1);
+    const int mode = any2 ? 2 : any1 ? 1 : 0;
     const bool f16 = mode != 2;
     auto token_sexp = [&](int n) {
         if (mode == 0) return -4;
-        if (mode == 2 || n >= N || s_emin[n] == INT_MAX) return 0;
-        return s_emax[n] - 127 - 14;
+        if (mode == 2 || n >= N || (s_range[0][n] >> 9) == 256u) return 0;
+        return static_cast<int>(s_range[0][n] & 0x1FFu) - 127 - 14;
     };
     if (mode != 0) {
         // ---- pass 2 (all threads, only for activations outside the window)
@@ -429,8 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             uint32_t slot = 0, phase = 0;
             for (int t = 0; t < nst; ++t) {
-                if (t >= ns) {
-                    if (ok) ok = mbar_wait(&empty[slot], phase ^ 1u, &g_mma_error);
+                if (t >= kInitStages || t >= ns) {
+                    // a slot's first use needs no wait
+                    if (t >= ns && ok) ok = mbar_wait(&empty[slot], phase ^ 1u, &g_mma_error);
                     mbar_arrive_expect_tx(&full[slot], kStageBytes);
                     tma_load_2d(ring + slot * kStageBytes, &map_codes, unit_stage(t) * (kStageK / 2), unit_row0(t),
                                 &full[slot]);
@@ -472,9 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kBatch = 4;
         static_assert(kASlots >= 2 * kBatch, "decoders must be able to run a batch ahead");
         static_assert(kBatch == kChunksPerStage, "a batch is one unit (one stage of one tile)");
-        const int c_seg1 = n0 * kChunksPerStage;  // first chunk of segment 1
         bool ok = true;
         uint32_t slot = 0, phase = 0;
+        int sb = 0, ti = 0;  // the batch's unit: stage within B, tile of the cluster
         for (int c = 0; c < nchunks; c += kBatch) {
             uint32_t ws = slot + (lane & (kBatch - 1)), wp = phase;
             if (ws >= kASlots) {
@@ -484,9 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && lane < kBatch) ok = mbar_wait(&afull[ws], wp, &g_mma_error);
             __syncwarp();
             tc_fence_after();
-            // the unit's accumulator, and whether this batch starts it
-            const uint32_t dcol = tm + (c < c_seg1 ? 0u : 16u);
-            const bool first = c == 0 || c == c_seg1;
+            // the unit's tile accumulator, and whether this batch starts it
+            const uint32_t dcol = tm + 16u * static_cast<uint32_t>(ti);
+            const bool first = sb == 0;
             if (elect_one()) {
 #pragma unroll
                 for (int h = 0; h < kBatch; ++h) {
@@ -497,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < kChunkK / 16; ++j) {
                         // 16 k = two groups of B
                         const uint64_t bdesc =
-                            bdesc0 + static_cast<uint64_t>(((c + h) * (kChunkK / 8) + 2 * j) * bstep);
+                            bdesc0 + static_cast<uint64_t>(((sb * kBatch + h) * (kChunkK / 8) + 2 * j) * bstep);
                         mma_tmem_a(dcol, a_col + 8 * j, bdesc, idesc, (first && (h | j) == 0) ? 0u : 1u);
                     }
                     mma_commit(&aempty[sl]);
@@ -508,6 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (slot >= kASlots) {
                 slot -= kASlots;
                 phase ^= 1u;
+            }
+            if (++sb == nsr) {
+                sb = 0;
+                ++ti;
             }
         }
         if (elect_one()) mma_commit(&dfull);
@@ -558,15 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // ---- epilogue: decoder group g takes this row's 16 accumulators of
-        // segment g (groups past the CTA's segments have nothing to do)
-        const int nseg = nst > n0 ? 2 : 1;
-        if (grp < nseg) {
+        // the cluster's tile g (groups past the cluster's tiles have nothing
+        // to do)
+        if (grp < tcl) {
             if (ok) ok = mbar_wait_warp(&dfull, 0, &g_mma_error);
             tc_fence_after();
             uint32_t v[16];
             tmem_ld_x16(tmem + lane_base + 16 * grp, v);
-            if (cs == 1) {  // one tile, all of k: the result itself
-                const int64_t m = static_cast<int64_t>(ta) * kTileM + row;
+            if (cs == 1) {  // all of k: the result itself
+                const int64_t m = static_cast<int64_t>(tile0 + grp) * kTileM + row;
                 if (m < M) {
 #pragma unroll
                     for (int n = 0; n < kNPad; ++n)
@@ -575,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // push the row's partial sums (in x's own scale: the staging
                 // scale is per CTA) into the receive area of its owner
-                const int q = ((grp == 0 ? ta : ta + 1) - tile0) * kTileM + row;
+                const int q = grp * kTileM + row;
                 const int o = ((q + 1) * cs - 1) / R;  // the rank with R o / cs <= q < R (o + 1) / cs
                 const uint32_t dst =
                     mapa(recv + (rank * kNPad) * rows_max + (q - R * o / cs), static_cast<uint32_t>(o));
@@ -589,22 +638,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (cs > 1) {
         // ---- cluster reduction: after the barrier (its release / acquire
-        // makes the pushed partials visible) each rank sums its own rows in
-        // rank order from its receive area: a row of local tile j takes the
-        // ranks whose units touch tile j. Nothing is read or written in a
-        // peer's shared memory after the barrier, so CTAs may then exit.
+        // makes the pushed partials visible) each rank sums its own rows
+        // over all ranks, in rank order, from its receive area. Nothing is
+        // read or written in a peer's shared memory after the barrier, so
+        // CTAs may then exit.
         cluster_sync();
         const int q_lo = R * rank / cs, q_hi = R * (rank + 1) / cs, nq = q_hi - q_lo;
         for (int i = threadIdx.x; i < nq * N; i += kThreads) {
             const int n = i / nq, qq = i % nq, q = q_lo + qq;
-            const int j = q / kTileM;
             float s = 0.f;
 #pragma unroll
-            for (int p = 0; p < kMaxCluster; ++p) {
-                const int plo = U * p / cs, phi = U * (p + 1) / cs;
-                if (p < cs && plo < (j + 1) * nst_all && phi > j * nst_all)
-                    s += recv[(p * kNPad + n) * rows_max + qq];  // rank order
-            }
+            for (int p = 0; p < kMaxCluster; ++p)
+                if (p < cs) s += recv[(p * kNPad + n) * rows_max + qq];  // rank order
             const int64_t m = static_cast<int64_t>(tile0) * kTileM + q;
             if (m < M) y[static_cast<int64_t>(n) * M + m] = s * ts;
         }
@@ -728,22 +773,23 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
     const int tiles = static_cast<int>((M + kTileM - 1) / kTileM);
     const int nst_all = static_cast<int>(K / kStageK);
     const int brows = N <= 8 ? 8 : 16;
-    // Clusters of cs CTAs over tc <= cs tiles: fewest waves x stages per
-    // CTA (plus ~2 stages of fixed cost per wave); ties go to the smaller
-    // cluster, then to fewer tiles per cluster.
+    // Clusters of cs CTAs over tc tiles. Cost in tenths of a stage's time:
+    // per wave, the CTA's units plus a fixed 2 stages plus ~0.6 stage per
+    // stage of activations staged; a cluster reduction adds ~3 stages. Ties
+    // go to the smaller cluster, then to fewer tiles per cluster.
     int cs = 0, tc = 0;
     int64_t best_cost = INT64_MAX;
     for (int c = 1; c <= kMaxCluster && c <= nst_all; ++c) {
-        for (int t = 1; t <= c && t <= tiles; ++t) {
-            const int per = (t * nst_all + c - 1) / c;
-            const size_t sm = smem_bytes(per, brows, 3, recv_bytes(c, t));
+        const int xst = (nst_all + c - 1) / c;  // stages of k per CTA
+        for (int t = 1; t <= kMaxTiles && t <= tiles; ++t) {
+            const size_t sm = smem_bytes(xst, brows, 3, recv_bytes(c, t));
             if (sm > static_cast<size_t>(limit)) continue;
             // one CTA per SM whatever its shared memory (see kMinSmem), so
             // the count depends on c alone; asked once per c at the limit
             const int act = active_clusters(dev, di.sms, c, static_cast<size_t>(limit));
             const int64_t clusters = (tiles + t - 1) / t;
             const int64_t waves = (clusters + act - 1) / act;
-            const int64_t cost = waves * (per + 2);
+            const int64_t cost = waves * (10 * t * xst + 20 + 6 * xst) + (c > 1 ? 30 : 0);
             if (cost < best_cost) {
                 best_cost = cost;
                 cs = c;
@@ -752,14 +798,14 @@ cudaError_t launch_nvfp4_gemv_mma(const uint8_t* codes, const uint8_t* scales, f
         }
     }
     if (cs == 0) return cudaErrorInvalidValue;
-    const int per_cta = (tc * nst_all + cs - 1) / cs;
+    const int per_cta = (nst_all + cs - 1) / cs;  // stages of k per CTA (B holds them once)
     // Ring: as many stages as shared memory holds (up to 8, no more than the
     // CTA's stages); at least 3 fit by the choice of cs and tc.
     const size_t recv = recv_bytes(cs, tc);
     const int64_t bbytes = static_cast<int64_t>(per_cta) * kStageK * brows * 2;
     int ns = static_cast<int>((limit - 1024 - bbytes - static_cast<int64_t>(recv)) / kStageBytes);
     if (ns > kMaxStages) ns = kMaxStages;
-    if (ns > per_cta) ns = per_cta;
+    if (ns > per_cta * tc) ns = per_cta * tc;
     const size_t smem = smem_bytes(per_cta, brows, ns, recv);
     const int recv_off = static_cast<int>(ns * kStageBytes + bbytes);
 

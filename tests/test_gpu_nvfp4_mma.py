@@ -48,9 +48,10 @@ def check(w, rows=None, what=""):
     (1, 256, 1), (128, 256, 16), (129, 512, 2), (300, 768, 4), (257, 1024, 8), (640, 2304, 3),
     (1000, 4096, 16), (77, 8192, 5), (4096, 256, 2), (383, 3072, 7), (200, 16384, 9), (1, 12288, 16),
     (513, 1536, 11), (64, 2048, 13),
-    # clusters that take 2..5 tiles (3..6 CTAs each on a 152-SM part), so a
-    # CTA's units cross a tile boundary, with a partial last cluster
-    (9819, 768, 3), (11995, 1024, 12), (5979, 3072, 12), (9819, 2048, 3), (13915, 1536, 5), (14427, 1536, 12),
+    # clusters of 2..6 CTAs over 2..4 tiles each (on a 152-SM part), one
+    # accumulator per tile and a partial last cluster; and one CTA over 2
+    # tiles with all of k (no cluster)
+    (5979, 3072, 12), (9819, 2048, 3), (20000, 768, 4), (20000, 1024, 12), (20000, 512, 5), (30000, 256, 16),
 ])
 def test_mma_matches_oracle(M, K, N):
     check(syn.dense_nvfp4(M, K, N=N, seed=3 * M + K + N), what=f"{M}x{K} N={N}")
@@ -62,6 +63,16 @@ def test_mma_full_size_sampled_rows(M, K, N):
     w = syn.dense_nvfp4(M, K, N=N, seed=11)
     rng = np.random.default_rng(M + K + N)
     rows = np.unique(np.concatenate([[0, 1, 127, 128, M - 2, M - 1], rng.choice(M, 384, replace=False)]))
+    check(w, rows=rows, what=f"{M}x{K} N={N}")
+
+
+def test_mma_lm_head_shape_sampled_rows():
+    # 1187 row tiles: CTAs of four whole tiles each, two waves, a partial
+    # last group
+    M, K, N = 151936, 4096, 8
+    w = syn.dense_nvfp4(M, K, N=N, seed=13)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 127, 128, 511, 512, M - 129, M - 128, M - 1], rng.choice(M, 256, replace=False)]))
     check(w, rows=rows, what=f"{M}x{K} N={N}")
 
 
