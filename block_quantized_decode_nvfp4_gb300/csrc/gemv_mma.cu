@@ -244,8 +244,9 @@ __device__ __forceinline__ void decode_chunk(const uint4& c0, const uint4& c1, u
 
 // ------------------------------------------------------------ kernel
 // Dynamic shared memory (1024-byte aligned): ring [ns][codes 16 KiB |
-// scales 2 KiB], then the activations B of the CTA's units in unit order:
-// 32 groups per unit of [brows tokens][8 k] as f16 (or bf16), brows * 16
+// scales 2 KiB], then the activations B of the CTA's k slice (its nsr
+// stages, used for every tile of the cluster): 32 groups per stage of
+// [brows tokens][8 k] as f16 (or bf16), brows * 16
 // bytes per group: the K-major core-matrix layout with brows * 16 bytes
 // between k-adjacent core matrices. With brows = 16 the second 8-token core
 // matrix follows at +128 bytes; with brows = 8 (N <= 8) the descriptor's
@@ -333,10 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     pdl_trigger();
 
-    // ---- activations, pass 1 (warps 1..; warp 0 has just issued the ring's
-    // first copies, and its shared-memory accesses queue behind them): B = f16(x * 2^4) written while each token's exponent
-    // range is scanned. Each thread keeps one token, with up to eight 16-byte
-    // loads in flight together. The 2^4 prescale is exact for
+    // ---- activations, pass 1 (warps 1..17; warp 0 has just issued the
+    // ring's first copies): B = f16(x * 2^4) written while each token's
+    // exponent range is scanned. Each thread keeps one token, with up to
+    // eight 16-byte loads in flight together. The 2^4 prescale is exact for
     // 2^-21 <= |x| < 2^11; a token outside that window takes pass 2.
     pdl_wait();  // the activations may come from the previous kernel in the stream
     const int groups = nsr * (kStageK / 8);  // B covers the CTA's stages once; 8 k = one 16-byte piece
@@ -395,16 +396,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bad |= __shfl_xor_sync(0xFFFFFFFFu, bad, off);
             }
         } else {
+            // the reductions read every lane's own values, so lane t keeps
+            // token t's result apart until the loop ends
+            int tmax = 0, tmin = INT_MAX, tbad = 0;
             for (int t = 0; t < N; ++t) {
                 const int mx = __reduce_max_sync(0xFFFFFFFFu, n == t ? emax : 0);
                 const int mn = __reduce_min_sync(0xFFFFFFFFu, n == t ? emin : INT_MAX);
                 const int bd = static_cast<int>(__reduce_or_sync(0xFFFFFFFFu, n == t ? static_cast<unsigned>(bad) : 0u));
                 if (lane == t) {
-                    emax = mx;
-                    emin = mn;
-                    bad = bd;
+                    tmax = mx;
+                    tmin = mn;
+                    tbad = bd;
                 }
             }
+            emax = tmax;
+            emin = tmin;
+            bad = tbad;
         }
         if (lane < N)  // lane t now holds token t's range over the warp
             s_range[warp][lane] = static_cast<uint32_t>(emax) | static_cast<uint32_t>(min(emin, 256)) << 9 |
