@@ -67,6 +67,24 @@ def test_nvfp4_gemv_validation(L):
     assert L.nvfp4_gemv(A, A, 1.0, A, A, 1 << 40, 1 << 30, 1, s) == 2  # M * K overflow
 
 
+def test_compute_path_restrictions(L):
+    # a path that does not take the arguments answers BQD_ERR_PATH (7) on
+    # the host, before any CUDA call
+    s, MMA, STREAM = None, 3, 2
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 256, 4112, 8, MMA, s) == 7      # K % 256 != 0
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 256, 128, 8, MMA, s) == 7       # K < 256
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 4, (1 << 20) + 256, 2, MMA, s) == 7  # K > 2^20
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 256, 65536, 16, MMA, s) == 7    # activations exceed shared memory
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 256, 4096, 2, STREAM, s) == 7   # stream path is N = 1 only
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 256, 16640, 1, STREAM, s) == 7  # K > 16384
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 256, 4112, 1, STREAM, s) == 7   # K % 256 != 0
+    assert L.q8_0_gemv_path(A, A, A, A, 256, 4096, 4, MMA, s) == 7            # no tensor-core Q8_0 path
+    assert L.q8_0_gemv_path(A, A, A, A, 256, 4096, 2, STREAM, s) == 7
+    assert L.q8_0_gemv_path(A, A, A, A, 256, 4096, 1, 99, s) == 7
+    # argument errors come before path errors
+    assert L.nvfp4_gemv_path(A, A, 1.0, A, A, 256, 4096, 17, MMA, s) == 2
+
+
 def test_q8_0_and_dequant_validation(L):
     s = None
     assert L.q8_0_gemv(A, A, A, A, 4, 48, 1, s) == 2                   # K % 32
