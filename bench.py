@@ -10,7 +10,7 @@ weights resident in HBM:
     combine)
 The metric is algorithmic HBM bytes (packed weights + scales + activations +
 outputs; MoE: the experts the routing actually selects) per second; a step
-touches ~1.8 GB, far more than L2, so successive steps read from HBM.
+touches ~1.1 GB, far more than L2, so successive steps read from HBM.
 
 Printed: one JSON line (rank 0). `--impl reference` times the fp64 CPU
 oracle on a bounded sample of the same workload instead.

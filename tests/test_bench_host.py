@@ -1,0 +1,72 @@
+"""Host logic of bench.py that needs no GPU: the algorithmic byte counts
+behind every GB/s figure and the roofline's numerator, the MoE expert count
+they use, the whole-job rate, and the traffic record lookup."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_dense_byte_counts():
+    # NVFP4: M*K/2 code bytes + M*K/16 scale bytes + 4 (fp32 tensor scale)
+    # + 2NK (bf16 x) + 4NM (fp32 y)
+    assert bench.nvfp4_bytes(12288, 4096, 1) == 25165824 + 3145728 + 4 + 8192 + 49152 == 28368900
+    assert bench.nvfp4_bytes(4096, 4096, 8) == 8388608 + 1048576 + 4 + 65536 + 131072
+    # Q8_0: M*K int8 + M*K/32 fp16 scales + x + y (the LM head figures of
+    # the committed DRAM summary)
+    assert bench.q8_0_bytes(151936, 4096, 1) == 622329856 + 38895616 + 8192 + 607744 == 661841408
+    assert bench.q8_0_bytes(32, 64, 2) == 2048 + 128 + 256 + 256
+
+
+def test_moe_expert_bytes():
+    # gate_up [2I][H] and down [H][I], NVFP4 each, plus two fp32 tensor scales
+    H, I = 2048, 512
+    gate_up = 2 * I * H // 2 + 2 * I * H // 16
+    down = H * I // 2 + H * I // 16
+    assert gate_up == 1048576 + 131072 and down == 524288 + 65536
+    assert bench.moe_expert_bytes(H, I) == gate_up + down + 8 == 1769480
+
+
+def test_moe_unique_experts_and_bytes():
+    # token 0 picks experts 0 and 2; token 1 has a tie between experts 1
+    # and 2 and picks both (2 slots): three distinct experts in all
+    logits = np.array([[3.0, 1.0, 2.0, 0.0], [0.0, 2.0, 2.0, 1.0]], dtype=np.float32)
+    assert bench.moe_unique_experts(logits, 2) == 3
+    assert bench.moe_unique_experts(logits, 1) == 2  # experts 0 and 1 (the tie goes to the lower index)
+    assert bench.moe_unique_experts(logits[:1], 4) == 4
+    T, E, H, I = 2, 4, 32, 32
+    assert bench.moe_bytes(T, E, H, I, 2, logits) == 3 * bench.moe_expert_bytes(H, I) + T * H * 2 + T * H * 4 + T * E * 4
+
+
+def test_whole_job_rate():
+    # every rank streams the step's bytes; the job's rate divides all ranks'
+    # bytes by the slowest rank's time
+    assert bench.whole_job_gbs(10**9, 2, 10, 4.0) == 5.0
+    assert bench.whole_job_gbs(10**9, 1, 1, 0.5) == 2.0
+    assert bench.max_over_ranks(1.25, 1, None) == 1.25
+
+
+def test_step_rows_cover_the_workload():
+    names = [n for n, _, _ in bench.rows_spec()]
+    assert names == ["nvfp4 12288x4096 N=1", "nvfp4 4096x12288 N=1", "nvfp4 4096x4096 N=1",
+                     "q8_0 12288x4096 N=1", "q8_0 4096x12288 N=1", "q8_0 151936x4096 N=1",
+                     "nvfp4 4096x4096 N=4", "nvfp4 4096x4096 N=8", "nvfp4 12288x4096 N=4",
+                     "nvfp4 12288x4096 N=8", "moe T=1", "moe T=16"]
+
+
+def test_traffic_record_lookup():
+    import json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    ent = rec["q8_0_gemv 151936x4096 N=1"]
+    assert ent["algorithmic_bytes"] == bench.q8_0_bytes(151936, 4096, 1)
+    # means of three launches, each rounded to a byte
+    assert abs(ent["dram_bytes_per_launch"] - (ent["dram_read"] + ent["dram_write"])) <= 1
+    # the hash covers the named sources in a fixed order
+    assert bench.source_sha(ent["sources"]) == bench.source_sha(list(reversed(ent["sources"])))
+    assert bench.source_sha(ent["sources"]) != bench.source_sha(ent["sources"][:1])
+    assert bench.profiled_traffic("no such kernel") is None
