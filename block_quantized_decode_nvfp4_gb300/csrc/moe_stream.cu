@@ -11,17 +11,17 @@
 // segment of the expert-major list, in increasing order) form one virtual
 // row space, cut into equal contiguous ranges, one per CTA (one CTA per SM).
 // Warp 0 streams a CTA's rows with 1-D bulk copies into a ring of shared-
-// memory stages (a stage never spans two experts); eight consumer warps
+// memory stages (a stage never spans two experts); sixteen consumer warps
 // multiply each stage by all of that expert's tokens, staged once per
 // expert in shared memory, so an expert's weights leave HBM once however
 // many tokens it has. A gate_up stage holds matching gate and up rows
 // (rows i and I + i of the expert), so h = SiLU(g) * u is formed at once;
 // the down stage multiplies by h.
 //
-// Device-side checks as in moe.cu: a token or slot id out of range sets bit
-// 2 of the status word and that pair's outputs are skipped; a CSR that is
-// not monotone sets bit 1 (reported by the gate_up kernel) and the
-// affected experts are skipped. Every wait is bounded.
+// Device-side checks as in moe.cu: a token or slot id out of range sets
+// BQD_MOE_BAD_PAIR in the status word and that pair's outputs are skipped; a
+// CSR that is not monotone sets BQD_MOE_BAD_OFFSETS (reported by the gate_up
+// kernel) and the affected experts are skipped. Every wait is bounded.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -55,8 +55,8 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Token-count class of a group of ng tokens (the compute loops are unrolled
-// for 1, 2, 4 or 8 tokens; staged rows past ng hold no token and their
-// results are dropped).
+// for 1, 2 or 4 tokens; staged rows past ng hold no token and their results
+// are dropped).
 __device__ __forceinline__ int tok_class(int ng) { return ng <= 1 ? 1 : (ng <= 2 ? 2 : 4); }
 
 // Relative cost of one row of an expert with ntok tokens: the decode (2)

@@ -154,8 +154,9 @@ bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x,
 
 /*
  * bqd_device_error -- waits for the device, copies the device error words of
- * the streaming and tensor-core kernels (BQD_PATH_STREAM, BQD_PATH_MMA) to
- * *bits_out (OR of the two) and clears them. Bit 0: a pipeline wait ran out
+ * the streaming and tensor-core GEMV kernels (BQD_PATH_STREAM, BQD_PATH_MMA)
+ * and of the MoE stream kernels to *bits_out (OR of the three) and clears
+ * them. Bit 0: a pipeline wait ran out
  * (the kernel gave up instead of hanging; its outputs are unspecified).
  * Returns BQD_ERR_DEVICE if any bit was set. Synchronising: do not call it
  * inside a stream capture.
