@@ -42,14 +42,19 @@ def round_e4m3(v: np.ndarray) -> np.ndarray:
     return torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
-def split_planes(x: np.ndarray, P: int) -> list:
-    """P residual NVFP4 planes of x [N][K] (K % 16 == 0), each an exact fp64 array."""
+def split_planes(x: np.ndarray, P: int, pow2_ts: bool = False) -> list:
+    """P residual NVFP4 planes of x [N][K] (K % 16 == 0), each an exact fp64
+    array. pow2_ts: each plane's tensor scale is rounded up to a power of
+    two (then every plane value and residual is exact in fp32 as well)."""
     N, K = x.shape
     r = x.copy()
     planes = []
     for _ in range(P):
         amax_tok = np.abs(r).max(axis=1, keepdims=True)
         ts = (amax_tok / (6.0 * 448.0)).astype(np.float32).astype(np.float64)
+        if pow2_ts:
+            with np.errstate(divide="ignore"):
+                ts = np.where(ts > 0, 2.0 ** np.ceil(np.log2(np.where(ts > 0, ts, 1.0))), 0.0)
         rb = r.reshape(N, K // 16, 16)
         amax_b = np.abs(rb).max(axis=2, keepdims=True)
         with np.errstate(divide="ignore", invalid="ignore"):
@@ -110,3 +115,20 @@ def test_split_planes_sum_exactly_to_x_in_the_limit():
     assert set(np.unique(round_e2m1(np.array([0.25, 0.75, 2.5, 5.0, 7.0, -1.25])))) <= set(
         np.concatenate([E2M1_VALUES, -E2M1_VALUES]))
     assert list(round_e2m1(np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]))) == [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0]
+
+
+def test_m2_power_of_two_plane_scales():
+    # the device-side choice: power-of-two tensor scales per plane. Every
+    # plane value and every residual is then exact in fp32, and three planes
+    # still meet the tolerance
+    W, x, y, tol = _workload()
+    acc = np.zeros_like(x)
+    ratios = []
+    for plane in split_planes(x, 4, pow2_ts=True):
+        acc = acc + plane
+        ratios.append(float((np.abs(acc @ W.T - y) / tol).max()))
+        assert np.array_equal(plane.astype(np.float32).astype(np.float64), plane)
+        r = x - acc
+        assert np.array_equal(r.astype(np.float32).astype(np.float64), r)
+    assert ratios[2] <= 1.0, ratios
+    print("pow2 ts, max err / tol for P = 1..4:", ["%.3g" % v for v in ratios])
