@@ -8,12 +8,10 @@ import torch
 import oracle
 import block_quantized_decode_nvfp4_gb300 as bqd
 from block_quantized_decode_nvfp4_gb300 import synthetic as syn
+from tests.bounds import abs_planes, moe_check, silu_up_spread
 from tests.gpu_util import assert_within, dev, need_gpu
 
 pytestmark = pytest.mark.gpu
-
-SILU_LIP = 1.1  # sup |d/dg SiLU(g)| = 1.0998 (attained near g = 2.4)
-
 
 @pytest.fixture(scope="module", autouse=True)
 def _gpu():
@@ -86,10 +84,6 @@ def _ws_h(ws, T, topk, I):
     return ws[start:start + 4 * P * I].view(torch.float32).cpu().numpy().reshape(P, I)
 
 
-def _abs_planes(codes, scales):
-    return codes & 0x77, scales & 0x7F  # |w| for non-negative scales: clear the sign bits
-
-
 @pytest.mark.parametrize("T", [1, 16])
 def test_moe_layer_full_size(T):
     L = syn.moe_layer(T=T, seed=0)
@@ -104,20 +98,19 @@ def test_moe_layer_full_size(T):
     for p in range(T * topk):
         t, s = ptok[p], pslot[p]
         e = sel[t, s]
-        g, u, h = parts["g"][t, s], parts["u"][t, s], parts["h"][t, s]
-        tg = 1e-3 * parts["ag"][t, s] + 1e-6
-        tu = 1e-3 * parts["au"][t, s] + 1e-6
-        sig = 1 / (1 + np.exp(-g))
-        dh = SILU_LIP * tg * (np.abs(u) + tu) + np.abs(g * sig) * tu + 1e-6 * np.abs(h) + 1e-30
+        h = parts["h"][t, s]
+        dh = silu_up_spread(parts["g"][t, s], parts["u"][t, s], h, parts["ag"][t, s], parts["au"][t, s]) + 1e-30
         # stage 1: h = SiLU(gate) * up within the propagated GEMV tolerance
         assert np.all(np.abs(h_gpu[p] - h) <= dh), f"h of pair {p}"
         # stage 2: down projection of the GPU's own h within the GEMV tolerance
         dc, dsc = L["dn_codes"][e], L["dn_scales"][e]
         d_gpu_h, a_gpu_h = oracle.nvfp4_gemv_f64x(dc, dsc, float(L["dn_ts"][e]), h_gpu[p].astype(np.float64), H, I)
-        ac, asc = _abs_planes(dc, dsc)
+        ac, asc = abs_planes(dc, dsc)
         spread, _ = oracle.nvfp4_gemv_f64x(ac, asc, abs(float(L["dn_ts"][e])), dh, H, I)  # |W_dn| . dh
         tol_y[t] += wref[t, s] * (spread[0] + 1e-3 * a_gpu_h[0] + 1e-6 + 1e-6 * np.abs(d_gpu_h[0]))
     assert_within(y, yref, tol_y, f"MoE y T={T}", rel=1.0, absol=0.0)
+    # end to end, from the oracle's stage values alone
+    moe_check(y, L, sel, wref, parts, yref, f"MoE y T={T} (propagated bound)")
 
 
 # I = 128 takes the register-streaming kernels, I = 256 the bulk-copy ones
@@ -131,10 +124,9 @@ def test_moe_deterministic_and_identical_experts(I):
     for k in ("gu_codes", "gu_scales", "dn_codes", "dn_scales"):
         L[k] = np.ascontiguousarray(np.broadcast_to(L[k][0], L[k].shape))
     y, _, _ = _layer_run(L)
-    yref, parts = oracle.moe_layer(L, want_parts=True)
     sel, w = oracle.moe_route(L["logits"], 4)
-    scale = np.einsum("ts,tsh->th", w, parts["ad"])
-    assert_within(y, yref, 3 * scale + 1e-5, "identical experts", rel=1e-3, absol=0.0)
+    yref, parts = oracle.moe_layer(L, sel=sel, weights=w, want_parts=True)
+    moe_check(y, L, sel, w, parts, yref, "identical experts")
 
 
 @pytest.mark.parametrize("I", [64, 256])
@@ -142,10 +134,9 @@ def test_moe_small_shapes_and_many_tokens_per_expert(I):
     # few experts, many tokens: token groups of 8 and more per expert
     L = syn.moe_layer(T=40, E=4, H=256, I=I, topk=2, seed=4)
     y, _, _ = _layer_run(L)
-    yref, parts = oracle.moe_layer(L, want_parts=True)
     sel, w = oracle.moe_route(L["logits"], 2)
-    scale = np.einsum("ts,tsh->th", w, parts["ad"])
-    assert_within(y, yref, 3 * scale + 1e-5, f"T=40 E=4 I={I}", rel=1e-3, absol=0.0)
+    yref, parts = oracle.moe_layer(L, sel=sel, weights=w, want_parts=True)
+    moe_check(y, L, sel, w, parts, yref, f"T=40 E=4 I={I}")
 
 
 @pytest.mark.parametrize("H,I", [(128, 64), (256, 256)])
