@@ -45,7 +45,7 @@ thread_local const char* t_last_cuda_error = "cudaSuccess";
 bqd_status from_cuda(cudaError_t e)
 {
     if (e == cudaSuccess) return BQD_OK;
-    t_last_cuda_error = cudaGetErrorName(e);
+    bqd::record_cuda_error(e);
     return BQD_ERR_LAUNCH;
 }
 
@@ -72,6 +72,11 @@ bqd_status check_dense(const void* a, const void* b, const void* x, const void* 
 }
 
 }  // namespace
+
+void bqd::record_cuda_error(cudaError_t e)
+{
+    if (e != cudaSuccess) t_last_cuda_error = cudaGetErrorName(e);
+}
 
 extern "C" {
 
@@ -159,6 +164,13 @@ bqd_status bqd_device_error(unsigned int* bits_out)
     v |= w | m;
     *bits_out = v;
     return v ? BQD_ERR_DEVICE : BQD_OK;
+}
+
+bqd_status bqd_debug_stream_fault(int withhold_last_stage, long long wait_limit_cycles)
+{
+    if (wait_limit_cycles < 0) return BQD_ERR_SHAPE;
+    bqd::set_stream_fault(withhold_last_stage, wait_limit_cycles);
+    return BQD_OK;
 }
 
 bqd_status nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tensor_scale, float* w, int64_t M,

@@ -10,6 +10,10 @@
 
 namespace bqd {
 
+// Records the name of a failed CUDA call as the calling thread's last CUDA
+// error (what bqd_last_cuda_error returns); cudaSuccess records nothing.
+void record_cuda_error(cudaError_t e);
+
 cudaError_t launch_nvfp4_gemv_cuda_core(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
                                         float* y, int64_t M, int64_t K, int N, cudaStream_t s);
 cudaError_t launch_q8_0_gemv_cuda_core(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
@@ -26,6 +30,8 @@ cudaError_t launch_q8_0_gemv_stream(const int8_t* q, const uint16_t* d, const ui
                                     int64_t K, cudaStream_t s);
 // Reads and clears the device error word of the streaming kernels (synchronous).
 cudaError_t read_and_clear_stream_error(unsigned int* out);
+// Failure-path test setting of the streaming kernel (bqd_debug_stream_fault).
+void set_stream_fault(int withhold_last, long long wait_limit);
 
 // Tensor-core GEMV (gemv_mma.cu): NVFP4, 1 <= N <= 16, K % 256 == 0.
 bool mma_gemv_supported(int64_t M, int64_t K, int N);

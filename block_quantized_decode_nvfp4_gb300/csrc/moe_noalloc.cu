@@ -11,8 +11,12 @@
 //
 // The array (kScratchBytes) exists on every GPU that loads the library, for
 // the life of the process. Host code cannot use the array's name as a
-// device address, so on the first call on a device (with that device
-// current) the address is looked up with cudaGetSymbolAddress and cached.
+// device address, so the address is looked up with cudaGetSymbolAddress, with
+// the device current, on the first call in each CUDA context, and cached
+// under that context's id. A device reset (cudaDeviceReset) destroys the
+// context and the module with it; the next call sees a new context id and
+// looks the address up again instead of using the freed one.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -29,44 +33,95 @@ constexpr size_t kScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_moe_scratch[kScratchBytes];
 
+// Driver entry points for the current context and its id, taken through the
+// runtime so that the library does not link the driver library itself.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+struct DriverFns {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+
+const DriverFns& driver_fns()
+{
+    static DriverFns fns = [] {
+        DriverFns f;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f.get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+        return f;
+    }();
+    return fns;
+}
+
+// Id of the calling thread's current context; 0 if there is none yet (the
+// runtime makes the device's primary context current lazily).
+unsigned long long current_context_id()
+{
+    const DriverFns& f = driver_fns();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!f.get_current || !f.get_id || f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (f.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
 struct DeviceScratch {
-    bool ready = false;
+    bool arch_known = false;
     bool sm103 = false;
+    unsigned long long ctx_id = 0;  // context the cached address belongs to (0: none)
     void* addr = nullptr;
 };
 
-// Per-device set-up, once: architecture check and the device address of the
-// scratch array (the device must be current).
+// Per-device set-up: architecture check (once) and the device address of the
+// scratch array in the current context (once per context). The device must
+// be current. CUDA failures are recorded for bqd_last_cuda_error().
 bqd_status scratch_for_current_device(void** out)
 {
     static std::mutex mu;
     static DeviceScratch cache[64];
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        bqd::record_cuda_error(e);
         cudaGetLastError();
         return BQD_ERR_ARCH;
     }
     std::lock_guard<std::mutex> g(mu);
     DeviceScratch& c = cache[dev];
-    if (!c.ready) {
+    if (!c.arch_known) {
         int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) {
+            bqd::record_cuda_error(e);
             cudaGetLastError();
             return BQD_ERR_ARCH;
         }
         c.sm103 = major == 10 && minor == 3;
-        if (c.sm103) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_moe_scratch) != cudaSuccess || p == nullptr) {
-                cudaGetLastError();
-                return BQD_ERR_LAUNCH;
-            }
-            c.addr = p;
-        }
-        c.ready = true;
+        c.arch_known = true;
     }
     if (!c.sm103) return BQD_ERR_ARCH;
+    const unsigned long long id = current_context_id();
+    if (id == 0 || id != c.ctx_id) {
+        // First call in this context (or no context current yet: the lookup
+        // below makes the device's primary context current).
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_moe_scratch)) != cudaSuccess || p == nullptr) {
+            bqd::record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+            cudaGetLastError();
+            return BQD_ERR_LAUNCH;
+        }
+        c.addr = p;
+        c.ctx_id = current_context_id();
+    }
     *out = c.addr;
     return BQD_OK;
 }
@@ -103,5 +158,7 @@ extern "C" bqd_status moe_grouped_gemv_noalloc(const uint8_t* gu_codes, const ui
     const cudaError_t e = bqd::launch_moe_grouped(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x,
                                                   expert_offsets, pair_token, pair_weight, pair_slot, y, ws, E, H,
                                                   I, T, topk, stream);
-    return e == cudaSuccess ? BQD_OK : BQD_ERR_LAUNCH;
+    if (e == cudaSuccess) return BQD_OK;
+    bqd::record_cuda_error(e);
+    return BQD_ERR_LAUNCH;
 }
