@@ -46,6 +46,7 @@ SIGNATURES = {
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "bqd_device_error": (_i32, [C.POINTER(C.c_uint)]),
+    "bqd_debug_stream_fault": (_i32, [_i32, C.c_longlong]),
     "nvfp4_dequant": (_i32, [_vp, _vp, _f32, _vp, _i64, _i64, _vp]),
     "q8_0_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
     "moe_route_topk": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
@@ -133,6 +134,12 @@ def bqd_device_error() -> int:
     if st not in (BQD_OK, 8):
         raise BqdError(st, "bqd_device_error")
     return out.value
+
+
+def debug_stream_fault(withhold_last_stage: bool, wait_limit_cycles: int = 0) -> None:
+    """Failure-path test switch of the streaming GEMV kernel (see bqd.h)."""
+    _check(lib().bqd_debug_stream_fault(1 if withhold_last_stage else 0, wait_limit_cycles),
+           "bqd_debug_stream_fault")
 
 
 def nvfp4_dequant(codes, scales, tensor_scale, w, M, K, stream=None):

@@ -27,6 +27,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "gemv.h"
@@ -188,7 +189,8 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 template <class F>
 __global__ void __launch_bounds__(kThreadsS, 1)
     gemv_stream_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, float ts,
-                       const uint16_t* __restrict__ x, float* __restrict__ y, int64_t M, int64_t K, int rs, int ns)
+                       const uint16_t* __restrict__ x, float* __restrict__ y, int64_t M, int64_t K, int rs, int ns,
+                       long long wait_limit, int withhold_last)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_emax, s_emin, s_flags;
@@ -226,10 +228,12 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         int64_t issued = 0;
         for (int64_t t = 0; t < nstages; ++t) {
             const int slot = static_cast<int>(t % ns);
-            if (t >= ns) ok = mbar_wait(&empty[slot], static_cast<uint32_t>(((t / ns) - 1) & 1), &g_stream_error);
-            if (t == kInitStagesS && ok) ok = mbar_wait(&xready, 0u, &g_stream_error);
+            if (t >= ns)
+                ok = mbar_wait(&empty[slot], static_cast<uint32_t>(((t / ns) - 1) & 1), &g_stream_error, wait_limit);
+            if (t == kInitStagesS && ok) ok = mbar_wait(&xready, 0u, &g_stream_error, wait_limit);
             ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
+            if (withhold_last && t == nstages - 1) break;  // failure-path test: this stage never arrives
             const int64_t row0 = r_lo + t * rs;
             const int rows = static_cast<int>(r_hi - row0 < rs ? r_hi - row0 : rs);
             unsigned char* st = ring + slot * stage_bytes;
@@ -245,7 +249,8 @@ __global__ void __launch_bounds__(kThreadsS, 1)
         if (lane == 0) {
             const int64_t first = issued > ns ? issued - ns : 0;
             for (int64_t t = first; t < issued; ++t)
-                if (!mbar_wait(&full[t % ns], static_cast<uint32_t>((t / ns) & 1), &g_stream_error)) break;
+                if (!mbar_wait(&full[t % ns], static_cast<uint32_t>((t / ns) & 1), &g_stream_error, wait_limit))
+                    break;
         }
         return;
     }
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     bool ok = true;
     for (int64_t t = 0; t < nstages; ++t) {
         const int slot = static_cast<int>(t % ns);
-        if (ok) ok = mbar_wait(&full[slot], static_cast<uint32_t>((t / ns) & 1), &g_stream_error);
+        if (ok) ok = mbar_wait(&full[slot], static_cast<uint32_t>((t / ns) & 1), &g_stream_error, wait_limit);
         ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
         const int64_t row0 = r_lo + t * rs;
         const int rows = static_cast<int>(r_hi - row0 < rs ? r_hi - row0 : rs);
@@ -350,6 +355,21 @@ __global__ void __launch_bounds__(kThreadsS, 1)
     }
 }
 
+// Failure-path test setting (bqd_debug_stream_fault): wait limit of the
+// kernel's bounded waits, and whether the producer withholds the last stage.
+struct StreamFault {
+    long long wait_limit = kWaitCycles;
+    int withhold_last = 0;
+};
+std::mutex g_fault_mu;
+StreamFault g_fault;
+
+StreamFault stream_fault()
+{
+    std::lock_guard<std::mutex> g(g_fault_mu);
+    return g_fault;
+}
+
 template <class F>
 cudaError_t launch_stream(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
                           int64_t M, int64_t K, cudaStream_t stream)
@@ -383,7 +403,8 @@ cudaError_t launch_stream(const uint8_t* codes, const uint8_t* scales, float ts,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = launch_flags() & kLaunchPdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, codes, scales, ts, x, y, M, K, rs, ns);
+    const StreamFault f = stream_fault();
+    return cudaLaunchKernelEx(&cfg, kern, codes, scales, ts, x, y, M, K, rs, ns, f.wait_limit, f.withhold_last);
 }
 
 }  // namespace
@@ -405,6 +426,13 @@ cudaError_t launch_q8_0_gemv_stream(const int8_t* q, const uint16_t* d, const ui
 {
     return launch_stream<FmtQ8>(reinterpret_cast<const uint8_t*>(q), reinterpret_cast<const uint8_t*>(d), 1.0f, x,
                                 y, M, K, s);
+}
+
+void set_stream_fault(int withhold_last, long long wait_limit)
+{
+    std::lock_guard<std::mutex> g(g_fault_mu);
+    g_fault.withhold_last = withhold_last ? 1 : 0;
+    g_fault.wait_limit = wait_limit > 0 ? wait_limit : kWaitCycles;
 }
 
 cudaError_t read_and_clear_stream_error(unsigned int* out)

@@ -59,13 +59,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 // after setting kErrWaitTimeout in *err. try_wait itself suspends the thread
 // until the phase completes or a short hardware time limit passes, so the
 // loop needs no sleep of its own (a sleep only delays the wake-up).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                          long long limit = kWaitCycles)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     do {
         if (mbar_try_wait(bar, parity)) return true;
-    } while (clock64() - t0 < kWaitCycles);
+    } while (clock64() - t0 < limit);
     atomicOr(err, kErrWaitTimeout);
     return false;
 }

@@ -24,8 +24,9 @@
  * Conventions for every call:
  *  - All array pointers are DEVICE pointers owned by the caller. The library
  *    never allocates, frees or prints, and never synchronises except in
- *    bqd_moe_read_status. Work is enqueued on `stream` (0 = legacy default
- *    stream) in stream order; calls return before the GPU finishes.
+ *    the two status readers, bqd_moe_read_status and bqd_device_error. Work
+ *    is enqueued on `stream` (0 = legacy default stream) in stream order;
+ *    calls return before the GPU finishes.
  *  - Arrays are dense, row-major, innermost index contiguous, and every base
  *    pointer must be 16-byte aligned.
  *  - Activations are bf16 bit patterns, token-major: x[n][k], row pitch K.
@@ -164,6 +165,20 @@ bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x,
 bqd_status bqd_device_error(unsigned int* bits_out);
 
 /*
+ * bqd_debug_stream_fault -- a switch for testing the failure path of the
+ * streaming GEMV kernel (BQD_PATH_STREAM), not for production use. With
+ * withhold_last_stage != 0, each CTA's producer stops before issuing the
+ * copy of its last ring stage, so the consumer warps' wait for it can only
+ * run out: they give up after wait_limit_cycles SM clock cycles, set bit 0
+ * of the device error word (bqd_device_error) and leave that stage's rows
+ * unwritten. No copy is in flight when they give up. wait_limit_cycles = 0
+ * restores the default limit (2^31 cycles, about one second);
+ * withhold_last_stage = 0 restores normal operation. Process-wide; affects
+ * calls made after it returns. Returns BQD_ERR_SHAPE for a negative limit.
+ */
+bqd_status bqd_debug_stream_fault(int withhold_last_stage, long long wait_limit_cycles);
+
+/*
  * nvfp4_dequant -- w[m][k] = fl32(e2m1(c[m][k]) * e4m3(s[m][k/16]) * ts),
  * the dequantised weight rounded once to fp32 (bit-exact). Uses the same
  * device decoders as the GEMV. w fp32 [M][K]. Shape rules as nvfp4_gemv.
@@ -231,6 +246,11 @@ bqd_status moe_grouped_gemv(const uint8_t* gu_codes, const uint8_t* gu_scales, c
  * before touching the GPU. The library allocates nothing on this path.
  * The first call on each device (with that device current) looks up the
  * array's device address; make that first call before any stream capture.
+ * The address is cached per CUDA context: after cudaDeviceReset (or any
+ * other way the context is destroyed and created again) the next call looks
+ * it up again, so that call too should come before any stream capture.
+ * A failed lookup or launch returns BQD_ERR_LAUNCH and records the CUDA
+ * error's name for bqd_last_cuda_error().
  * Every call shares the one array: calls that may run at the same time on
  * the GPU (other streams, other threads) race and give unspecified results.
  * The array keeps the last call's contents; whatever a call needs zeroed it

@@ -223,3 +223,48 @@ def test_pdl_output_may_overwrite_previous_input(pdl_on):
         bqd.nvfp4_gemv(dev(wb["codes"]), dev(wb["scales"]), wb["ts"], dev(wb["x"]), shared, K // 2, 4096, 1)
         torch.cuda.synchronize()
         assert_within(ya.cpu().numpy()[None], ref_a, a_a, "A under PDL")
+
+
+# ---------------------------------------------------------------- N = 1 stream kernel, exact invariants
+def test_stream_n1_exact_invariants():
+    """Through BQD_PATH_STREAM at N = 1 (the decode hot path): a one-hot x
+    gives the dequantised column bit for bit; a one-hot x of 3 gives the
+    exact product rounded once; sign flip negates exactly; zero codes give
+    zero; ts = 2 doubles exactly."""
+    M, K = 1000, 4096
+    P = bqd.BQD_PATH_STREAM
+    w = syn.dense_nvfp4(M, K, N=1, seed=12)
+    W = oracle.nvfp4_dequant(w["codes"], w["scales"], w["ts"], M, K, dtype=np.float32)
+    for k in (0, 1, 15, 16, 255, 256, 2047, 4095):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k] = 0x3F80  # 1.0
+        assert np.array_equal(run(dict(w, x=x), path=P)[0], W[:, k]), f"one-hot k={k}"
+        x[0, k] = 0x4040  # 3.0
+        ref, _ = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], x, M, K)
+        assert np.array_equal(run(dict(w, x=x), path=P)[0], ref[0].astype(np.float32)), f"one-hot 3 k={k}"
+    y = run(w, path=P)
+    assert np.array_equal(run(dict(w, codes=w["codes"] ^ 0x88), path=P), -y)
+    assert np.all(run(dict(w, codes=np.zeros_like(w["codes"])), path=P) == 0)
+    y1 = run(dict(w, ts=1.0), path=P)
+    assert np.array_equal(run(dict(w, ts=2.0), path=P), 2 * y1)
+
+
+def test_stream_bounded_wait_gives_up_and_reports():
+    """Failure path without a GPU fault: the producer withholds each CTA's last
+    ring stage (no copy of it is ever issued), so the consumers' bounded wait
+    for it runs out after 2^20 cycles; the call completes, bit 0 of the
+    device error word is set, a second read finds it cleared, and the next
+    normal call is correct."""
+    M, K = 2000, 4096
+    w = syn.dense_nvfp4(M, K, N=1, seed=15)
+    assert bqd.bqd_device_error() == 0
+    bqd.debug_stream_fault(True, 1 << 20)
+    try:
+        run(w, path=bqd.BQD_PATH_STREAM)  # returns: the waits gave up instead of hanging
+        torch.cuda.synchronize()
+    finally:
+        bqd.debug_stream_fault(False, 0)
+    assert bqd.bqd_device_error() & 1
+    assert bqd.bqd_device_error() == 0
+    ref, a = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], w["x"], M, K)
+    assert_within(run(w, path=bqd.BQD_PATH_STREAM), ref, a, "after the failure test")

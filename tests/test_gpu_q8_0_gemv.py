@@ -116,3 +116,34 @@ def test_stream_and_cuda_core_paths_match_oracle(M, K):
         out = Guarded(M)
         bqd.q8_0_gemv_path(dev(w["q"]), dev(w["d"]), dev(w["x"]), out.ptr, M, K, 1, path)
         assert_within(out.get()[None], ref, a, f"{M}x{K} path {path}")
+
+
+# ---------------------------------------------------------------- N = 1 stream kernel, exact invariants
+def _run_path(w, path, q=None, x=None):
+    M, K = w["M"], w["K"]
+    xx = w["x"] if x is None else x
+    out = Guarded(M)
+    bqd.q8_0_gemv_path(dev(w["q"] if q is None else q), dev(w["d"]), dev(xx), out.ptr, M, K, 1, path)
+    return out.get()
+
+
+def test_stream_n1_extremes_and_exact_invariants():
+    """Through BQD_PATH_STREAM at N = 1: blocks of q = -128 and 127 within the
+    tolerance; a one-hot x gives the dequantised column bit for bit;
+    negating q negates y exactly."""
+    M, K = 700, 4096
+    P = bqd.BQD_PATH_STREAM
+    w = syn.dense_q8_0(M, K, N=1, seed=13)
+    w["q"][:, :64] = -128
+    w["q"][:, 64:128] = 127
+    ref, a = oracle.q8_0_gemv(w["q"], w["d"], w["x"], M, K)
+    assert_within(_run_path(w, P)[None], ref, a, "stream int8 extremes")
+    W = oracle.q8_0_dequant(w["q"], w["d"], M, K, dtype=np.float32)
+    for k in (0, 31, 32, 63, 64, 100, 2048, 4095):
+        x = np.zeros((1, K), dtype=np.uint16)
+        x[0, k] = 0x3F80
+        assert np.array_equal(_run_path(w, P, x=x), W[:, k]), f"one-hot k={k}"
+    q3 = w["q"].copy()
+    q3[:, :64] = 0  # -128 has no int8 negation
+    q2 = (-q3.astype(np.int16)).astype(np.int8)
+    assert np.array_equal(_run_path(w, P, q=q2), -_run_path(w, P, q=q3))
