@@ -12,6 +12,13 @@ The metric is algorithmic HBM bytes (packed weights + scales + activations +
 outputs; MoE: the experts the routing actually selects) per second; a step
 touches ~1.1 GB, far more than L2, so successive steps read from HBM.
 
+Per row, beside the step: an isolated call after an L2 flush, and calls back
+to back (200 graph-captured calls cycling through weight copies whose calls
+stream more than 3x L2), each as GB/s and a fraction of the measured HBM
+copy peak, with the row's ncu DRAM traffic where a record of the current
+kernel sources exists. The 256 x 512 NVFP4 workload is reported the same way
+but is not part of the step.
+
 Printed: one JSON line (rank 0). `--impl reference` times the fp64 CPU
 oracle on a bounded sample of the same workload instead.
 """
@@ -79,7 +86,15 @@ def rows_spec():
     return rows
 
 
+def extra_rows_spec():
+    """Rows reported beside the step but not part of it: the tiny 256 x 512
+    NVFP4 workload (ts = 1.0), whose time is launch latency, not bandwidth."""
+    return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1))]
+
+
 def host_inputs(kind, p, seed=0):
+    if kind == "nvfp4_tiny":
+        return syn.tiny_nvfp4(seed=seed)
     if kind == "nvfp4":
         return syn.dense_nvfp4(p["M"], p["K"], N=p["N"], seed=seed)
     if kind == "q8_0":
@@ -88,7 +103,7 @@ def host_inputs(kind, p, seed=0):
 
 
 def row_bytes(kind, p, host):
-    if kind == "nvfp4":
+    if kind in ("nvfp4", "nvfp4_tiny"):
         return nvfp4_bytes(p["M"], p["K"], p["N"])
     if kind == "q8_0":
         return q8_0_bytes(p["M"], p["K"], p["N"])
@@ -169,18 +184,27 @@ def source_sha(files=None):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+def profiled_traffic(row_key):
+    """DRAM bytes per call of a row (all its kernels) from the committed ncu
+    record, if it was taken on the current kernel sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    ent = d.get(kernel_key)
+    ent = d.get(row_key)
     if not ent or ent.get("source_sha") != source_sha(ent.get("sources")):
         return None
     return ent.get("dram_bytes_per_launch")
+
+
+def rotating_copies(call_bytes, weight_bytes, l2, mem_budget):
+    """Weight copies that a back-to-back loop cycles through so that a call's
+    weights are out of L2 when they come round again: the working set of
+    the copies' calls must exceed 3x L2 (at least 2 copies, within budget)."""
+    r = math.ceil(3 * l2 / max(1, call_bytes)) + 1
+    r = min(r, max(2, mem_budget // max(1, weight_bytes)))
+    return max(2, r)
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -211,9 +235,9 @@ class Row:
         self.torch, self.bqd = torch, bqd
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
         self.launches = 1
-        if kind in ("nvfp4", "q8_0"):
+        if kind in ("nvfp4", "q8_0", "nvfp4_tiny"):
             M, K, N = p["M"], p["K"], p["N"]
-            if kind == "nvfp4":
+            if kind != "q8_0":
                 self.w = (d(host["codes"]), d(host["scales"]))
                 self.ts = host["ts"]
             else:
@@ -238,22 +262,32 @@ class Row:
             self.launches = 4  # route, gate_up, down, combine
             self.in_bytes = self.x.numel() * 2 + self.logits.numel() * 4
         self.out_bytes = self.y.numel() * 4
+        self.weight_bytes = sum(t.numel() * t.element_size() for t in self.w)
+        self.copies = [self.w]
+
+    def make_copies(self, n):
+        """n device copies of the weights in all (the original included)."""
+        self.copies = [self.w] + [tuple(t.clone() for t in self.w) for _ in range(n - 1)]
+
+    def drop_copies(self):
+        self.copies = [self.w]
 
     def run_path(self, path):
         """The NVFP4 GEMV of this row through an explicit compute path."""
         p = self.p
         self.bqd.nvfp4_gemv_path(self.w[0], self.w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"], path)
 
-    def run(self):
+    def run(self, copy=0):
         p, b = self.p, self.bqd
-        if self.kind == "nvfp4":
-            b.nvfp4_gemv(self.w[0], self.w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"])
+        w = self.copies[copy]
+        if self.kind in ("nvfp4", "nvfp4_tiny"):
+            b.nvfp4_gemv(w[0], w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "q8_0":
-            b.q8_0_gemv(self.w[0], self.w[1], self.x, self.y, p["M"], p["K"], p["N"])
+            b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         else:
             T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
             b.moe_route_topk(self.logits, T, E, k, self.off, self.ptok, self.pw, self.pslot)
-            b.moe_grouped_gemv(*self.w, self.x, self.off, self.ptok, self.pw, self.pslot, self.y, self.ws, self.wsb,
+            b.moe_grouped_gemv(*w, self.x, self.off, self.ptok, self.pw, self.pslot, self.y, self.ws, self.wsb,
                                E, H, I, T, k)
 
 
@@ -291,9 +325,18 @@ def cpu_units(rows):
     return out
 
 
+def _sample_plan(units, costs, cpu_seconds):
+    """The same leading fraction of every row's remaining units, sized so the
+    estimated CPU time (per-row unit cost x units) is cpu_seconds."""
+    rest = sum(c * (len(u) - 1) for c, (_, u) in zip(costs, units))
+    frac = 0.0 if rest <= 0 else max(0.0, min(1.0, cpu_seconds / rest))
+    return frac, [1 + int(math.floor((len(u) - 1) * frac)) for _, u in units]
+
+
 def cpu_baseline_sample(units, budget_s):
-    """The same leading fraction of every row's units, sized to ~budget_s
-    from a timing of each row's first unit (which is part of the sample)."""
+    """One host core: the first unit of every row (timed, which gives the
+    per-row unit cost) plus the same leading fraction of every row's other
+    units, ~budget_s in all. Returns (bytes, seconds, description, costs)."""
     done_b, secs = 0, 0.0
     cost = []
     for _, u in units:
@@ -304,12 +347,8 @@ def cpu_baseline_sample(units, budget_s):
         secs += dt
         done_b += nb
         cost.append(max(dt, 1e-5))
-    rest = sum(c * (len(u) - 1) for c, (_, u) in zip(cost, units))
-    frac = 0.0 if rest <= 0 else max(0.0, min(1.0, (budget_s - secs) / rest))
-    taken = []
-    for _, u in units:
-        take = 1 + int(math.floor((len(u) - 1) * frac))
-        taken.append(take)
+    frac, taken = _sample_plan(units, cost, budget_s - secs)
+    for (_, u), take in zip(units, taken):
         for f, nb in u[1:take]:
             t0 = time.perf_counter()
             f()
@@ -318,7 +357,45 @@ def cpu_baseline_sample(units, budget_s):
     desc = (f"fp64 C oracle on 1 host core: the first unit of every row plus the first {frac:.4f} of the "
             f"remaining work units of every row (GEMV unit: 64 weight rows; MoE unit: one routed (token, slot) "
             f"pair); {sum(taken)} of {sum(len(u) for _, u in units)} units")
-    return done_b, secs, desc
+    return done_b, secs, desc, cost
+
+
+def cpu_baseline_all_cores(units, costs, budget_s, workers):
+    """All host cores: the oracle's work units run by `workers` threads (the
+    oracle's C calls release the interpreter lock), the leading fraction of
+    every row sized to ~budget_s of wall time. Returns (bytes, wall seconds,
+    description)."""
+    from concurrent.futures import ThreadPoolExecutor
+    frac, taken = _sample_plan(units, costs, budget_s * workers)
+    work = [u[i] for (_, u), take in zip(units, taken) for i in range(take)]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda fu: fu[0](), work))
+    wall = time.perf_counter() - t0
+    desc = (f"fp64 C oracle on {workers} host threads (one per core): the first {frac:.4f} of every row's work "
+            f"units (GEMV unit: 64 weight rows; MoE unit: one routed (token, slot) pair); {len(work)} of "
+            f"{sum(len(u) for _, u in units)} units")
+    return sum(nb for _, nb in work), wall, desc
+
+
+def host_cpu_info():
+    """Core count and CPU model of this host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    return {"nproc": os.cpu_count(), "model": model}
 
 
 def run_reference(args, rank):
@@ -384,6 +461,7 @@ def run_ours(args, rank, world):
     spec = rows_spec()
     hosts = {n: host_inputs(k, p, seed=0) for n, k, p in spec}
     rows = [Row(n, k, p, hosts[n], torch, bqd) for n, k, p in spec]
+    extra = [Row(n, k, p, host_inputs(k, p, seed=0), torch, bqd) for n, k, p in extra_rows_spec()]
     step_bytes = sum(r.bytes for r in rows)
     launches_per_step = sum(r.launches for r in rows)
     dominant = next(r for r in rows if r.name.startswith("q8_0 151936"))
@@ -391,7 +469,7 @@ def run_ours(args, rank, world):
 
     # warm-up (also performs the library's one-time per-kernel setup)
     for _ in range(max(3, args.warmup)):
-        for r in rows:
+        for r in rows + extra:
             r.run()
     torch.cuda.synchronize()
 
@@ -411,7 +489,39 @@ def run_ours(args, rank, world):
                 ts.append(e0.elapsed_time(e1) * 1e3)  # us
         return statistics.median(ts)
 
-    per_row = [(r, isolated_us(r.run)) for r in rows]
+    per_row = [(r, isolated_us(r.run)) for r in rows + extra]
+
+    # ---- per-row back-to-back timings: 200 calls captured in a CUDA graph,
+    # cycling through weight copies whose calls' working set exceeds 3x L2
+    def back_to_back_us(r, n_calls=200, reps=10):
+        R = rotating_copies(r.bytes, r.weight_bytes, l2, args.copy_budget_gb * 1e9)
+        r.make_copies(R)
+        for i in range(R):
+            r.run(i)
+        torch.cuda.synchronize()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for i in range(n_calls):
+                r.run(i % R)
+        ts = []
+        with torch.cuda.stream(cs):
+            for rep in range(reps + 2):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(cs)
+                g.replay()
+                e1.record(cs)
+                e1.synchronize()
+                if rep >= 2:
+                    ts.append(e0.elapsed_time(e1) * 1e3 / n_calls)
+        del g
+        r.drop_copies()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        return statistics.median(ts), R
+
+    b2b = {r.name: back_to_back_us(r) for r in rows + extra}
     # the multi-token (verify) rows through both compute paths
     verify_paths = {}
     for r in rows:
@@ -478,23 +588,36 @@ def run_ours(args, rank, world):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         units = cpu_units([(r.name, r.kind, r.p, hosts[r.name]) for r in rows])
-        b, s, desc = cpu_baseline_sample(units, args.cpu_budget)
-        cpu = {"value": b / s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+        b1, s1, desc1, costs = cpu_baseline_sample(units, args.cpu_budget)
+        info = host_cpu_info()
+        workers = info["nproc"] or 1
+        bn, sn, descn = cpu_baseline_all_cores(units, costs, args.cpu_budget, workers)
+        cpu = {"value": bn / sn / 1e9, "unit": "GB/s", "cores": workers, "kind": "oracle", "sample": descn,
+               "single_core": {"value": b1 / s1 / 1e9, "unit": "GB/s", "cores": 1, "sample": desc1},
+               "host": info}
 
     if rank != 0:
         return
     ms = elapsed_s / args.steps * 1e3
     value = whole_job_gbs(step_bytes, world, args.steps, elapsed_s)
-    traffic = profiled_traffic("q8_0_gemv 151936x4096 N=1")
+    traffic = profiled_traffic(dominant.name)
     breakdown = {}
     for r, us in per_row:
         gbs = r.bytes / us / 1e3
+        bus, copies = b2b[r.name]
+        bgbs = r.bytes / bus / 1e3
         ent = {"us_per_call": round(us, 3), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / peak, 4),
-               "bytes": r.bytes}
+               "b2b_us_per_call": round(bus, 3), "b2b_GB_s": round(bgbs, 1), "b2b_frac_hbm": round(bgbs / peak, 4),
+               "b2b_weight_copies": copies, "bytes": r.bytes, "in_step": r in rows}
+        tr = profiled_traffic(r.name)
+        ent["traffic"] = tr
+        ent["traffic_ratio"] = None if tr is None else round(tr / r.bytes, 4)
         if r.kind == "moe":
             ent["us_per_token"] = round(us / r.p["T"], 3)
+            ent["b2b_us_per_token"] = round(bus / r.p["T"], 3)
         else:
             ent["tokens_per_s_equiv"] = round(r.p["N"] * 1e6 / us, 1)
+            ent["b2b_tokens_per_s_equiv"] = round(r.p["N"] * 1e6 / bus, 1)
         breakdown[r.name] = ent
     dom_gbs = dominant.bytes / dom_us / 1e3
     line = {
@@ -503,9 +626,11 @@ def run_ours(args, rank, world):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded; the method's workload shapes)",
         "config": {"workload": WORKLOAD, "step_bytes": step_bytes, "launch_pdl": args.launch_pdl,
                    "l2": f"inputs larger than L2: one step streams {step_bytes / 1e9:.2f} GB vs L2 "
-                         f"{l2 / 2**20:.0f} MiB; per-row figures flush L2 with a read sweep before each call",
+                         f"{l2 / 2**20:.0f} MiB; per-row isolated figures flush L2 with a read sweep before "
+                         f"each call; per-row back-to-back figures replay 200 graph-captured calls cycling "
+                         f"through weight copies whose calls stream more than 3x L2",
                    "formats": "NVFP4 (E2M1 + E4M3/16 + fp32 ts), Q8_0 (int8 + fp16/32); bf16 x; fp32 accumulate"},
-        "roofline": {"bound": "hbm", "kernel": "q8_0_gemv 151936x4096 N=1", "achieved": round(dom_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": dominant.name, "achieved": round(dom_gbs, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": dominant.bytes},
         "rows": breakdown,
@@ -529,7 +654,7 @@ def run_profile_row(args):
     from block_quantized_decode_nvfp4_gb300 import build as _build
 
     _build.build()
-    spec = {n: (k, p) for n, k, p in rows_spec()}
+    spec = {n: (k, p) for n, k, p in rows_spec() + extra_rows_spec()}
     if args.profile_row not in spec:
         raise SystemExit(f"unknown row {args.profile_row!r}; rows: {sorted(spec)}")
     kind, p = spec[args.profile_row]
@@ -547,6 +672,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--copy-budget-gb", type=float, default=40.0,
+                    help="device memory for the weight copies of one row's back-to-back timing")
     ap.add_argument("--launch-pdl", choices=["on", "off"], default="on",
                     help="programmatic dependent launch between the step's kernels (BQD_LAUNCH_PDL)")
     ap.add_argument("--profile-row", default=None,

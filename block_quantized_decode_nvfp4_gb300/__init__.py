@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     get_launch_flags,
     set_launch_flags,
     bqd_device_error,
+    debug_stream_fault,
     BqdError,
     bqd_moe_read_status,
     lib,

@@ -62,11 +62,26 @@ def test_traffic_record_lookup():
     import json
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         rec = json.load(f)
-    ent = rec["q8_0_gemv 151936x4096 N=1"]
-    assert ent["algorithmic_bytes"] == bench.q8_0_bytes(151936, 4096, 1)
-    # means of three launches, each rounded to a byte
-    assert abs(ent["dram_bytes_per_launch"] - (ent["dram_read"] + ent["dram_write"])) <= 1
-    # the hash covers the named sources in a fixed order
-    assert bench.source_sha(ent["sources"]) == bench.source_sha(list(reversed(ent["sources"])))
-    assert bench.source_sha(ent["sources"]) != bench.source_sha(ent["sources"][:1])
+    rows = {n: (k, p) for n, k, p in bench.rows_spec() + bench.extra_rows_spec()}
+    assert rec, "no traffic record"
+    for name, ent in rec.items():
+        assert name in rows, f"traffic record {name!r} is not a bench row"
+        kind, p = rows[name]
+        if kind == "q8_0":
+            assert ent["algorithmic_bytes"] == bench.q8_0_bytes(p["M"], p["K"], p["N"])
+        elif kind.startswith("nvfp4"):
+            assert ent["algorithmic_bytes"] == bench.nvfp4_bytes(p["M"], p["K"], p["N"])
+        # per-call means, each rounded to a byte
+        assert abs(ent["dram_bytes_per_launch"] - (ent["dram_read"] + ent["dram_write"])) <= 1
+        # the hash covers the named sources in a fixed order
+        assert bench.source_sha(ent["sources"]) == bench.source_sha(list(reversed(ent["sources"])))
+        assert bench.source_sha(ent["sources"]) != bench.source_sha(ent["sources"][:1])
     assert bench.profiled_traffic("no such kernel") is None
+
+
+def test_rotating_copies_exceed_three_l2():
+    l2 = 129 * 2**20
+    for call_bytes, weight_bytes in ((28_368_900, 28_311_552), (661_841_408, 661_225_472), (14_170_000, 453e6)):
+        r = bench.rotating_copies(call_bytes, weight_bytes, l2, 40e9)
+        assert r >= 2 and (r - 1) * call_bytes > 3 * l2
+    assert bench.rotating_copies(10**6, 10**10, l2, 40e9) == 4  # capped by the memory budget, at least 2
