@@ -71,6 +71,14 @@ def moe_bytes(T, E, H, I, topk, logits):
     return (moe_unique_experts(logits, topk) * moe_expert_bytes(H, I) + T * H * 2 + T * H * 4 + T * E * 4)
 
 
+def moe_launches(T, E, H, I, topk):
+    """Kernel launches of one moe_layer call: the two small-batch kernels
+    (routing inside them, combine inside the down kernel) for a few tokens,
+    else route, gate_up, down and combine (plus the status word's memset)."""
+    small = (T <= 4 and T * topk <= 32 and E <= 512 and H % 1024 == 0 and H <= 8192 and I in (256, 512, 1024))
+    return 2 if small else 4
+
+
 def rows_spec():
     """(name, kind, params) of every row of a step, in step order."""
     rows = []
@@ -251,15 +259,10 @@ class Row:
             self.w = tuple(d(host[n]) for n in ("gu_codes", "gu_scales", "gu_ts", "dn_codes", "dn_scales", "dn_ts"))
             self.x_host, self.logits_host = host["x"], host["logits"]
             self.x, self.logits = d(host["x"]), d(host["logits"])
-            P = T * k
-            self.off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
-            self.ptok = torch.empty(P, dtype=torch.int32, device="cuda")
-            self.pw = torch.empty(P, dtype=torch.float32, device="cuda")
-            self.pslot = torch.empty(P, dtype=torch.int32, device="cuda")
-            self.wsb = bqd.moe_workspace_bytes(T, k, H, I)
+            self.wsb = bqd.moe_layer_workspace_bytes(T, k, H, I, E)
             self.ws = torch.empty(self.wsb, dtype=torch.uint8, device="cuda")
             self.y = torch.empty(T * H, dtype=torch.float32, device="cuda")
-            self.launches = 4  # route, gate_up, down, combine
+            self.launches = moe_launches(T, E, H, I, k)
             self.in_bytes = self.x.numel() * 2 + self.logits.numel() * 4
         self.out_bytes = self.y.numel() * 4
         self.weight_bytes = sum(t.numel() * t.element_size() for t in self.w)
@@ -286,9 +289,7 @@ class Row:
             b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         else:
             T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
-            b.moe_route_topk(self.logits, T, E, k, self.off, self.ptok, self.pw, self.pslot)
-            b.moe_grouped_gemv(*w, self.x, self.off, self.ptok, self.pw, self.pslot, self.y, self.ws, self.wsb,
-                               E, H, I, T, k)
+            b.moe_layer(self.logits, *w, self.x, self.y, self.ws, self.wsb, E, H, I, T, k)
 
 
 # ---------------------------------------------------------------- CPU oracle arms

@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     BQD_LAUNCH_PDL,
     BQD_PATH_STREAM,
     BQD_PATH_MMA,
+    BQD_PATH_DIRECT,
     get_launch_flags,
     set_launch_flags,
     bqd_device_error,
@@ -21,6 +22,8 @@ from ._binding import (  # noqa: F401
     lib,
     moe_grouped_gemv,
     moe_grouped_gemv_noalloc,
+    moe_layer,
+    moe_layer_workspace_bytes,
     moe_route_topk,
     moe_workspace_bytes,
     nvfp4_dequant,

@@ -20,6 +20,7 @@ BQD_PATH_AUTO = 0
 BQD_PATH_CUDA_CORE = 1
 BQD_PATH_STREAM = 2
 BQD_PATH_MMA = 3
+BQD_PATH_DIRECT = 4
 BQD_LAUNCH_PDL = 1
 
 _lib = None
@@ -54,6 +55,8 @@ SIGNATURES = {
     "moe_grouped_gemv": (_i32, [_vp] * 13 + [_sz, _i32, _i32, _i32, _i32, _i32, _vp]),
     "bqd_moe_read_status": (_i32, [_vp, C.POINTER(C.c_int32), _vp]),
     "moe_grouped_gemv_noalloc": (_i32, [_vp] * 12 + [_i32, _i32, _i32, _i32, _i32, _vp]),
+    "moe_layer": (_i32, [_vp] * 10 + [_sz, _i32, _i32, _i32, _i32, _i32, _vp]),
+    "moe_layer_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
 }
 
 
@@ -175,6 +178,18 @@ def moe_grouped_gemv_noalloc(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn
                                           _ptr(dn_scales), _ptr(dn_ts), _ptr(x), _ptr(expert_offsets),
                                           _ptr(pair_token), _ptr(pair_weight), _ptr(pair_slot), _ptr(y), E, H, I, T,
                                           topk, _stream(stream)), "moe_grouped_gemv_noalloc")
+
+
+def moe_layer(logits, gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, y, workspace, workspace_bytes,
+              E, H, I, T, topk, stream=None):
+    """Router and routed MoE layer from logits (moe_route_topk + moe_grouped_gemv in one call)."""
+    _check(lib().moe_layer(_ptr(logits), _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_ts), _ptr(dn_codes),
+                           _ptr(dn_scales), _ptr(dn_ts), _ptr(x), _ptr(y), _ptr(workspace), workspace_bytes, E, H, I,
+                           T, topk, _stream(stream)), "moe_layer")
+
+
+def moe_layer_workspace_bytes(T, topk, H, I, E) -> int:
+    return lib().moe_layer_workspace_bytes(T, topk, H, I, E)
 
 
 def bqd_moe_read_status(workspace, stream=None) -> int:

@@ -110,16 +110,21 @@ unsigned int bqd_get_launch_flags(void) { return bqd::launch_flags(); }
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream)
 {
-    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM && path != BQD_PATH_MMA)
+    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM && path != BQD_PATH_MMA &&
+        path != BQD_PATH_DIRECT)
         return BQD_ERR_PATH;
     bqd_status st = check_dense(codes, scales, x, y, M, K, N, 16, true);
     if (st != BQD_OK || M == 0) return st;
     if (path == BQD_PATH_STREAM && !bqd::stream_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if (path == BQD_PATH_MMA && !bqd::mma_gemv_supported(M, K, N)) return BQD_ERR_PATH;
+    if (path == BQD_PATH_DIRECT && !bqd::direct_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if ((st = check_arch()) != BQD_OK) return st;
     if (K == 0) return zero_output(y, M * N, stream);
+    const bool use_direct = path == BQD_PATH_DIRECT || (path == BQD_PATH_AUTO && bqd::direct_gemv_supported(M, K, N));
     const bool use_stream = path == BQD_PATH_STREAM || (path == BQD_PATH_AUTO && bqd::stream_gemv_supported(M, K, N));
     const bool use_mma = path == BQD_PATH_MMA || (path == BQD_PATH_AUTO && N >= 2 && bqd::mma_gemv_supported(M, K, N));
+    if (use_direct)
+        return from_cuda(bqd::launch_nvfp4_gemv_direct(codes, scales, tensor_scale, x, y, M, K, stream));
     if (use_stream)
         return from_cuda(bqd::launch_nvfp4_gemv_stream(codes, scales, tensor_scale, x, y, M, K, stream));
     if (use_mma) return from_cuda(bqd::launch_nvfp4_gemv_mma(codes, scales, tensor_scale, x, y, M, K, N, stream));
@@ -135,12 +140,16 @@ bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_
 bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K,
                           int N, int path, cudaStream_t stream)
 {
-    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM) return BQD_ERR_PATH;
+    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM && path != BQD_PATH_DIRECT)
+        return BQD_ERR_PATH;
     bqd_status st = check_dense(q, d, x, y, M, K, N, 32, true);
     if (st != BQD_OK || M == 0) return st;
     if (path == BQD_PATH_STREAM && !bqd::stream_gemv_supported(M, K, N)) return BQD_ERR_PATH;
+    if (path == BQD_PATH_DIRECT && !bqd::direct_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if ((st = check_arch()) != BQD_OK) return st;
     if (K == 0) return zero_output(y, M * N, stream);
+    if (path == BQD_PATH_DIRECT || (path == BQD_PATH_AUTO && bqd::direct_gemv_supported(M, K, N)))
+        return from_cuda(bqd::launch_q8_0_gemv_direct(q, d, x, y, M, K, stream));
     if (path != BQD_PATH_CUDA_CORE && bqd::stream_gemv_supported(M, K, N))
         return from_cuda(bqd::launch_q8_0_gemv_stream(q, d, x, y, M, K, stream));
     return from_cuda(bqd::launch_q8_0_gemv_cuda_core(q, d, x, y, M, K, N, stream));
@@ -237,6 +246,56 @@ bqd_status moe_grouped_gemv(const uint8_t* gu_codes, const uint8_t* gu_scales, c
     return from_cuda(bqd::launch_moe_grouped(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x,
                                              expert_offsets, pair_token, pair_weight, pair_slot, y, ws, E, H, I, T,
                                              topk, stream));
+}
+
+static size_t align256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+size_t moe_layer_workspace_bytes(int T, int topk, int H, int I, int E)
+{
+    if (T < 1 || topk < 1 || H < 1 || I < 1 || E < 1) return 0;
+    const size_t P = static_cast<size_t>(T) * topk;
+    return bqd::moe_workspace_size(T, topk, H, I) + align256((static_cast<size_t>(E) + 1) * 4) + 3 * align256(P * 4);
+}
+
+bqd_status moe_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
+                     const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts, const uint16_t* x,
+                     float* y, void* workspace, size_t workspace_bytes, int E, int H, int I, int T, int topk,
+                     cudaStream_t stream)
+{
+    if (T < 1 || E < 1 || E > bqd::kMoeMaxExperts || topk < 1 || topk > E || topk > bqd::kMoeMaxTopk ||
+        static_cast<int64_t>(T) * topk > bqd::kMoeMaxPairs || H < 32 || H > 8192 || H % 32 != 0 || I < 32 ||
+        I > 4096 || I % 32 != 0)
+        return BQD_ERR_SHAPE;
+    const void* ptrs[] = {logits, gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, y};
+    for (const void* p : ptrs)
+        if (!p) return BQD_ERR_NULL;
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return BQD_ERR_ALIGN;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        workspace_bytes < moe_layer_workspace_bytes(T, topk, H, I, E))
+        return BQD_ERR_WORKSPACE;
+    bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    const bqd::MoeWorkspace ws = bqd::moe_workspace_carve(workspace, T, topk, H, I);
+    if (bqd::moe_small_supported(E, H, I, T, topk))
+        return from_cuda(bqd::launch_moe_small_layer(logits, gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts,
+                                                     x, nullptr, nullptr, nullptr, nullptr, y, ws, E, H, I, T, topk,
+                                                     stream));
+    // the list after the layer's own workspace
+    const size_t P = static_cast<size_t>(T) * topk;
+    char* lp = static_cast<char*>(workspace) + bqd::moe_workspace_size(T, topk, H, I);
+    int32_t* offsets = reinterpret_cast<int32_t*>(lp);
+    lp += align256((static_cast<size_t>(E) + 1) * 4);
+    int32_t* pair_token = reinterpret_cast<int32_t*>(lp);
+    lp += align256(P * 4);
+    float* pair_weight = reinterpret_cast<float*>(lp);
+    lp += align256(P * 4);
+    int32_t* pair_slot = reinterpret_cast<int32_t*>(lp);
+    st = from_cuda(
+        bqd::launch_moe_route(logits, T, E, topk, offsets, pair_token, pair_weight, pair_slot, stream));
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_moe_grouped(gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, offsets,
+                                             pair_token, pair_weight, pair_slot, y, ws, E, H, I, T, topk, stream));
 }
 
 bqd_status bqd_moe_read_status(const void* workspace, int32_t* status_out, cudaStream_t stream)

@@ -22,6 +22,14 @@ cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, fl
                                  int64_t K, cudaStream_t s);
 cudaError_t launch_q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t s);
 
+// Register-streaming GEMV (gemv_direct.cu): N == 1, K a multiple of 1024
+// with K / 1024 in {1, 2, 3, 4, 6, 8, 12, 16}.
+bool direct_gemv_supported(int64_t M, int64_t K, int N);
+cudaError_t launch_nvfp4_gemv_direct(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                     float* y, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
+                                    int64_t K, cudaStream_t s);
+
 // Bulk-copy streaming GEMV (gemv_stream.cu): N == 1, K % 256 == 0.
 bool stream_gemv_supported(int64_t M, int64_t K, int N);
 cudaError_t launch_nvfp4_gemv_stream(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
@@ -67,6 +75,19 @@ cudaError_t launch_moe_stream_layer(const uint8_t* gu_codes, const uint8_t* gu_s
                                     const float* pair_weight, const int32_t* pair_slot, const MoeWorkspace& ws, int E,
                                     int H, int I, int T, int topk, cudaStream_t stream);
 cudaError_t read_and_clear_moe_stream_error(unsigned int* out);
+
+// Small-batch MoE kernels (moe_small.cu): T <= 4, T * topk <= 32, E <= 512,
+// H % 1024 == 0, I in {256, 512, 1024}. With logits != nullptr every CTA
+// routes the tokens itself (the list arguments are ignored); otherwise the
+// caller's expert-major list is checked and used. Writes the workspace's
+// status word, h, and y (the combine is part of the down kernel).
+bool moe_small_supported(int E, int H, int I, int T, int topk);
+cudaError_t launch_moe_small_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales,
+                                   const float* gu_ts, const uint8_t* dn_codes, const uint8_t* dn_scales,
+                                   const float* dn_ts, const uint16_t* x, const int32_t* offsets,
+                                   const int32_t* pair_token, const float* pair_weight, const int32_t* pair_slot,
+                                   float* y, const MoeWorkspace& ws, int E, int H, int I, int T, int topk,
+                                   cudaStream_t stream);
 
 cudaError_t launch_moe_grouped(const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
                                const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts,

@@ -1,0 +1,386 @@
+// gemv_direct.cu -- GEMV for one token (N = 1), NVFP4 and Q8_0, streaming
+// the weights straight from HBM into registers.
+//
+// y[m] = ts * sum_b scale[m][b] * sum_{k in b} elem[m][k] * x[k]
+// ("robertbfuentes7-cloud/bw24" README, NVFP4 (W4) decode path;
+// "avifenesh/memra" README, Decode kernels: NVFP4 and Q8_0 matvecs;
+// "Vemloir/LumenLLM" README, Kernels: warp-shuffle GEMVs).
+//
+// Every warp owns a contiguous, balanced range of rows and reads each row
+// with fully coalesced 16-byte loads: lane l takes the 32-element chunks
+// l, l + 32, ... of the row (16 code bytes and 2 scale bytes each for NVFP4,
+// 32 int8 and one fp16 scale for Q8_0). K is a multiple of 1024, so a row is
+// CPL = K / 1024 such chunks per lane, a compile-time constant: the loop
+// over a row is unrolled and every load offset and every activation offset
+// is an immediate. D chunks per lane stay in flight in registers (a ring
+// indexed at compile time). The first D are requested before the kernel
+// waits for the previous kernel in the stream (programmatic dependent
+// launch), so they overlap its tail.
+//
+// Activations are staged once per CTA in shared memory as f16 after an exact
+// power-of-two prescale (chosen from their largest exponent; f16 then holds
+// every bf16 value exactly when all nonzero magnitudes lie within 31
+// binades of the largest) and multiplied in by the mixed-precision FMA
+// (f16 x f16 products are exact in fp32; sums fp32). Outside that range, or
+// with subnormal, inf or NaN activations, the CTA keeps the bf16 values and
+// uses fp32 FMAs (exact products as well). Block scales multiply 16-element
+// partial sums; the tensor scale and the prescale's inverse multiply the
+// warp-shuffle row sum. Results are deterministic.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "common.cuh"
+#include "gemv.h"
+#include "host_util.h"
+
+namespace bqd {
+
+namespace {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Two fp32 accumulators += (lo, hi) f16 halves of w2 times those of x2.
+__device__ __forceinline__ void fma_f16x2(uint32_t w2, uint32_t x2, float& a0, float& a1)
+{
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "mov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.f16 %0, wl, xl, %0;\n\t"
+        "fma.rn.f32.f16 %1, wh, xh, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w2), "r"(x2));
+}
+
+// Four int8 (one word) to two f16x2 pairs, exactly: the byte q + 128 is the
+// low mantissa byte of the f16 0x6400 (= 1024), so the pair reads 1024 +
+// q + 128; subtracting 1152 leaves q.
+__device__ __forceinline__ void s8x4_to_f16x2(uint32_t w, uint32_t& p01, uint32_t& p23)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+    __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+    p01 = *reinterpret_cast<uint32_t*>(&ha);
+    p23 = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// 2^e as a float, e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// Activations: 32-element chunks of 64 bytes (f16, or the raw bf16 in exact
+// mode); the 16-byte piece p of chunk c sits at slot p ^ ((c >> 1) & 3), so
+// the 32 lanes, which read the same piece of 32 consecutive chunks, hit
+// distinct banks. Lane l's chunks are l + 32 i: its swizzle depends on l
+// only, and chunk l + 32 i starts 1024 i elements after chunk l.
+__device__ __forceinline__ int x_index(int c, int p) { return c * 32 + ((p ^ ((c >> 1) & 3)) << 3); }
+
+struct Nvfp4Item {  // 32 elements of one row: 16 code bytes, two E4M3 scales
+    uint4 c;
+    uint32_t s;
+};
+struct Q8Item {  // 32 elements of one row: 32 int8, one fp16 scale
+    uint4 a, b;
+    uint32_t d;
+};
+
+struct DirNvfp4 {
+    using Item = Nvfp4Item;
+    static constexpr int kCodeBytes = 16;  // per 32-element chunk
+    __device__ static __forceinline__ Item load(const uint8_t* c, const uint8_t* s)
+    {
+        Item it;
+        it.c = ld_stream_v4(c);
+        it.s = ld_stream_u16(s);
+        return it;
+    }
+    // xc: this lane's chunk in shared memory; sw: its swizzle
+    template <bool FAST>
+    __device__ static __forceinline__ void dot(const Item& it, const uint16_t* xc, int sw, float& acc)
+    {
+        const float2 sc = e4m3x2_to_float2(it.s);
+        const uint32_t words[4] = {it.c.x, it.c.y, it.c.z, it.c.w};
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {  // 16-element blocks
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int wi = 2 * b + j;  // elements 8 wi .. 8 wi + 7 = activation piece wi
+                const uint4 xq = *reinterpret_cast<const uint4*>(xc + ((wi ^ sw) << 3));
+                const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+                uint32_t h[4];
+                e2m1x8_to_f16x2(words[wi], h);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if constexpr (FAST) {
+                        fma_f16x2(h[q], xp[q], a0, a1);
+                    } else {
+                        const float2 wf = f16x2_to_float2(h[q]);
+                        a0 = fmaf(wf.x, bf16_lo(xp[q]), a0);
+                        a1 = fmaf(wf.y, bf16_hi(xp[q]), a1);
+                    }
+                }
+            }
+            acc = fmaf(b ? sc.y : sc.x, a0 + a1, acc);
+        }
+    }
+};
+
+struct DirQ8 {
+    using Item = Q8Item;
+    static constexpr int kCodeBytes = 32;
+    __device__ static __forceinline__ Item load(const uint8_t* c, const uint8_t* s)
+    {
+        Item it;
+        it.a = ld_stream_v4(c);
+        it.b = ld_stream_v4(c + 16);
+        it.d = ld_stream_u16(s);
+        return it;
+    }
+    template <bool FAST>
+    __device__ static __forceinline__ void dot(const Item& it, const uint16_t* xc, int sw, float& acc)
+    {
+        const uint32_t words[8] = {it.a.x, it.a.y, it.a.z, it.a.w, it.b.x, it.b.y, it.b.z, it.b.w};
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {  // 8 elements = 2 int8 words = activation piece p
+            const uint4 xq = *reinterpret_cast<const uint4*>(xc + ((p ^ sw) << 3));
+            const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t w = words[2 * p + h];
+                if constexpr (FAST) {
+                    uint32_t q01, q23;
+                    s8x4_to_f16x2(w, q01, q23);
+                    fma_f16x2(q01, xp[2 * h], a0, a1);
+                    fma_f16x2(q23, xp[2 * h + 1], a0, a1);
+                } else {
+                    float2 lo, hi;
+                    s8x4_to_float(w, lo, hi);
+                    a0 = fmaf(lo.x, bf16_lo(xp[2 * h]), a0);
+                    a1 = fmaf(lo.y, bf16_hi(xp[2 * h]), a1);
+                    a0 = fmaf(hi.x, bf16_lo(xp[2 * h + 1]), a0);
+                    a1 = fmaf(hi.y, bf16_hi(xp[2 * h + 1]), a1);
+                }
+            }
+        }
+        acc = fmaf(fp16_to_float(it.d), a0 + a1, acc);
+    }
+};
+
+// Rows [r_lo, r_hi) of a warp. Item g of the stream (row g / CPL, chunk
+// g % CPL) lives in buf[g % D]; D divides CPL or is a multiple of it, so
+// with U = max(1, D / CPL) rows unrolled per body the slot, the chunk and
+// the row offset of every item are compile-time constants.
+template <class F, int CPL, int D, bool FAST>
+__device__ __forceinline__ void direct_rows(typename F::Item (&buf)[D], const uint8_t* cp, const uint8_t* sp,
+                                            int64_t cpitch, int64_t spitch, const uint16_t* xl, int sw, float* y,
+                                            int64_t r_lo, int64_t r_hi, float ts, int sexp, int lane)
+{
+    static_assert(CPL % D == 0 || D % CPL == 0, "the ring depth must divide a row or be a multiple of one");
+    constexpr int U = D > CPL ? D / CPL : 1;
+    for (int64_t row0 = r_lo; row0 < r_hi; row0 += U) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (row0 + u < r_hi) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    const int g = u * CPL + i;
+                    const typename F::Item cur = buf[g % D];
+                    const int nr = (g + D) / CPL, nc = (g + D) % CPL;
+                    if (row0 + nr < r_hi)
+                        buf[g % D] = F::load(cp + (row0 + nr) * cpitch + nc * 32 * F::kCodeBytes,
+                                             sp + (row0 + nr) * spitch + nc * 64);
+                    F::template dot<FAST>(cur, xl + i * 1024, sw, acc);
+                    // keep the next chunk's shared-memory loads after this chunk's arithmetic
+                    asm volatile("" ::: "memory");
+                }
+                const float v = warp_sum(acc);
+                if (lane == 0) y[row0 + u] = ldexpf(v * ts, sexp);
+            }
+        }
+    }
+}
+
+// Dynamic shared memory: K f16 (or bf16) activations.
+template <class F, int CPL, int THREADS, int D>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemv_direct_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, float ts,
+                       const uint16_t* __restrict__ x, float* __restrict__ y, int64_t M)
+{
+    constexpr int W = THREADS / kWarp;
+    constexpr int64_t K = 1024 * CPL;
+    constexpr int64_t cpitch = K / 32 * F::kCodeBytes, spitch = K / 16;
+    extern __shared__ __align__(16) uint16_t xs[];
+    __shared__ int s_emax, s_emin, s_flags;
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + warp, nw = static_cast<int64_t>(gridDim.x) * W;
+    const int64_t r_lo = M * gw / nw, r_hi = M * (gw + 1) / nw;
+    const uint8_t* cp = codes + lane * F::kCodeBytes;
+    const uint8_t* sp = scales + lane * 2;
+    if (threadIdx.x == 0) {
+        s_emax = 0;
+        s_emin = INT_MAX;
+        s_flags = 0;
+    }
+    // the first D chunks: weights only, before the wait for the previous kernel
+    typename F::Item buf[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+        const int64_t row = r_lo + d / CPL;
+        if (row < r_hi) buf[d] = F::load(cp + row * cpitch + (d % CPL) * 32 * F::kCodeBytes, sp + row * spitch + (d % CPL) * 64);
+    }
+    pdl_trigger();
+    __syncthreads();
+    pdl_wait();  // the activations may come from the previous kernel; y may be read by it
+
+    // exponent range of the nonzero activations (bf16 biased exponents)
+    int emax = 0, emin = INT_MAX, flags = 0;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < static_cast<int>(K / 2); i += THREADS) {
+        const uint32_t v = reinterpret_cast<const uint32_t*>(x)[i];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t b = (v >> (16 * h)) & 0x7FFFu;
+            const int e = static_cast<int>(b >> 7);
+            if (b == 0) continue;
+            if (e == 0 || e == 255) flags = 1;
+            emax = max(emax, e);
+            emin = min(emin, e);
+        }
+    }
+    emax = __reduce_max_sync(0xFFFFFFFFu, emax);
+    emin = __reduce_min_sync(0xFFFFFFFFu, emin);
+    flags = __reduce_or_sync(0xFFFFFFFFu, flags);
+    if (lane == 0) {
+        if (flags) atomicOr(&s_flags, 1);
+        atomicMax(&s_emax, emax);
+        atomicMin(&s_emin, emin);
+    }
+    __syncthreads();
+    // f16 holds x * 2^-sexp exactly when every nonzero |x| is within 31
+    // binades of the largest; the largest lands in [2^14, 2^15).
+    const bool fast = !s_flags && (s_emin == INT_MAX || s_emax - s_emin <= 31);
+    const int sexp = fast && s_emin != INT_MAX ? s_emax - 127 - 14 : 0;
+    // x * 2^-sexp as two exact multiplies by normal powers of two
+    const int e1 = max(-126, min(127, -sexp));
+    const float f1 = pow2f(e1), f2 = pow2f(max(-126, min(127, -sexp - e1)));
+    for (int i = threadIdx.x; i < static_cast<int>(K / 8); i += THREADS) {  // 8 elements = one 16-byte piece
+        uint4 u = reinterpret_cast<const uint4*>(x)[i];
+        if (fast) {
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                __half2 hv = __floats2half2_rn(bf16_lo(w[q]) * f1 * f2, bf16_hi(w[q]) * f1 * f2);
+                o[q] = *reinterpret_cast<uint32_t*>(&hv);
+            }
+            u = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        *reinterpret_cast<uint4*>(xs + x_index(i / 4, i % 4)) = u;
+    }
+    __syncthreads();
+    const uint16_t* xl = xs + lane * 32;
+    const int sw = (lane >> 1) & 3;
+    if (fast)
+        direct_rows<F, CPL, D, true>(buf, cp, sp, cpitch, spitch, xl, sw, y, r_lo, r_hi, ts, sexp, lane);
+    else
+        direct_rows<F, CPL, D, false>(buf, cp, sp, cpitch, spitch, xl, sw, y, r_lo, r_hi, ts, sexp, lane);
+}
+
+// Launch shape per format, from back-to-back timings of 12288 x 4096 and
+// 4096 x 12288 calls (GB300): NVFP4 one CTA of 1024 threads per SM with two
+// chunks in flight per lane; Q8_0 (twice the bytes per element) one CTA of
+// 512 threads per SM with up to eight.
+template <class F>
+struct DirCfg;
+template <>
+struct DirCfg<DirNvfp4> {
+    static constexpr int kThreads = 1024;
+    template <int CPL>
+    static constexpr int depth() { return CPL % 2 == 0 || CPL == 1 ? 2 : CPL; }
+};
+template <>
+struct DirCfg<DirQ8> {
+    static constexpr int kThreads = 512;
+    template <int CPL>
+    static constexpr int depth() { return CPL == 1 || CPL == 2 || CPL == 4 || CPL == 8 ? 8 : (CPL % 4 == 0 ? 4 : CPL); }
+};
+
+template <class F, int CPL>
+cudaError_t launch_cpl(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y, int64_t M,
+                       cudaStream_t stream)
+{
+    constexpr int T = DirCfg<F>::kThreads;
+    constexpr int D = DirCfg<F>::template depth<CPL>();
+    auto kern = gemv_direct_kernel<F, CPL, T, D>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const size_t smem = static_cast<size_t>(CPL) * 1024 * 2;
+    static OccCache occ;
+    blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, T, smem);  // sets the shared-memory opt-in
+    int64_t grid = dev_info(dev).sms;
+    const int64_t need = (M + T / kWarp - 1) / (T / kWarp);
+    if (grid > need) grid = need;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(T);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = launch_flags() & kLaunchPdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, codes, scales, ts, x, y, M);
+}
+
+template <class F>
+cudaError_t launch_direct(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
+                          int64_t M, int64_t K, cudaStream_t s)
+{
+    switch (K / 1024) {
+        case 1: return launch_cpl<F, 1>(codes, scales, ts, x, y, M, s);
+        case 2: return launch_cpl<F, 2>(codes, scales, ts, x, y, M, s);
+        case 3: return launch_cpl<F, 3>(codes, scales, ts, x, y, M, s);
+        case 4: return launch_cpl<F, 4>(codes, scales, ts, x, y, M, s);
+        case 6: return launch_cpl<F, 6>(codes, scales, ts, x, y, M, s);
+        case 8: return launch_cpl<F, 8>(codes, scales, ts, x, y, M, s);
+        case 12: return launch_cpl<F, 12>(codes, scales, ts, x, y, M, s);
+        case 16: return launch_cpl<F, 16>(codes, scales, ts, x, y, M, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool direct_gemv_supported(int64_t M, int64_t K, int N)
+{
+    if (N != 1 || M < 1 || K < 1024 || K % 1024 != 0 || M > (int64_t(1) << 40)) return false;
+    switch (K / 1024) {
+        case 1: case 2: case 3: case 4: case 6: case 8: case 12: case 16: return true;
+        default: return false;
+    }
+}
+
+cudaError_t launch_nvfp4_gemv_direct(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                     float* y, int64_t M, int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirNvfp4>(codes, scales, ts, x, y, M, K, s);
+}
+
+cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
+                                    int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirQ8>(reinterpret_cast<const uint8_t*>(q), reinterpret_cast<const uint8_t*>(d), 1.0f, x, y,
+                                M, K, s);
+}
+
+}  // namespace bqd

@@ -29,6 +29,7 @@
 #include "common.cuh"
 #include "gemv.h"
 #include "host_util.h"
+#include "moe_route.cuh"
 
 namespace bqd {
 
@@ -72,9 +73,10 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total)
 }
 
 // ------------------------------------------------------------------ route
-// One CTA. Warp w routes tokens [T*w/8, T*(w+1)/8): top-k by repeated warp
-// argmax (larger logit first, lower expert index on ties), weights as the
-// softmax of the selected logits (equal to renormalising the full softmax).
+// One CTA. Warp w routes tokens [T*w/8, T*(w+1)/8) with route_token
+// (moe_route.cuh): top-k by repeated warp argmax over logits held in
+// registers, weights as the softmax of the selected logits (equal to
+// renormalising the full softmax).
 // Then a counting sort by expert: per-warp counts, a CTA-wide scan, and each
 // warp placing its own tokens in order, so a segment lists tokens ascending.
 __global__ void __launch_bounds__(kThreads) moe_route_kernel(const float* __restrict__ logits, int T, int E,
@@ -85,12 +87,10 @@ __global__ void __launch_bounds__(kThreads) moe_route_kernel(const float* __rest
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const int P = T * topk;
-    float* wl = reinterpret_cast<float*>(smem);  // [kWarps][E] logits of the warp's token
-    int* wc = reinterpret_cast<int*>(wl + kWarps * E);  // [kWarps][E] counts, then write cursors
-    int* sel_e = wc + kWarps * E;                       // [P]
-    float* sel_w = reinterpret_cast<float*>(sel_e + P);  // [P]
-    int* scratch = reinterpret_cast<int*>(sel_w + P);    // [kWarps + 1]
-    unsigned char* taken = reinterpret_cast<unsigned char*>(scratch + kWarps + 1);  // [kWarps][E]
+    int* wc = reinterpret_cast<int*>(smem);               // [kWarps][E] counts, then write cursors
+    int* sel_e = wc + kWarps * E;                         // [P]
+    float* sel_w = reinterpret_cast<float*>(sel_e + P);   // [P]
+    int* scratch = reinterpret_cast<int*>(sel_w + P);     // [kWarps + 1]
 
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
     for (int i = threadIdx.x; i < kWarps * E; i += kThreads) wc[i] = 0;
@@ -98,72 +98,14 @@ __global__ void __launch_bounds__(kThreads) moe_route_kernel(const float* __rest
 
     const int t_lo = static_cast<int>(static_cast<int64_t>(T) * warp / kWarps);
     const int t_hi = static_cast<int>(static_cast<int64_t>(T) * (warp + 1) / kWarps);
-    float* L = wl + warp * E;
-    unsigned char* tk = taken + warp * E;
     int* cnt = wc + warp * E;
     for (int t = t_lo; t < t_hi; ++t) {
-        // the token's logits: eight loads in flight per lane, then to shared memory
-        for (int e0 = 0; e0 < E; e0 += 8 * kWarp) {
-            float v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = e0 + i * kWarp + lane;
-                v[i] = e < E ? logits[static_cast<int64_t>(t) * E + e] : 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = e0 + i * kWarp + lane;
-                if (e < E) {
-                    L[e] = v[i];
-                    tk[e] = 0;
-                }
-            }
-        }
-        __syncwarp();
         int my_e = 0;
-        float my_l = 0.f, lmax = 0.f;
-        for (int s = 0; s < topk; ++s) {
-            float bv = -INFINITY;
-            int be = INT_MAX;
-            for (int e = lane; e < E; e += kWarp) {
-                if (tk[e]) continue;
-                const float v = L[e];
-                if (v > bv || (v == bv && e < be)) {
-                    bv = v;
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if (be == INT_MAX) {  // only NaN logits left: take the lowest free index
-                int fe = INT_MAX;
-                for (int e = lane; e < E; e += kWarp)
-                    if (!tk[e] && e < fe) fe = e;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) fe = min(fe, __shfl_xor_sync(0xFFFFFFFFu, fe, o));
-                be = fe;
-                bv = L[be];
-            }
-            if (lane == 0) tk[be] = 1;
-            if (lane == s) {
-                my_e = be;
-                my_l = bv;
-            }
-            if (s == 0) lmax = bv;
-            __syncwarp();
-        }
-        const float ex = lane < topk ? expf(my_l - lmax) : 0.f;
-        const float z = warp_sum(ex);
+        float my_w = 0.f;
+        route_token(logits + static_cast<int64_t>(t) * E, E, topk, lane, &my_e, &my_w);
         if (lane < topk) {
             sel_e[t * topk + lane] = my_e;
-            sel_w[t * topk + lane] = ex / z;
+            sel_w[t * topk + lane] = my_w;
             cnt[my_e] += 1;  // the topk experts of one token are distinct
         }
         __syncwarp();
@@ -570,8 +512,7 @@ cudaError_t launch_moe_route(const float* logits, int T, int E, int topk, int32_
                              float* pair_weight, int32_t* pair_slot, cudaStream_t s)
 {
     const int P = T * topk;
-    const size_t smem = static_cast<size_t>(kWarps) * E * 4 * 2 + static_cast<size_t>(P) * 8 + (kWarps + 1) * 4 +
-                        static_cast<size_t>(kWarps) * E;
+    const size_t smem = static_cast<size_t>(kWarps) * E * 4 + static_cast<size_t>(P) * 8 + (kWarps + 1) * 4;
     static OccCache occ;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -592,6 +533,9 @@ cudaError_t launch_moe_grouped(const uint8_t* gu_codes, const uint8_t* gu_scales
     const int sms = dev_info(dev).sms;
     const int P = T * topk;
     const int max_active = P < E ? P : E;
+    if (moe_small_supported(E, H, I, T, topk))  // writes the status word itself
+        return launch_moe_small_layer(nullptr, gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, offsets,
+                                      pair_token, pair_weight, pair_slot, y, ws, E, H, I, T, topk, s);
     err = cudaMemsetAsync(ws.status, 0, sizeof(int32_t), s);
     if (err != cudaSuccess) return err;
     const dim3 grid_c((H + kThreads - 1) / kThreads, T);

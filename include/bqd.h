@@ -73,6 +73,10 @@ enum {
     BQD_PATH_CUDA_CORE = 1, /* register-prefetch loads, in-register decode, fp32 FMA; any shape */
     BQD_PATH_STREAM = 2,    /* bulk-copy (TMA) stream into a shared-memory ring, decode on the CUDA
                                cores; N == 1 and K % 256 == 0 (K <= 16384) only, else BQD_ERR_PATH */
+    BQD_PATH_DIRECT = 4,    /* weights streamed from HBM straight into registers by fully coalesced 16-byte
+                               loads, compile-time unrolled over a row, decode and mixed-precision FMAs on the
+                               CUDA cores; N == 1 and K a multiple of 1024 with K / 1024 one of 1, 2, 3, 4, 6,
+                               8, 12, 16, else BQD_ERR_PATH */
     BQD_PATH_MMA = 3        /* NVFP4 only: weights decoded exactly to f16 (or bf16) in tensor memory and
                                multiplied on the tensor cores (tcgen05.mma, fp32 accumulation), the
                                (row tile, k) work split over thread-block clusters with a fixed-order
@@ -133,8 +137,10 @@ bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_
                       int64_t M, int64_t K, int N, cudaStream_t stream);
 
 /* nvfp4_gemv with an explicit compute path (BQD_PATH_*), to compare paths.
- * AUTO takes BQD_PATH_STREAM for N == 1 and BQD_PATH_MMA for N >= 2 where
- * they apply, else BQD_PATH_CUDA_CORE. */
+ * AUTO takes, for N == 1, BQD_PATH_DIRECT where it applies, else
+ * BQD_PATH_STREAM where it applies; for N >= 2 BQD_PATH_MMA where it
+ * applies; else BQD_PATH_CUDA_CORE. q8_0_gemv_path's AUTO is the same
+ * without the MMA path. */
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream);
 
@@ -233,6 +239,30 @@ bqd_status moe_grouped_gemv(const uint8_t* gu_codes, const uint8_t* gu_scales, c
                             const int32_t* expert_offsets, const int32_t* pair_token, const float* pair_weight,
                             const int32_t* pair_slot, float* y, void* workspace, size_t workspace_bytes, int E,
                             int H, int I, int T, int topk, cudaStream_t stream);
+
+/*
+ * moe_layer -- the routed MoE layer from router logits: the same results as
+ * moe_route_topk followed by moe_grouped_gemv ("robertbfuentes7-cloud/bw24"
+ * README, MoE bullet), in fewer launches.
+ *   logits fp32 [T][E]; the other arguments as in moe_grouped_gemv;
+ *   workspace: at least moe_layer_workspace_bytes(T, topk, H, I, E) bytes,
+ *   256-byte aligned, owned by the caller, not shared by calls that may
+ *   overlap. Its first int32 is the status word, h starts where
+ *   moe_grouped_gemv puts it.
+ *   For a few tokens (T <= 4, T * topk <= 32, E <= 512, H % 1024 == 0, I one
+ *   of 256, 512, 1024) the routing is computed inside the two layer kernels
+ *   (no route kernel, no list in memory; the down kernel folds in the
+ *   weighted combine); otherwise moe_route_topk writes the list into the
+ *   workspace and moe_grouped_gemv follows. Limits as moe_grouped_gemv plus
+ *   those of moe_route_topk. NaN logits are outside the contract.
+ */
+bqd_status moe_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
+                     const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts, const uint16_t* x,
+                     float* y, void* workspace, size_t workspace_bytes, int E, int H, int I, int T, int topk,
+                     cudaStream_t stream);
+
+/* Bytes of device workspace moe_layer needs for these sizes (0 if a size is < 1). */
+size_t moe_layer_workspace_bytes(int T, int topk, int H, int I, int E);
 
 /*
  * moe_grouped_gemv_noalloc -- moe_grouped_gemv for callers that cannot

@@ -129,3 +129,17 @@ def test_binding_raises_on_error():
     with pytest.raises(bqd.BqdError) as ei:
         bqd.nvfp4_gemv(None, A, 1.0, A, A, 4, 32, 1, stream=0)
     assert ei.value.status == 1
+
+
+def test_moe_layer_validation(L):
+    s = None
+    a = [A] * 9
+    wsb = L.moe_layer_workspace_bytes(1, 8, 2048, 512, 256)
+    assert wsb >= L.moe_workspace_bytes(1, 8, 2048, 512) + 257 * 4
+    assert L.moe_layer(None, *a[1:], A, wsb, 256, 2048, 512, 1, 8, s) == 1          # NULL logits
+    assert L.moe_layer(*a, A, wsb, 256, 2048, 512, 1, 0, s) == 2                    # topk < 1
+    assert L.moe_layer(*a, A, wsb, 256, 2040, 512, 1, 8, s) == 2                    # H % 32
+    assert L.moe_layer(*a, A, wsb - 1, 256, 2048, 512, 1, 8, s) == 6                # workspace too small
+    assert L.moe_layer(*a, A + 16, wsb, 256, 2048, 512, 1, 8, s) == 6               # workspace misaligned
+    assert L.moe_layer(*a[:8], U, A, wsb, 256, 2048, 512, 1, 8, s) == 3             # misaligned y
+    assert L.moe_layer_workspace_bytes(0, 8, 2048, 512, 256) == 0

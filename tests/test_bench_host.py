@@ -85,3 +85,12 @@ def test_rotating_copies_exceed_three_l2():
         r = bench.rotating_copies(call_bytes, weight_bytes, l2, 40e9)
         assert r >= 2 and (r - 1) * call_bytes > 3 * l2
     assert bench.rotating_copies(10**6, 10**10, l2, 40e9) == 4  # capped by the memory budget, at least 2
+
+
+def test_moe_launch_count():
+    # T = 1 and 4 at top-8 with H = 2048, I = 512: the two small-batch kernels
+    assert bench.moe_launches(1, 256, 2048, 512, 8) == 2
+    assert bench.moe_launches(4, 256, 2048, 512, 8) == 2
+    # T = 16: route, gate_up, down, combine
+    assert bench.moe_launches(16, 256, 2048, 512, 8) == 4
+    assert bench.moe_launches(1, 256, 2048, 384, 8) == 4

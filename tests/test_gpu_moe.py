@@ -9,6 +9,7 @@ import oracle
 import block_quantized_decode_nvfp4_gb300 as bqd
 from block_quantized_decode_nvfp4_gb300 import synthetic as syn
 from tests.bounds import abs_planes, moe_check, silu_up_spread
+from tests import pins
 from tests.gpu_util import assert_within, dev, need_gpu
 
 pytestmark = pytest.mark.gpu
@@ -163,3 +164,81 @@ def test_moe_malformed_list_sets_status_without_faulting(H, I):
     # a valid call afterwards clears the status
     bqd.moe_grouped_gemv(*args, off, ptok, pw, pslot, y, ws, wsb, E, H, I, T, topk)
     assert bqd.bqd_moe_read_status(ws) == 0
+
+
+# ---------------------------------------------------------------- moe_layer and the small-batch path
+def _layer_fused(L):
+    T, E, H, I, topk = L["T"], L["E"], L["H"], L["I"], L["topk"]
+    wsb = bqd.moe_layer_workspace_bytes(T, topk, H, I, E)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    y = torch.full((T * H,), float("nan"), dtype=torch.float32, device="cuda")
+    bqd.moe_layer(dev(L["logits"]), dev(L["gu_codes"]), dev(L["gu_scales"]), dev(L["gu_ts"]), dev(L["dn_codes"]),
+                  dev(L["dn_scales"]), dev(L["dn_ts"]), dev(L["x"]), y, ws, wsb, E, H, I, T, topk)
+    assert bqd.bqd_moe_read_status(ws) == 0
+    return y.cpu().numpy().reshape(T, H), ws
+
+
+# (T, E, H, I, topk): the first five take the small-batch kernels (T <= 4,
+# T * topk <= 32, H % 1024 == 0, I in {256, 512, 1024}), the last two the
+# route kernel and the expert streams
+SMALL_AND_LARGE = [(1, 64, 1024, 256, 8), (2, 16, 1024, 512, 4), (3, 64, 2048, 256, 8), (4, 32, 2048, 1024, 8),
+                   (4, 256, 2048, 512, 8), (5, 64, 1024, 256, 8), (16, 64, 1024, 256, 8)]
+
+
+@pytest.mark.parametrize("T,E,H,I,topk", SMALL_AND_LARGE)
+def test_moe_layer_matches_route_then_grouped_and_oracle(T, E, H, I, topk):
+    L = syn.moe_layer(T=T, E=E, H=H, I=I, topk=topk, seed=T * 131 + E + I)
+    y_fused, ws = _layer_fused(L)
+    y_two, ws2, _ = _layer_run(L)
+    assert np.array_equal(y_fused.view(np.uint32), y_two.view(np.uint32)), "moe_layer differs from route + grouped"
+    # h sits where moe_grouped_gemv documents it, in both workspaces
+    assert np.array_equal(_ws_h(ws, T, topk, I), _ws_h(ws2, T, topk, I))
+    sel, wts = oracle.moe_route(L["logits"], topk)
+    yref, parts = oracle.moe_layer(L, sel=sel, weights=wts, want_parts=True)
+    moe_check(y_fused, L, sel, wts, parts, yref, f"moe_layer T={T} E={E} H={H} I={I} k={topk}")
+    y3, _ = _layer_fused(L)
+    assert np.array_equal(y_fused.view(np.uint32), y3.view(np.uint32)), "not deterministic"
+
+
+def test_small_path_identical_experts_and_activation_range():
+    L = syn.moe_layer(T=4, E=32, H=1024, I=256, topk=4, seed=17)
+    for k in ("gu_codes", "gu_scales", "dn_codes", "dn_scales"):
+        L[k] = np.ascontiguousarray(np.broadcast_to(L[k][0], L[k].shape))
+    y, _, _ = _layer_run(L)
+    sel, w = oracle.moe_route(L["logits"], 4)
+    yref, parts = oracle.moe_layer(L, sel=sel, weights=w, want_parts=True)
+    moe_check(y, L, sel, w, parts, yref, "small path, identical experts")
+    # one token with a range wider than f16 holds: the CTA takes the exact fp32 path
+    xf = pins.bf16_lib(L["x"]).astype(np.float32)
+    xf[2, 5], xf[2, 9] = 2.0 ** 40, 2.0 ** -40
+    L["x"] = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y, _, _ = _layer_run(L)
+    yref, parts = oracle.moe_layer(L, sel=sel, weights=w, want_parts=True)
+    moe_check(y, L, sel, w, parts, yref, "small path, wide-range token")
+
+
+def test_small_path_malformed_list_sets_status_without_faulting():
+    T, E, H, I, topk = 2, 8, 1024, 256, 2
+    L = syn.moe_layer(T=T, E=E, H=H, I=I, topk=topk, seed=55)
+    off, ptok, pw, pslot = route(L["logits"], topk)
+    wsb = bqd.moe_workspace_bytes(T, topk, H, I)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    y = torch.zeros(T * H, dtype=torch.float32, device="cuda")
+    args = [dev(L[k]) for k in ("gu_codes", "gu_scales", "gu_ts", "dn_codes", "dn_scales", "dn_ts", "x")]
+    bad_off = off.clone()
+    bad_off[E] = T * topk + 3
+    bqd.moe_grouped_gemv(*args, bad_off, ptok, pw, pslot, y, ws, wsb, E, H, I, T, topk)
+    assert bqd.bqd_moe_read_status(ws) & 1
+    bad_tok = ptok.clone()
+    bad_tok[0] = 99
+    bqd.moe_grouped_gemv(*args, off, bad_tok, pw, pslot, y, ws, wsb, E, H, I, T, topk)
+    assert bqd.bqd_moe_read_status(ws) & 2
+    dup = pslot.clone()
+    dup[:] = 0
+    bqd.moe_grouped_gemv(*args, off, ptok, pw, dup, y, ws, wsb, E, H, I, T, topk)
+    assert bqd.bqd_moe_read_status(ws) & 4
+    bqd.moe_grouped_gemv(*args, off, ptok, pw, pslot, y, ws, wsb, E, H, I, T, topk)
+    assert bqd.bqd_moe_read_status(ws) == 0
+    sel, w = oracle.moe_route(L["logits"], topk)
+    yref, parts = oracle.moe_layer(L, sel=sel, weights=w, want_parts=True)
+    moe_check(y.cpu().numpy(), L, sel, w, parts, yref, "small path after malformed lists")

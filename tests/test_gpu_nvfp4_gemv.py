@@ -133,6 +133,23 @@ def test_stream_and_cuda_core_paths_match_oracle(M, K):
         assert_within(y, ref, a, f"{M}x{K} path {path}")
 
 
+# every K the direct path instantiates, row counts around the warp split
+# (1 row; fewer rows than warps; odd splits; a multiple of 152 x 32 warps)
+@pytest.mark.parametrize("M,K", syn.NVFP4_SHAPES + [(1, 1024), (31, 2048), (257, 3072), (4864, 4096),
+                                                    (1000, 6144), (333, 8192), (77, 12288), (3001, 16384)])
+def test_direct_path_matches_oracle(M, K):
+    w = syn.dense_nvfp4(M, K, N=1, seed=K + 3 * M)
+    ref, a = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], w["x"], M, K)
+    assert_within(run(w, path=bqd.BQD_PATH_DIRECT), ref, a, f"{M}x{K} direct")
+
+
+def test_direct_path_rejects_unsupported_shapes():
+    for M, K, N in ((8, 4112, 1), (8, 5120, 1), (8, 512, 1), (8, 1024, 2)):
+        w = syn.dense_nvfp4(M, K, N=N, seed=1)
+        with pytest.raises(bqd.BqdError):
+            run(w, path=bqd.BQD_PATH_DIRECT)
+
+
 def test_stream_path_rejects_unsupported_shapes():
     w = syn.dense_nvfp4(8, 4112, N=1, seed=1)
     with pytest.raises(bqd.BqdError):
@@ -162,11 +179,12 @@ def test_stream_activation_range_cases(case):
     elif case == "zeros":
         xf = xf * 0
     w["x"] = _bf16(xf.numpy())[None]
-    y = run(w, path=bqd.BQD_PATH_STREAM)
     ref, a = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], w["x"], M, K)
-    assert_within(y, ref, a, case, absol=0.0 if case != "zeros" else 0.0)
-    if case == "zeros":
-        assert np.all(y == 0)
+    for path in (bqd.BQD_PATH_STREAM, bqd.BQD_PATH_DIRECT):
+        y = run(w, path=path)
+        assert_within(y, ref, a, f"{case} path {path}", absol=0.0 if case != "zeros" else 0.0)
+        if case == "zeros":
+            assert np.all(y == 0)
 
 
 def test_stream_nonfinite_activation_pattern():
@@ -175,7 +193,15 @@ def test_stream_nonfinite_activation_pattern():
     x = w["x"].copy()
     x[0, 3] = 0x7F80  # +inf
     w["x"] = x
-    y = run(w, path=bqd.BQD_PATH_STREAM)
+    _nonfinite_check(w, run(w, path=bqd.BQD_PATH_STREAM), M, K)
+    w2 = syn.dense_nvfp4(M, 1024, N=1, seed=79)
+    x2 = w2["x"].copy()
+    x2[0, 700] = 0xFF80  # -inf
+    w2["x"] = x2
+    _nonfinite_check(w2, run(w2, path=bqd.BQD_PATH_DIRECT), M, 1024)
+
+
+def _nonfinite_check(w, y, M, K):
     ref, _ = oracle.nvfp4_gemv(w["codes"], w["scales"], w["ts"], w["x"], M, K)
     assert np.array_equal(np.isnan(y[0]), np.isnan(ref[0]))
     assert np.array_equal(np.isinf(y[0]), np.isinf(ref[0]))
@@ -226,13 +252,14 @@ def test_pdl_output_may_overwrite_previous_input(pdl_on):
 
 
 # ---------------------------------------------------------------- N = 1 stream kernel, exact invariants
-def test_stream_n1_exact_invariants():
-    """Through BQD_PATH_STREAM at N = 1 (the decode hot path): a one-hot x
+@pytest.mark.parametrize("path", ["stream", "direct"])
+def test_n1_exact_invariants(path):
+    """Through the N = 1 paths (the decode hot path): a one-hot x
     gives the dequantised column bit for bit; a one-hot x of 3 gives the
     exact product rounded once; sign flip negates exactly; zero codes give
     zero; ts = 2 doubles exactly."""
     M, K = 1000, 4096
-    P = bqd.BQD_PATH_STREAM
+    P = bqd.BQD_PATH_STREAM if path == "stream" else bqd.BQD_PATH_DIRECT
     w = syn.dense_nvfp4(M, K, N=1, seed=12)
     W = oracle.nvfp4_dequant(w["codes"], w["scales"], w["ts"], M, K, dtype=np.float32)
     for k in (0, 1, 15, 16, 255, 256, 2047, 4095):

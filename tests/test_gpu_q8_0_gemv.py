@@ -108,11 +108,12 @@ def _no_device_error():
     assert bqd.bqd_device_error() == 0, "a pipeline wait ran out"
 
 
-@pytest.mark.parametrize("M,K", syn.Q8_0_SHAPES[:2] + [(1, 256), (33, 768), (500, 16384)])
+@pytest.mark.parametrize("M,K", syn.Q8_0_SHAPES[:2] + [(1, 256), (33, 768), (500, 16384), (4864, 4096), (70, 3072),
+                                                      (9, 6144), (1, 1024)])
 def test_stream_and_cuda_core_paths_match_oracle(M, K):
     w = syn.dense_q8_0(M, K, N=1, seed=M + K)
     ref, a = oracle.q8_0_gemv(w["q"], w["d"], w["x"], M, K)
-    for path in (bqd.BQD_PATH_STREAM, bqd.BQD_PATH_CUDA_CORE):
+    for path in (bqd.BQD_PATH_STREAM, bqd.BQD_PATH_CUDA_CORE) + ((bqd.BQD_PATH_DIRECT,) if K % 1024 == 0 else ()):
         out = Guarded(M)
         bqd.q8_0_gemv_path(dev(w["q"]), dev(w["d"]), dev(w["x"]), out.ptr, M, K, 1, path)
         assert_within(out.get()[None], ref, a, f"{M}x{K} path {path}")
@@ -127,12 +128,13 @@ def _run_path(w, path, q=None, x=None):
     return out.get()
 
 
-def test_stream_n1_extremes_and_exact_invariants():
-    """Through BQD_PATH_STREAM at N = 1: blocks of q = -128 and 127 within the
+@pytest.mark.parametrize("path", ["stream", "direct"])
+def test_n1_extremes_and_exact_invariants(path):
+    """Through the N = 1 paths: blocks of q = -128 and 127 within the
     tolerance; a one-hot x gives the dequantised column bit for bit;
     negating q negates y exactly."""
     M, K = 700, 4096
-    P = bqd.BQD_PATH_STREAM
+    P = bqd.BQD_PATH_STREAM if path == "stream" else bqd.BQD_PATH_DIRECT
     w = syn.dense_q8_0(M, K, N=1, seed=13)
     w["q"][:, :64] = -128
     w["q"][:, 64:128] = 127
