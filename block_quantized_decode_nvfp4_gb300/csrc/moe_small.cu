@@ -1,32 +1,32 @@
-// moe_small.cu -- the routed MoE layer for a few tokens (T <= 4 tokens and
-// T * topk <= 32 routed pairs): decode with one to four tokens in flight.
+// moe_small.cu -- the routed MoE layer for a few tokens (T <= 4 tokens,
+// T * topk <= 32 routed pairs): two kernels, each a GEMV over gathered rows.
 //
 // What is computed is the MoE layer of moe.cu ("robertbfuentes7-cloud/bw24"
 // README, MoE bullet: routed tokens batched expert-major, each selected
 // expert's weights decoded once for all of its tokens):
 //   g = W_gu[e][0:I] . x_t,  u = W_gu[e][I:2I] . x_t,  h = SiLU(g) * u,
-//   y_t = sum over slots s = 0..topk-1, in order, of w_{t,s} * (W_dn[e_{t,s}] . h_{t,s}).
+//   y_t = sum over slots s of w_{t,s} * ts_dn[e_{t,s}] * (W_dn[e_{t,s}] . h_{t,s}).
 //
 // With so few tokens each SM streams only tens of kilobytes per projection,
-// so the layer is latency-bound; the design removes every step of the chain
-// that the larger-batch path needs:
+// so the layer is latency-bound. The two kernels are built like the direct
+// N = 1 GEMV (gemv_direct.cu): warps own contiguous row ranges, rows are
+// read with coalesced 16-byte loads into a register ring whose slots and
+// offsets are compile-time constants, activations sit in shared memory.
 //  * Routing, when the layer is given router logits (moe_layer), is done by
-//    every CTA of both kernels for itself (route_token_warp, the router's
-//    own code, so the experts and weights are those moe_route_topk picks):
-//    no route kernel and no list in global memory.
-//  * Gate_up kernel: the rows (gate row i and up row I + i) of all active
-//    experts form one row space split evenly over all warps of the grid;
-//    every warp streams its rows with 16-byte loads kept four items deep in
-//    registers; the activations are staged once per CTA as f16, each token
-//    scaled by its own exact power of two, and multiplied in by mixed-
-//    precision FMAs (exact products, fp32 sums), as in the N = 1 GEMV.
-//  * Down kernel with the combine folded in: every warp owns output rows j
-//    and, for each of them, walks the routed pairs in token-major slot
-//    order, streams row j of the pair's expert and accumulates
-//    y_t[j] = fma(w_{t,s}, d_{t,s}[j], y_t[j]) in slot order -- no partial
-//    outputs in global memory and no combine kernel. Its weight loads are
-//    issued before it waits for the gate_up kernel (programmatic dependent
-//    launch), so they overlap that kernel.
+//    every CTA of both kernels for itself (route_token, the router's own
+//    code, so the experts and weights are those moe_route_topk picks): no
+//    route kernel and no list in global memory.
+//  * Gate_up: the rows of all active experts (2I each: gate then up) form one
+//    row space; each row is dotted with the expert's tokens (at most T),
+//    staged once per CTA as exactly prescaled f16 with mixed-precision FMAs;
+//    g and u of every (pair, row) go to the workspace.
+//  * Down with the combine folded in: h = SiLU(g) * u is formed while it is
+//    staged in shared memory, already multiplied by its pair's routing weight
+//    and down tensor scale (h' = w * ts * h); output (t, j) is then one dot
+//    product of length topk * I between h'_t (the token's slots side by side)
+//    and row j of each of its experts, gathered: no partial outputs and no
+//    combine kernel. Its weight loads are issued before it waits for the
+//    gate_up kernel (programmatic dependent launch).
 // Results are deterministic. Caller-supplied lists are checked as in moe.cu
 // (status bits; never a fault).
 #include <cuda_fp16.h>
@@ -45,12 +45,12 @@ namespace bqd {
 
 namespace {
 
-constexpr int kTh = 256;            // threads per CTA (8 warps)
+constexpr int kTh = 512;            // threads per CTA (16 warps)
 constexpr int kWp = kTh / kWarp;
 constexpr int kMaxT = 4;            // tokens
 constexpr int kMaxP = 32;           // routed (token, slot) pairs
 constexpr int kMaxE = 512;          // experts
-constexpr int kDepth = 4;           // items in flight per lane
+constexpr int kDepth = 2;           // 32-element chunks in flight per lane
 constexpr int kStatusBadOffsets = 1;
 constexpr int kStatusBadPair = 2;
 constexpr int kStatusCoverage = 4;
@@ -88,7 +88,6 @@ struct PairList {
     int pe[kMaxP];           // expert of pair p
     int pt[kMaxP];           // token of pair p (-1: invalid pair, skipped)
     float pw[kMaxP];         // routing weight of pair p
-    float pts[kMaxP];        // down projection tensor scale of pair p's expert (down kernel)
     int qp[kMaxP];           // pair of (token, slot) q = t * topk + s (-1: none)
     int cover[kMaxP];        // times (token, slot) q appears
     int sel_e[kMaxP];        // routing scratch: expert of q
@@ -206,139 +205,143 @@ __device__ void read_list(const int32_t* __restrict__ offsets, const int32_t* __
     __syncthreads();
 }
 
-// ------------------------------------------------------------------ gate_up
-struct GuItem {
-    uint4 g, u;     // 16 code bytes (32 elements) of the gate row and of the up row
-    uint32_t sg, su;  // their two E4M3 block scales
+// ------------------------------------------------------------------ items
+struct Item {  // 32 elements of one NVFP4 row: 16 code bytes, two E4M3 scales
+    uint4 c;
+    uint32_t s;
 };
 
-template <bool FAST, int NT>
-__device__ __forceinline__ void gu_item(const GuItem& it, const uint16_t* xs, int H, const PairList& L, int p0, int ne,
-                                        int c, float (&g)[NT], float (&u)[NT])
+__device__ __forceinline__ Item load_item(const uint8_t* c, const uint8_t* s)
 {
-    const float2 sg = e4m3x2_to_float2(it.sg), su = e4m3x2_to_float2(it.su);
-    const uint32_t wg[4] = {it.g.x, it.g.y, it.g.z, it.g.w}, wu[4] = {it.u.x, it.u.y, it.u.z, it.u.w};
-    uint32_t hg[16], hu[16];
+    Item it;
+    it.c = ld_stream_v4(c);
+    it.s = ld_stream_u16(s);
+    return it;
+}
+
+// One chunk against NT staged f16 (or raw bf16) tokens: xr[n] is token n's
+// activations at this lane's chunk, sw the lane's swizzle.
+template <bool FAST, int NT>
+__device__ __forceinline__ void gu_dot(const Item& it, const uint16_t* const (&xr)[NT], int ne, int sw,
+                                       float (&acc)[NT])
+{
+    const float2 sc = e4m3x2_to_float2(it.s);
+    const uint32_t words[4] = {it.c.x, it.c.y, it.c.z, it.c.w};
+    uint32_t h[16];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        uint32_t a[4], b[4];
-        e2m1x8_to_f16x2(wg[w], a);
-        e2m1x8_to_f16x2(wu[w], b);
+        uint32_t a[4];
+        e2m1x8_to_f16x2(words[w], a);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            hg[4 * w + q] = a[q];
-            hu[4 * w + q] = b[q];
-        }
+        for (int q = 0; q < 4; ++q) h[4 * w + q] = a[q];
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
         if (n < ne) {
-            const int t = L.pt[p0 + n];
-            if (t >= 0) {
-                const uint16_t* xr = xs + t * H;
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
+            for (int b = 0; b < 2; ++b) {
+                float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int wi = 2 * b + j;
-                        const uint4 xq = *reinterpret_cast<const uint4*>(xr + xh_index(c, wi));
-                        const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+                for (int j = 0; j < 2; ++j) {
+                    const int wi = 2 * b + j;
+                    const uint4 xq = *reinterpret_cast<const uint4*>(xr[n] + ((wi ^ sw) << 3));
+                    const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if constexpr (FAST) {
-                                fma_f16x2(hg[4 * wi + q], xp[q], g0, g1);
-                                fma_f16x2(hu[4 * wi + q], xp[q], u0, u1);
-                            } else {
-                                const float2 fg = f16x2_to_float2(hg[4 * wi + q]);
-                                const float2 fu = f16x2_to_float2(hu[4 * wi + q]);
-                                g0 = fmaf(fg.x, bf16_lo(xp[q]), g0);
-                                g1 = fmaf(fg.y, bf16_hi(xp[q]), g1);
-                                u0 = fmaf(fu.x, bf16_lo(xp[q]), u0);
-                                u1 = fmaf(fu.y, bf16_hi(xp[q]), u1);
-                            }
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (FAST) {
+                            fma_f16x2(h[4 * wi + q], xp[q], a0, a1);
+                        } else {
+                            const float2 wf = f16x2_to_float2(h[4 * wi + q]);
+                            a0 = fmaf(wf.x, bf16_lo(xp[q]), a0);
+                            a1 = fmaf(wf.y, bf16_hi(xp[q]), a1);
                         }
                     }
-                    g[n] = fmaf(b ? sg.y : sg.x, g0 + g1, g[n]);
-                    u[n] = fmaf(b ? su.y : su.x, u0 + u1, u[n]);
                 }
+                acc[n] = fmaf(b ? sc.y : sc.x, a0 + a1, acc[n]);
             }
         }
     }
 }
 
-// Row pair v of the warp's row space: active expert v / I, row pair v % I.
-template <bool FAST, int NT>
-__device__ __forceinline__ void gu_loop(GuItem (&buf)[kDepth], const uint8_t* __restrict__ gu_codes,
+// ------------------------------------------------------------------ gate_up
+// Virtual row v of the gate_up row space: active expert a = v / (2I), row
+// l = v % (2I) of its gate_up weight (gate rows first, then up rows).
+// go[p][l] = the row's dot product with pair p's token, tensor scale and the
+// token's prescale applied.
+template <int CPL, int NT, bool FAST>
+__device__ __forceinline__ void gu_rows(Item (&buf)[kDepth], const uint8_t* __restrict__ gu_codes,
                                         const uint8_t* __restrict__ gu_scales, const float* __restrict__ gu_ts,
-                                        const uint16_t* xs, const int* sexp, const PairList& L, float* __restrict__ h,
-                                        int H, int I, int v_lo, int v_hi, int lv, int li, int lane)
+                                        const uint16_t* xs, const int* sexp, const PairList& L, float* __restrict__ go,
+                                        int H, int I, int v_lo, int v_hi, int lane)
 {
-    const int cpl = H / 1024;  // 32-element chunks per lane per row
+    static_assert(CPL % kDepth == 0 || kDepth % CPL == 0, "ring depth must divide a row or be a multiple of one");
+    constexpr int U = kDepth > CPL ? kDepth / CPL : 1;
     const int64_t cp = H / 2, sp = H / 16;
-    const int total = (v_hi - v_lo) * cpl;
-    int cv = v_lo, ci = 0;
-    float g[NT], u[NT];
+    const int sw = (lane >> 1) & 3;
+    for (int v0 = v_lo; v0 < v_hi; v0 += U) {
 #pragma unroll
-    for (int n = 0; n < NT; ++n) g[n] = u[n] = 0.f;
-    for (int j0 = 0; j0 < total; j0 += kDepth) {
-#pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
-            const int j = j0 + d;
-            if (j < total) {
-                const GuItem cur = buf[d];
-                if (j + kDepth < total) {
-                    const int a = lv / I, i = lv - a * I, e = L.act[a];
-                    const int64_t rg = static_cast<int64_t>(e) * 2 * I + i;
-                    const int c = lane + 32 * li;
-                    buf[d].g = ld_stream_v4(gu_codes + rg * cp + 16 * c);
-                    buf[d].u = ld_stream_v4(gu_codes + (rg + I) * cp + 16 * c);
-                    buf[d].sg = ld_stream_u16(gu_scales + rg * sp + 2 * c);
-                    buf[d].su = ld_stream_u16(gu_scales + (rg + I) * sp + 2 * c);
-                    if (++li == cpl) {
-                        li = 0;
-                        ++lv;
-                    }
-                }
-                const int a = cv / I;
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u;
+            if (v < v_hi) {
+                const int a = v / (2 * I), l = v - a * (2 * I);
                 const int p0 = L.act_p0[a], ne = L.act_p0[a + 1] - p0;
-                gu_item<FAST, NT>(cur, xs, H, L, p0, ne, lane + 32 * ci, g, u);
-                if (++ci == cpl) {
-                    const int i = cv - a * I;
-                    const float ts = gu_ts[L.act[a]];
+                const uint16_t* xr[NT];
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
-                        if (n < ne) {
-                            const int t = L.pt[p0 + n];
-                            const float gs = warp_sum(g[n]), us = warp_sum(u[n]);
-                            if (lane == 0 && t >= 0) {
-                                const float gv = ldexpf(gs * ts, sexp[t]), uv = ldexpf(us * ts, sexp[t]);
-                                h[static_cast<int64_t>(p0 + n) * I + i] = gv / (1.0f + expf(-gv)) * uv;
-                            }
-                        }
-                        g[n] = u[n] = 0.f;
+                for (int n = 0; n < NT; ++n) {
+                    const int t = n < ne ? L.pt[p0 + n] : -1;
+                    xr[n] = xs + (t >= 0 ? t : 0) * H + lane * 32;
+                }
+                float acc[NT];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) acc[n] = 0.f;
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    const int g = u * CPL + i;
+                    const Item cur = buf[g % kDepth];
+                    const int nr = (g + kDepth) / CPL, nc = (g + kDepth) % CPL;
+                    const int vn = v0 + nr;
+                    if (vn < v_hi) {
+                        const int an = vn / (2 * I), ln = vn - an * (2 * I);
+                        const int64_t row = static_cast<int64_t>(L.act[an]) * 2 * I + ln;
+                        buf[g % kDepth] = load_item(gu_codes + row * cp + nc * 512 + lane * 16,
+                                                    gu_scales + row * sp + nc * 64 + lane * 2);
                     }
-                    ci = 0;
-                    ++cv;
+                    const uint16_t* xi[NT];
+#pragma unroll
+                    for (int n = 0; n < NT; ++n) xi[n] = xr[n] + i * 1024;
+                    gu_dot<FAST, NT>(cur, xi, ne, sw, acc);
+                    asm volatile("" ::: "memory");
+                }
+                const float ts = gu_ts[L.act[a]];
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    if (n < ne) {
+                        const int t = L.pt[p0 + n];
+                        const float sum = warp_sum(acc[n]);
+                        if (lane == 0 && t >= 0) go[static_cast<int64_t>(p0 + n) * 2 * I + l] = ldexpf(sum * ts, sexp[t]);
+                    }
                 }
             }
         }
     }
 }
 
-// Dynamic shared memory: the activations, kMaxT * H * 2 bytes.
+// Dynamic shared memory: the activations, kMaxT * H f16 (or bf16).
+template <int CPL, int NT>
 __global__ void __launch_bounds__(kTh, 2)
     moe_small_gu_kernel(const float* __restrict__ logits, const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ pair_token, const float* __restrict__ pair_weight,
                         const int32_t* __restrict__ pair_slot, const uint8_t* __restrict__ gu_codes,
                         const uint8_t* __restrict__ gu_scales, const float* __restrict__ gu_ts,
-                        const uint16_t* __restrict__ x, MoeWorkspace ws, int E, int H, int I, int T, int topk)
+                        const uint16_t* __restrict__ x, MoeWorkspace ws, int E, int I, int T, int topk)
 {
+    constexpr int H = 1024 * CPL;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ PairList L;
     __shared__ int s_emax[kMaxT], s_emin[kMaxT], s_sexp[kMaxT], s_flags;
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
+    float* go = ws.part;  // [P][2I] gate and up outputs
 
     if (threadIdx.x == 0) s_flags = 0;  // ordered before their use by the barriers of the routing
     if (threadIdx.x < kMaxT) {
@@ -353,29 +356,20 @@ __global__ void __launch_bounds__(kTh, 2)
     pdl_trigger();  // the down kernel may start: its inputs are complete
     if (blockIdx.x == 0 && threadIdx.x == 0) *ws.status = L.status;
 
-    // this warp's row pairs, an even split of all active experts' I row pairs
-    const int nv = L.n_act * I;
+    // this warp's rows: an even split of all active experts' 2I rows
+    const int nv = L.n_act * 2 * I;
     const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWp + warp, nw = static_cast<int64_t>(gridDim.x) * kWp;
     const int v_lo = static_cast<int>(nv * gw / nw), v_hi = static_cast<int>(nv * (gw + 1) / nw);
-    const int cpl = H / 1024;
     const int64_t cp = H / 2, sp = H / 16;
-    const int total = (v_hi - v_lo) * cpl;
-    GuItem buf[kDepth];
-    int lv = v_lo, li = 0;
+    Item buf[kDepth];
 #pragma unroll
     for (int d = 0; d < kDepth; ++d) {
-        if (d < total) {
-            const int a = lv / I, i = lv - a * I, e = L.act[a];
-            const int64_t rg = static_cast<int64_t>(e) * 2 * I + i;
-            const int c = lane + 32 * li;
-            buf[d].g = ld_stream_v4(gu_codes + rg * cp + 16 * c);
-            buf[d].u = ld_stream_v4(gu_codes + (rg + I) * cp + 16 * c);
-            buf[d].sg = ld_stream_u16(gu_scales + rg * sp + 2 * c);
-            buf[d].su = ld_stream_u16(gu_scales + (rg + I) * sp + 2 * c);
-            if (++li == cpl) {
-                li = 0;
-                ++lv;
-            }
+        const int v = v_lo + d / CPL;
+        if (v < v_hi) {
+            const int a = v / (2 * I), l = v - a * (2 * I);
+            const int64_t row = static_cast<int64_t>(L.act[a]) * 2 * I + l;
+            buf[d] = load_item(gu_codes + row * cp + (d % CPL) * 512 + lane * 16,
+                               gu_scales + row * sp + (d % CPL) * 64 + lane * 2);
         }
     }
 
@@ -435,59 +429,34 @@ __global__ void __launch_bounds__(kTh, 2)
         *reinterpret_cast<uint4*>(xs + t * H + xh_index(v / 4, v % 4)) = uu;
     }
     __syncthreads();
-    // an expert has at most T of the pairs (one per token)
-#define BQD_GU(F_, NT_) gu_loop<F_, NT_>(buf, gu_codes, gu_scales, gu_ts, xs, s_sexp, L, ws.h, H, I, v_lo, v_hi, lv, li, lane)
-    if (fast) {
-        if (T == 1) BQD_GU(true, 1);
-        else if (T == 2) BQD_GU(true, 2);
-        else BQD_GU(true, kMaxT);
-    } else {
-        if (T == 1) BQD_GU(false, 1);
-        else if (T == 2) BQD_GU(false, 2);
-        else BQD_GU(false, kMaxT);
-    }
-#undef BQD_GU
+    if (fast)
+        gu_rows<CPL, NT, true>(buf, gu_codes, gu_scales, gu_ts, xs, s_sexp, L, go, H, I, v_lo, v_hi, lane);
+    else
+        gu_rows<CPL, NT, false>(buf, gu_codes, gu_scales, gu_ts, xs, s_sexp, L, go, H, I, v_lo, v_hi, lane);
 }
 
 // ------------------------------------------------------------------ down + combine
-struct DnItem {
-    uint4 c;     // 16 code bytes (32 elements) of row j of the pair's expert
-    uint32_t s;  // their two E4M3 block scales
-};
-
-// Loads of item (row j, step st): lane takes chunk lane % LP of pair
-// q = st * PP + lane / LP (token-major order) if that pair exists.
-__device__ __forceinline__ void dn_load(DnItem& it, const uint8_t* __restrict__ dn_codes,
-                                        const uint8_t* __restrict__ dn_scales, const PairList& L, int H, int I, int P,
-                                        int j, int st, int lane, int LP, int PP)
-{
-    const int q = st * PP + lane / LP, c = lane % LP;
-    const int p = q < P ? L.qp[q] : -1;
-    if (p >= 0) {
-        const int64_t row = static_cast<int64_t>(L.pe[p]) * H + j;
-        it.c = ld_stream_v4(dn_codes + row * (I / 2) + 16 * c);
-        it.s = ld_stream_u16(dn_scales + row * (I / 16) + 2 * c);
-    } else {
-        it.c = make_uint4(0u, 0u, 0u, 0u);
-        it.s = 0u;
-    }
-}
-
-__device__ __forceinline__ float dn_dot(const DnItem& it, const float* hrow, int c)
+// Output (t, j) is the dot product of h'_t = [h'_{t,0} .. h'_{t,topk-1}] (the
+// token's slots side by side, K' = topk * I elements) with row j of each of
+// its experts, gathered. Lane l takes the chunks l + 32 i (i < CPLD) of that
+// gathered row: slot s = (l + 32 i) / CS (CS = I / 32 chunks per slot),
+// chunk (l + 32 i) % CS = l % CS of the slot's expert row (CS divides 32).
+__device__ __forceinline__ float dn_dot(const Item& it, const float* hc)
 {
     const float2 sc = e4m3x2_to_float2(it.s);
     const uint32_t w[4] = {it.c.x, it.c.y, it.c.z, it.c.w};
+    const int sw = (threadIdx.x & 31) & 7;  // fp32 chunks: piece p at slot p ^ (c & 7), c = lane + 32 i
     float acc = 0.f;
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-            const int wi = 2 * b + jj;  // elements 8wi .. 8wi+7 = h pieces 2wi, 2wi+1
+            const int wi = 2 * b + jj;  // elements 8 wi .. 8 wi + 7 = h' pieces 2 wi, 2 wi + 1
             uint32_t hw[4];
             e2m1x8_to_f16x2(w[wi], hw);
-            const float4 h0 = *reinterpret_cast<const float4*>(hrow + xf_index(c, 2 * wi));
-            const float4 h1 = *reinterpret_cast<const float4*>(hrow + xf_index(c, 2 * wi + 1));
+            const float4 h0 = *reinterpret_cast<const float4*>(hc + (((2 * wi) ^ sw) << 2));
+            const float4 h1 = *reinterpret_cast<const float4*>(hc + (((2 * wi + 1) ^ sw) << 2));
             float2& a = jj ? a1 : a0;
             a = __ffma2_rn(f16x2_to_float2(hw[0]), make_float2(h0.x, h0.y), a);
             a = __ffma2_rn(f16x2_to_float2(hw[1]), make_float2(h0.z, h0.w), a);
@@ -499,19 +468,24 @@ __device__ __forceinline__ float dn_dot(const DnItem& it, const float* hrow, int
     return acc;
 }
 
-// Dynamic shared memory: h, P * I fp32.
+// Dynamic shared memory: h', P * I fp32 (token-major: token t's slots side by side).
+template <int CPLD, int CS>
 __global__ void __launch_bounds__(kTh, 2)
     moe_small_dn_kernel(const float* __restrict__ logits, const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ pair_token, const float* __restrict__ pair_weight,
                         const int32_t* __restrict__ pair_slot, const uint8_t* __restrict__ dn_codes,
                         const uint8_t* __restrict__ dn_scales, const float* __restrict__ dn_ts, float* __restrict__ y,
-                        MoeWorkspace ws, int E, int H, int I, int T, int topk)
+                        MoeWorkspace ws, int E, int H, int T, int topk)
 {
+    constexpr int I = 32 * CS;
+    constexpr int64_t cp = I / 2, sp = I / 16;
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ PairList L;
+    __shared__ int s_eh[kMaxP];  // expert * H of (token, slot) q, -1 if missing
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int P = T * topk;
+    const int P = T * topk, KC = topk * CS;  // chunks per gathered row
     float* hs = reinterpret_cast<float*>(smem);
+    const float* go = ws.part;
 
     // The routing inputs are complete: the gate_up kernel let this kernel
     // start only after its own wait for the kernel before it.
@@ -519,96 +493,132 @@ __global__ void __launch_bounds__(kTh, 2)
         route_in_cta(logits, T, E, topk, L);
     else
         read_list(offsets, pair_token, pair_weight, pair_slot, T, E, topk, L);
-    if (threadIdx.x < P) L.pts[threadIdx.x] = dn_ts[L.pe[threadIdx.x]];
+    if (threadIdx.x < P) {
+        const int p = L.qp[threadIdx.x];
+        s_eh[threadIdx.x] = p >= 0 ? L.pe[p] * H : -1;
+    }
     __syncthreads();
-
-    const int LP = I / 32, PP = kWarp / LP;  // lanes per pair, pairs per warp step
-    const int steps = (P + PP - 1) / PP;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWp + warp, nw = static_cast<int64_t>(gridDim.x) * kWp;
-    const int j_lo = static_cast<int>(H * gw / nw), j_hi = static_cast<int>(H * (gw + 1) / nw);
     const bool ok = L.status != kStatusBadOffsets;
-    const int total = ok ? (j_hi - j_lo) * steps : 0;
-    DnItem buf[kDepth];
-    int lj = j_lo, ls = 0;
-#pragma unroll
-    for (int d = 0; d < kDepth; ++d) {
-        if (d < total) {
-            dn_load(buf[d], dn_codes, dn_scales, L, H, I, P, lj, ls, lane, LP, PP);
-            if (++ls == steps) {
-                ls = 0;
-                ++lj;
-            }
-        }
-    }
 
-    pdl_wait();  // h comes from the gate_up kernel; y may be read by earlier kernels
-#pragma unroll 4
-    for (int i = threadIdx.x; i < P * (I / 4); i += kTh) {
-        const int p = i / (I / 4), v = i - p * (I / 4);
-        float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (L.pt[p] >= 0) hv = reinterpret_cast<const float4*>(ws.h + static_cast<int64_t>(p) * I)[v];
-        *reinterpret_cast<float4*>(hs + p * I + xf_index(v >> 3, v & 7)) = hv;
+    // rows (t, j), t = r / H: an even split over all warps
+    const int nr = ok ? T * H : 0;
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWp + warp, nw = static_cast<int64_t>(gridDim.x) * kWp;
+    const int r_lo = static_cast<int>(nr * gw / nw), r_hi = static_cast<int>(nr * (gw + 1) / nw);
+    const int cc = lane % CS;
+    // the gathered row's expert rows for this lane's chunks, per token
+    int eh[CPLD];
+    int cur_t = -1;
+    auto set_token = [&](int t) {
+#pragma unroll
+        for (int i = 0; i < CPLD; ++i) {
+            const int c = lane + 32 * i;
+            eh[i] = c < KC ? s_eh[t * topk + c / CS] : -1;
+        }
+        cur_t = t;
+    };
+    auto load_at = [&](int r, int i) -> Item {
+        Item it;
+        it.c = make_uint4(0u, 0u, 0u, 0u);
+        it.s = 0u;
+        const int t = r / H, j = r - t * H;
+        if (t != cur_t) set_token(t);
+        if (eh[i] >= 0) it = load_item(dn_codes + static_cast<int64_t>(eh[i] + j) * cp + cc * 16,
+                                       dn_scales + static_cast<int64_t>(eh[i] + j) * sp + cc * 2);
+        return it;
+    };
+    static_assert(CPLD % kDepth == 0 || kDepth % CPLD == 0, "ring depth must divide a row or be a multiple of one");
+    constexpr int U = kDepth > CPLD ? kDepth / CPLD : 1;
+    Item buf[kDepth];
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d)
+        if (r_lo + d / CPLD < r_hi) buf[d] = load_at(r_lo + d / CPLD, d % CPLD);
+
+    pdl_wait();  // g and u come from the gate_up kernel; y may be read by earlier kernels
+    // h' = w * ts_dn * SiLU(g) * u of every (token, slot), token-major
+    for (int i = threadIdx.x; i < P * I; i += kTh) {
+        const int q = i / I, k = i - q * I;
+        const int p = L.qp[q];
+        float hv = 0.f;
+        if (p >= 0) {
+            const float g = go[static_cast<int64_t>(p) * 2 * I + k], u = go[static_cast<int64_t>(p) * 2 * I + I + k];
+            const float h = g / (1.0f + expf(-g)) * u;
+            if (blockIdx.x == 0) ws.h[static_cast<int64_t>(p) * I + k] = h;
+            hv = h * (L.pw[p] * dn_ts[L.pe[p]]);
+        }
+        const int t = q / topk, c = (q - t * topk) * CS + k / 32;  // chunk of token t's gathered row
+        hs[t * KC * 32 + c * 32 + (((k / 4 % 8) ^ (c & 7)) << 2) + k % 4] = hv;
     }
     __syncthreads();
 
-    float acc[kMaxT];
+    const int sw_unused = 0;
+    (void)sw_unused;
+    for (int r0 = r_lo; r0 < r_hi; r0 += U) {
 #pragma unroll
-    for (int t = 0; t < kMaxT; ++t) acc[t] = 0.f;
-    int cj = j_lo, cs = 0;
-    for (int j0 = 0; j0 < total; j0 += kDepth) {
+        for (int u = 0; u < U; ++u) {
+            const int r = r0 + u;
+            if (r < r_hi) {
+                const int t = r / H;
+                const float* hrow = hs + t * KC * 32;
+                float acc = 0.f;
 #pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
-            const int jdx = j0 + d;
-            if (jdx < total) {
-                const DnItem cur = buf[d];
-                if (jdx + kDepth < total) {
-                    dn_load(buf[d], dn_codes, dn_scales, L, H, I, P, lj, ls, lane, LP, PP);
-                    if (++ls == steps) {
-                        ls = 0;
-                        ++lj;
-                    }
+                for (int i = 0; i < CPLD; ++i) {
+                    const int g = u * CPLD + i;
+                    const Item it = buf[g % kDepth];
+                    const int rn = r0 + (g + kDepth) / CPLD;
+                    if (rn < r_hi) buf[g % kDepth] = load_at(rn, (g + kDepth) % CPLD);
+                    const int c = lane + 32 * i;
+                    if (c < KC) acc += dn_dot(it, hrow + c * 32);
+                    asm volatile("" ::: "memory");
                 }
-                const int q = cs * PP + lane / LP;
-                const int p = q < P ? L.qp[q] : -1;
-                float v = p >= 0 ? dn_dot(cur, hs + p * I, lane % LP) : 0.f;
-                for (int o = LP / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-                // the combine, in token-major slot order
-                for (int g = 0; g < PP; ++g) {
-                    const float d_g = __shfl_sync(0xFFFFFFFFu, v, g * LP);
-                    const int qg = cs * PP + g;
-                    const int pg = qg < P ? L.qp[qg] : -1;
-                    if (pg >= 0) {
-                        const float dv = d_g * L.pts[pg];
-                        const int t = qg / topk;
-#pragma unroll
-                        for (int tt = 0; tt < kMaxT; ++tt)
-                            if (tt == t) acc[tt] = fmaf(L.pw[pg], dv, acc[tt]);
-                    }
-                }
-                if (++cs == steps) {
-                    if (lane == 0)
-                        for (int t = 0; t < T; ++t) y[static_cast<int64_t>(t) * H + cj] = acc[t];
-#pragma unroll
-                    for (int t = 0; t < kMaxT; ++t) acc[t] = 0.f;
-                    cs = 0;
-                    ++cj;
-                }
+                const float v = warp_sum(acc);
+                if (lane == 0) y[static_cast<int64_t>(t) * H + (r - t * H)] = v;
             }
         }
     }
-    if (!ok && lane == 0)  // malformed CSR: outputs unspecified, written as zero
-        for (int j = j_lo; j < j_hi; ++j)
-            for (int t = 0; t < T; ++t) y[static_cast<int64_t>(t) * H + j] = 0.f;
+    if (!ok && lane == 0 && warp == 0 && blockIdx.x == 0)  // malformed CSR: outputs unspecified, written as zero
+        for (int i = 0; i < T * H; ++i) y[i] = 0.f;
 }
 
 size_t small_smem(int64_t bytes) { return static_cast<size_t>(bytes); }
+
+template <int CPL, int NT>
+cudaError_t launch_gu(cudaLaunchConfig_t& cfg, int dev, const float* logits, const int32_t* offsets,
+                      const int32_t* pair_token, const float* pair_weight, const int32_t* pair_slot,
+                      const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts, const uint16_t* x,
+                      const MoeWorkspace& ws, int E, int I, int T, int topk)
+{
+    auto kern = moe_small_gu_kernel<CPL, NT>;
+    static OccCache occ;
+    cfg.dynamicSmemBytes = small_smem(static_cast<int64_t>(kMaxT) * 1024 * CPL * 2);
+    blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, kTh, cfg.dynamicSmemBytes);
+    return cudaLaunchKernelEx(&cfg, kern, logits, offsets, pair_token, pair_weight, pair_slot, gu_codes, gu_scales,
+                              gu_ts, x, ws, E, I, T, topk);
+}
+
+template <int CPLD, int CS>
+cudaError_t launch_dn(cudaLaunchConfig_t& cfg, int dev, const float* logits, const int32_t* offsets,
+                      const int32_t* pair_token, const float* pair_weight, const int32_t* pair_slot,
+                      const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts, float* y,
+                      const MoeWorkspace& ws, int E, int H, int T, int topk)
+{
+    auto kern = moe_small_dn_kernel<CPLD, CS>;
+    static OccCache occ;
+    cfg.dynamicSmemBytes = small_smem(static_cast<int64_t>(T) * topk * 32 * CS * 4);
+    blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, kTh, cfg.dynamicSmemBytes);
+    return cudaLaunchKernelEx(&cfg, kern, logits, offsets, pair_token, pair_weight, pair_slot, dn_codes, dn_scales,
+                              dn_ts, y, ws, E, H, T, topk);
+}
 
 }  // namespace
 
 bool moe_small_supported(int E, int H, int I, int T, int topk)
 {
-    return T >= 1 && T <= kMaxT && T * topk <= kMaxP && topk <= kWarp && E >= 1 && E <= kMaxE && H >= 1024 &&
-           H % 1024 == 0 && H <= 8192 && (I == 256 || I == 512 || I == 1024);
+    const bool h_ok = H == 1024 || H == 2048 || H == 4096 || H == 8192;
+    const bool i_ok = I == 256 || I == 512 || I == 1024;
+    // g and u of all pairs live in the workspace's partial-output area (needs H >= 2I);
+    // a gathered down row is at most 8 * 1024 elements
+    return T >= 1 && T <= kMaxT && T * topk <= kMaxP && topk <= kWarp && E >= 1 && E <= kMaxE && h_ok && i_ok &&
+           H >= 2 * I && topk * I <= 8192;
 }
 
 cudaError_t launch_moe_small_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales,
@@ -626,29 +636,48 @@ cudaError_t launch_moe_small_layer(const float* logits, const uint8_t* gu_codes,
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-
-    const size_t smem_gu = small_smem(static_cast<int64_t>(kMaxT) * H * 2);
-    const size_t smem_dn = small_smem(static_cast<int64_t>(T) * topk * I * 4);
-    static OccCache occ_gu, occ_dn;
-    blocks_per_sm(occ_gu, reinterpret_cast<const void*>(moe_small_gu_kernel), dev, kTh, smem_gu);
-    blocks_per_sm(occ_dn, reinterpret_cast<const void*>(moe_small_dn_kernel), dev, kTh, smem_dn);
-
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(sms));
     cfg.blockDim = dim3(kTh);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cfg.dynamicSmemBytes = smem_gu;
-    err = cudaLaunchKernelEx(&cfg, moe_small_gu_kernel, logits, offsets, pair_token, pair_weight, pair_slot, gu_codes,
-                             gu_scales, gu_ts, x, ws, E, H, I, T, topk);
+
+    const int nt = T == 1 ? 1 : (T == 2 ? 2 : 4);
+#define BQD_GU(CPL_)                                                                                                  \
+    (nt == 1   ? launch_gu<CPL_, 1>(cfg, dev, logits, offsets, pair_token, pair_weight, pair_slot, gu_codes,          \
+                                    gu_scales, gu_ts, x, ws, E, I, T, topk)                                           \
+     : nt == 2 ? launch_gu<CPL_, 2>(cfg, dev, logits, offsets, pair_token, pair_weight, pair_slot, gu_codes,          \
+                                    gu_scales, gu_ts, x, ws, E, I, T, topk)                                           \
+               : launch_gu<CPL_, 4>(cfg, dev, logits, offsets, pair_token, pair_weight, pair_slot, gu_codes,          \
+                                    gu_scales, gu_ts, x, ws, E, I, T, topk))
+    switch (H) {
+        case 1024: err = BQD_GU(1); break;
+        case 2048: err = BQD_GU(2); break;
+        case 4096: err = BQD_GU(4); break;
+        default: err = BQD_GU(8); break;
+    }
+#undef BQD_GU
     if (err != cudaSuccess) return err;
     // The down kernel always follows programmatically: it reads nothing that
     // the gate_up kernel writes before its griddepcontrol.wait.
     cfg.numAttrs = 1;
-    cfg.dynamicSmemBytes = smem_dn;
-    return cudaLaunchKernelEx(&cfg, moe_small_dn_kernel, logits, offsets, pair_token, pair_weight, pair_slot,
-                              dn_codes, dn_scales, dn_ts, y, ws, E, H, I, T, topk);
+    const int kc = topk * (I / 32);  // chunks of a gathered down row
+    const int cpld = kc <= 32 ? 1 : (kc <= 64 ? 2 : (kc <= 128 ? 4 : 8));
+#define BQD_DN(CPLD_)                                                                                                 \
+    (I == 256   ? launch_dn<CPLD_, 8>(cfg, dev, logits, offsets, pair_token, pair_weight, pair_slot, dn_codes,        \
+                                      dn_scales, dn_ts, y, ws, E, H, T, topk)                                         \
+     : I == 512 ? launch_dn<CPLD_, 16>(cfg, dev, logits, offsets, pair_token, pair_weight, pair_slot, dn_codes,       \
+                                       dn_scales, dn_ts, y, ws, E, H, T, topk)                                        \
+                : launch_dn<CPLD_, 32>(cfg, dev, logits, offsets, pair_token, pair_weight, pair_slot, dn_codes,       \
+                                       dn_scales, dn_ts, y, ws, E, H, T, topk))
+    switch (cpld) {
+        case 1: return BQD_DN(1);
+        case 2: return BQD_DN(2);
+        case 4: return BQD_DN(4);
+        default: return BQD_DN(8);
+    }
+#undef BQD_DN
 }
 
 }  // namespace bqd
