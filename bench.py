@@ -72,10 +72,12 @@ def moe_bytes(T, E, H, I, topk, logits):
 
 
 def moe_launches(T, E, H, I, topk):
-    """Kernel launches of one moe_layer call: the two small-batch kernels
-    (routing inside them, combine inside the down kernel) for a few tokens,
-    else route, gate_up, down and combine (plus the status word's memset)."""
-    small = (T <= 4 and T * topk <= 32 and E <= 512 and H % 1024 == 0 and H <= 8192 and I in (256, 512, 1024))
+    """Kernel launches of one moe_layer call: the two batched kernels
+    (routing inside them, combine inside the down kernel) for up to 16
+    tokens, else route, gate_up, down and combine (plus the status word's
+    memset)."""
+    small = (T <= 16 and T * topk <= 128 and E <= 512 and H in (1024, 2048, 4096, 8192) and I in (256, 512, 1024)
+             and H >= 2 * I and topk * I <= 8192 and T * H <= 32768)
     return 2 if small else 4
 
 

@@ -217,11 +217,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr int W = THREADS / kWarp;
     constexpr int64_t K = 1024 * CPL;
     constexpr int64_t cpitch = K / 32 * F::kCodeBytes, spitch = K / 16;
+    constexpr int NP = CPL * 128;                        // 16-byte activation pieces
+    constexpr int PPT = (NP + THREADS - 1) / THREADS;    // pieces per thread
     extern __shared__ __align__(16) uint16_t xs[];
     __shared__ int s_emax, s_emin, s_flags;
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * W + warp, nw = static_cast<int64_t>(gridDim.x) * W;
-    const int64_t r_lo = M * gw / nw, r_hi = M * (gw + 1) / nw;
+    // this warp's rows: an even split of [0, M) over all warps of the grid
+    const uint32_t gw = blockIdx.x * W + warp, nw = gridDim.x * W;
+    int64_t r_lo, r_hi;
+    if (M * nw < (int64_t(1) << 32)) {  // 32-bit division when it is exact
+        const uint32_t m = static_cast<uint32_t>(M);
+        r_lo = m * gw / nw;
+        r_hi = m * (gw + 1) / nw;
+    } else {
+        r_lo = M * gw / nw;
+        r_hi = M * (gw + 1) / nw;
+    }
     const uint8_t* cp = codes + lane * F::kCodeBytes;
     const uint8_t* sp = scales + lane * 2;
     if (threadIdx.x == 0) {
@@ -240,19 +251,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     pdl_wait();  // the activations may come from the previous kernel; y may be read by it
 
-    // exponent range of the nonzero activations (bf16 biased exponents)
+    // activations, one global read into registers: exponent range of the
+    // nonzero values (bf16 biased exponents), then the prescaled f16 copy
+    uint4 xv[PPT];
     int emax = 0, emin = INT_MAX, flags = 0;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < static_cast<int>(K / 2); i += THREADS) {
-        const uint32_t v = reinterpret_cast<const uint32_t*>(x)[i];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t b = (v >> (16 * h)) & 0x7FFFu;
-            const int e = static_cast<int>(b >> 7);
-            if (b == 0) continue;
-            if (e == 0 || e == 255) flags = 1;
-            emax = max(emax, e);
-            emin = min(emin, e);
+    for (int k = 0; k < PPT; ++k) {
+        const int i = threadIdx.x + k * THREADS;
+        if (i < NP) {
+            xv[k] = reinterpret_cast<const uint4*>(x)[i];
+            const uint32_t w[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t b = (w[q / 2] >> (16 * (q & 1))) & 0x7FFFu;
+                const int e = static_cast<int>(b >> 7);
+                if (b == 0) continue;
+                if (e == 0 || e == 255) flags = 1;  // subnormal, inf or NaN
+                emax = max(emax, e);
+                emin = min(emin, e);
+            }
         }
     }
     emax = __reduce_max_sync(0xFFFFFFFFu, emax);
@@ -271,19 +288,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     // x * 2^-sexp as two exact multiplies by normal powers of two
     const int e1 = max(-126, min(127, -sexp));
     const float f1 = pow2f(e1), f2 = pow2f(max(-126, min(127, -sexp - e1)));
-    for (int i = threadIdx.x; i < static_cast<int>(K / 8); i += THREADS) {  // 8 elements = one 16-byte piece
-        uint4 u = reinterpret_cast<const uint4*>(x)[i];
-        if (fast) {
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-            uint32_t o[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                __half2 hv = __floats2half2_rn(bf16_lo(w[q]) * f1 * f2, bf16_hi(w[q]) * f1 * f2);
-                o[q] = *reinterpret_cast<uint32_t*>(&hv);
+    for (int k = 0; k < PPT; ++k) {
+        const int i = threadIdx.x + k * THREADS;
+        if (i < NP) {
+            uint4 u = xv[k];
+            if (fast) {
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    __half2 hv = __floats2half2_rn(bf16_lo(w[q]) * f1 * f2, bf16_hi(w[q]) * f1 * f2);
+                    o[q] = *reinterpret_cast<uint32_t*>(&hv);
+                }
+                u = make_uint4(o[0], o[1], o[2], o[3]);
             }
-            u = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(xs + x_index(i / 4, i % 4)) = u;
         }
-        *reinterpret_cast<uint4*>(xs + x_index(i / 4, i % 4)) = u;
     }
     __syncthreads();
     const uint16_t* xl = xs + lane * 32;
@@ -295,29 +316,34 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // Launch shape per format, from back-to-back timings of 12288 x 4096 and
-// 4096 x 12288 calls (GB300): NVFP4 one CTA of 1024 threads per SM with two
-// chunks in flight per lane; Q8_0 (twice the bytes per element) one CTA of
-// 512 threads per SM with up to eight.
+// 4096 x 12288 calls over rotating weights (GB300): one CTA per SM; NVFP4
+// with K = 4096 768 threads and four chunks in flight per lane (0.61 of the
+// measured copy peak on 12288 x 4096; 1024 threads with two: 0.56), else 896
+// threads and two chunks; Q8_0 (twice the bytes per element) 896 threads
+// and two chunks (0.81 on 12288 x 4096). D must divide CPL or be a multiple
+// of it.
 template <class F>
 struct DirCfg;
 template <>
 struct DirCfg<DirNvfp4> {
-    static constexpr int kThreads = 1024;
     template <int CPL>
-    static constexpr int depth() { return CPL % 2 == 0 || CPL == 1 ? 2 : CPL; }
+    static constexpr int threads() { return CPL == 4 ? 768 : 896; }
+    template <int CPL>
+    static constexpr int depth() { return CPL == 4 ? 4 : (CPL == 3 ? 3 : 2); }
 };
 template <>
 struct DirCfg<DirQ8> {
-    static constexpr int kThreads = 512;
     template <int CPL>
-    static constexpr int depth() { return CPL == 1 || CPL == 2 || CPL == 4 || CPL == 8 ? 8 : (CPL % 4 == 0 ? 4 : CPL); }
+    static constexpr int threads() { return 896; }
+    template <int CPL>
+    static constexpr int depth() { return CPL == 3 ? 3 : 2; }
 };
 
 template <class F, int CPL>
 cudaError_t launch_cpl(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y, int64_t M,
                        cudaStream_t stream)
 {
-    constexpr int T = DirCfg<F>::kThreads;
+    constexpr int T = DirCfg<F>::template threads<CPL>();
     constexpr int D = DirCfg<F>::template depth<CPL>();
     auto kern = gemv_direct_kernel<F, CPL, T, D>;
     int dev = 0;

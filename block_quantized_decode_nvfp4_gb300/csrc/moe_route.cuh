@@ -20,63 +20,58 @@ namespace bqd {
 // memory, row `logits`): the larger logit first, the lower expert index on
 // equal logits; when only NaN logits are left, the lowest index not yet
 // taken. Lane l keeps the logits of experts l + 32 j (j < NJ, NJ * 32 >= E)
-// in registers and a bit per taken expert. The weights are the softmax of
-// the selected logits (equal to the full softmax renormalised over them).
-// Lane s < topk receives the slot-s expert in *e_out and its weight in
-// *w_out; topk <= 32. Warp-collective.
+// in registers and a bit per taken expert. Each round a lane picks its own
+// best, then two warp reductions pick the warp's: the largest order-
+// preserving key (NaN lowest, -0 counted as +0 so that equal values tie)
+// and, among the lanes holding it, the lowest expert index. The weights are
+// the softmax of the selected logits (equal to the full softmax renormalised
+// over them). Lane s < topk receives the slot-s expert in *e_out and its
+// weight in *w_out; topk <= 32. Warp-collective.
+__device__ __forceinline__ uint32_t order_key(float v)
+{
+    if (v != v) return 0u;  // NaN: below every number
+    const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 template <int NJ>
 __device__ __forceinline__ void route_token_warp(const float* __restrict__ logits, int E, int topk, int lane,
                                                  int* e_out, float* w_out)
 {
     float v[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) v[j] = lane + 32 * j < E ? logits[lane + 32 * j] : 0.f;
+    uint32_t key[NJ];
     uint32_t taken = 0;  // bit j: expert lane + 32 j is taken (or does not exist)
 #pragma unroll
-    for (int j = 0; j < NJ; ++j)
-        if (lane + 32 * j >= E) taken |= 1u << j;
+    for (int j = 0; j < NJ; ++j) {
+        const bool in = lane + 32 * j < E;
+        v[j] = in ? logits[lane + 32 * j] : 0.f;
+        key[j] = order_key(v[j]);
+        if (!in) taken |= 1u << j;
+    }
     int my_e = 0;
     float my_l = 0.f, lmax = 0.f;
     for (int s = 0; s < topk; ++s) {
-        float bv = -INFINITY;
+        uint32_t bk = 0u;
         int be = INT_MAX;
+        float bv = 0.f;
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int e = lane + 32 * j;
-            if (!((taken >> j) & 1u) && (v[j] > bv || (v[j] == bv && e < be))) {
-                bv = v[j];
+            if (!((taken >> j) & 1u) && (key[j] > bk || (key[j] == bk && e < be))) {
+                bk = key[j];
                 be = e;
+                bv = v[j];
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
-        if (be == INT_MAX) {  // only NaN logits left: take the lowest free index
-            int fe = INT_MAX;
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-                if (!((taken >> j) & 1u) && lane + 32 * j < fe) fe = lane + 32 * j;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) fe = min(fe, __shfl_xor_sync(0xFFFFFFFFu, fe, o));
-            be = fe;
-            float own = 0.f;
-#pragma unroll
-            for (int j = 0; j < NJ; ++j)
-                if (lane + 32 * j == be) own = v[j];
-            bv = __shfl_sync(0xFFFFFFFFu, own, be & 31);
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const int we = __reduce_min_sync(0xFFFFFFFFu, bk == wk ? be : INT_MAX);
+        const float wv = __shfl_sync(0xFFFFFFFFu, bv, we & 31);
+        if ((we & 31) == lane) taken |= 1u << (we >> 5);
         if (lane == s) {
-            my_e = be;
-            my_l = bv;
+            my_e = we;
+            my_l = wv;
         }
-        if (s == 0) lmax = bv;
+        if (s == 0) lmax = wv;
     }
     const float ex = lane < topk ? expf(my_l - lmax) : 0.f;
     const float z = warp_sum(ex);

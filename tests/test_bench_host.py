@@ -88,9 +88,10 @@ def test_rotating_copies_exceed_three_l2():
 
 
 def test_moe_launch_count():
-    # T = 1 and 4 at top-8 with H = 2048, I = 512: the two small-batch kernels
+    # T = 1, 4 and 16 at top-8 with H = 2048, I = 512: the two batched kernels
     assert bench.moe_launches(1, 256, 2048, 512, 8) == 2
     assert bench.moe_launches(4, 256, 2048, 512, 8) == 2
-    # T = 16: route, gate_up, down, combine
-    assert bench.moe_launches(16, 256, 2048, 512, 8) == 4
+    assert bench.moe_launches(16, 256, 2048, 512, 8) == 2
+    # beyond the batched kernels' limits: route, gate_up, down, combine
+    assert bench.moe_launches(32, 256, 2048, 512, 8) == 4
     assert bench.moe_launches(1, 256, 2048, 384, 8) == 4

@@ -178,11 +178,12 @@ def _layer_fused(L):
     return y.cpu().numpy().reshape(T, H), ws
 
 
-# (T, E, H, I, topk): the first five take the small-batch kernels (T <= 4,
-# T * topk <= 32, H % 1024 == 0, I in {256, 512, 1024}), the last two the
-# route kernel and the expert streams
+# (T, E, H, I, topk): all but the last two take the batched kernels (T <= 16,
+# T * topk <= 128, T * H <= 32768, H >= 2I, I in {256, 512, 1024}); the last
+# two the route kernel and the expert streams
 SMALL_AND_LARGE = [(1, 64, 1024, 256, 8), (2, 16, 1024, 512, 4), (3, 64, 2048, 256, 8), (4, 32, 2048, 1024, 8),
-                   (4, 256, 2048, 512, 8), (5, 64, 1024, 256, 8), (16, 64, 1024, 256, 8)]
+                   (4, 256, 2048, 512, 8), (5, 64, 1024, 256, 8), (16, 64, 1024, 256, 8), (11, 32, 2048, 512, 8),
+                   (16, 256, 2048, 512, 8), (24, 64, 1024, 256, 4), (16, 64, 4096, 512, 8)]
 
 
 @pytest.mark.parametrize("T,E,H,I,topk", SMALL_AND_LARGE)
