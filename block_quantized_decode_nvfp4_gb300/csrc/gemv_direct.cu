@@ -318,18 +318,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Launch shape per format, from back-to-back timings of 12288 x 4096 and
 // 4096 x 12288 calls over rotating weights (GB300): one CTA per SM; NVFP4
 // with K = 4096 768 threads and four chunks in flight per lane (0.61 of the
-// measured copy peak on 12288 x 4096; 1024 threads with two: 0.56), else 896
-// threads and two chunks; Q8_0 (twice the bytes per element) 896 threads
-// and two chunks (0.81 on 12288 x 4096). D must divide CPL or be a multiple
-// of it.
+// measured copy peak on 12288 x 4096; 1024 threads with two: 0.56; 512 with
+// eight: 0.55), with K = 12288 512 threads and six (0.56 on 4096 x 12288;
+// 896 threads with two: 0.52; 512 with twelve: 0.53), else 896 threads and
+// two chunks; Q8_0 (twice the bytes per element) 896 threads and two chunks
+// (0.81 on 12288 x 4096, 0.76 on 4096 x 12288). D must divide CPL or be a
+// multiple of it.
 template <class F>
 struct DirCfg;
 template <>
 struct DirCfg<DirNvfp4> {
     template <int CPL>
-    static constexpr int threads() { return CPL == 4 ? 768 : 896; }
+    static constexpr int threads() { return CPL == 4 ? 768 : (CPL == 12 ? 512 : 896); }
     template <int CPL>
-    static constexpr int depth() { return CPL == 4 ? 4 : (CPL == 3 ? 3 : 2); }
+    static constexpr int depth() { return CPL == 4 ? 4 : (CPL == 12 ? 6 : (CPL == 3 ? 3 : 2)); }
 };
 template <>
 struct DirCfg<DirQ8> {
