@@ -525,14 +525,16 @@ def run_ours(args, rank, world):
         return statistics.median(ts), R
 
     b2b = {r.name: back_to_back_us(r) for r in rows + extra}
-    # the multi-token (verify) rows through both compute paths
+    # the multi-token (verify) rows through the CUDA-core, tcgen05 and warp-tile paths
     verify_paths = {}
     for r in rows:
         if r.kind == "nvfp4" and r.p["N"] > 1:
             cc = isolated_us(lambda r=r: r.run_path(bqd.BQD_PATH_CUDA_CORE))
             mma = isolated_us(lambda r=r: r.run_path(bqd.BQD_PATH_MMA))
+            tiles = isolated_us(lambda r=r: r.run_path(bqd.BQD_PATH_TILES))
             verify_paths[r.name] = {"cuda_core_us": round(cc, 3), "mma_us": round(mma, 3),
-                                    "mma_GB_s": round(r.bytes / mma / 1e3, 1), "speedup": round(cc / mma, 3)}
+                                    "tiles_us": round(tiles, 3), "mma_GB_s": round(r.bytes / mma / 1e3, 1),
+                                    "speedup": round(cc / mma, 3)}
 
     # ---- headline: K full steps, inputs resident in HBM
     peak, peak_kind = measured_peaks()

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     BQD_PATH_STREAM,
     BQD_PATH_MMA,
     BQD_PATH_DIRECT,
+    BQD_PATH_TILES,
     get_launch_flags,
     set_launch_flags,
     bqd_device_error,

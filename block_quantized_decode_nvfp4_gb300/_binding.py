@@ -21,6 +21,7 @@ BQD_PATH_CUDA_CORE = 1
 BQD_PATH_STREAM = 2
 BQD_PATH_MMA = 3
 BQD_PATH_DIRECT = 4
+BQD_PATH_TILES = 5
 BQD_LAUNCH_PDL = 1
 
 _lib = None

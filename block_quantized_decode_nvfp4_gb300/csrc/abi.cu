@@ -111,15 +111,17 @@ bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float te
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream)
 {
     if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_STREAM && path != BQD_PATH_MMA &&
-        path != BQD_PATH_DIRECT)
+        path != BQD_PATH_DIRECT && path != BQD_PATH_TILES)
         return BQD_ERR_PATH;
     bqd_status st = check_dense(codes, scales, x, y, M, K, N, 16, true);
     if (st != BQD_OK || M == 0) return st;
     if (path == BQD_PATH_STREAM && !bqd::stream_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if (path == BQD_PATH_MMA && !bqd::mma_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if (path == BQD_PATH_DIRECT && !bqd::direct_gemv_supported(M, K, N)) return BQD_ERR_PATH;
+    if (path == BQD_PATH_TILES && !bqd::tiles_gemv_supported(M, K, N)) return BQD_ERR_PATH;
     if ((st = check_arch()) != BQD_OK) return st;
     if (K == 0) return zero_output(y, M * N, stream);
+    const bool use_tiles = path == BQD_PATH_TILES;
     const bool use_direct = path == BQD_PATH_DIRECT || (path == BQD_PATH_AUTO && bqd::direct_gemv_supported(M, K, N));
     const bool use_stream = path == BQD_PATH_STREAM || (path == BQD_PATH_AUTO && bqd::stream_gemv_supported(M, K, N));
     const bool use_mma = path == BQD_PATH_MMA || (path == BQD_PATH_AUTO && N >= 2 && bqd::mma_gemv_supported(M, K, N));
@@ -127,6 +129,8 @@ bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float te
         return from_cuda(bqd::launch_nvfp4_gemv_direct(codes, scales, tensor_scale, x, y, M, K, stream));
     if (use_stream)
         return from_cuda(bqd::launch_nvfp4_gemv_stream(codes, scales, tensor_scale, x, y, M, K, stream));
+    if (use_tiles)
+        return from_cuda(bqd::launch_nvfp4_gemv_tiles(codes, scales, tensor_scale, x, y, M, K, N, stream));
     if (use_mma) return from_cuda(bqd::launch_nvfp4_gemv_mma(codes, scales, tensor_scale, x, y, M, K, N, stream));
     return from_cuda(bqd::launch_nvfp4_gemv_cuda_core(codes, scales, tensor_scale, x, y, M, K, N, stream));
 }

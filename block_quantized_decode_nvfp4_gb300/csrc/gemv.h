@@ -30,6 +30,13 @@ cudaError_t launch_nvfp4_gemv_direct(const uint8_t* codes, const uint8_t* scales
 cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
                                     int64_t K, cudaStream_t s);
 
+// Warp-tile tensor-core GEMV for a few tokens (gemv_tiles.cu): 2 <= N <= 16,
+// K a multiple of 1024, N * K <= 32768 (the activations pass through
+// registers once per CTA).
+bool tiles_gemv_supported(int64_t M, int64_t K, int N);
+cudaError_t launch_nvfp4_gemv_tiles(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                    float* y, int64_t M, int64_t K, int N, cudaStream_t s);
+
 // Bulk-copy streaming GEMV (gemv_stream.cu): N == 1, K % 256 == 0.
 bool stream_gemv_supported(int64_t M, int64_t K, int N);
 cudaError_t launch_nvfp4_gemv_stream(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,

@@ -77,6 +77,11 @@ enum {
                                loads, compile-time unrolled over a row, decode and mixed-precision FMAs on the
                                CUDA cores; N == 1 and K a multiple of 1024 with K / 1024 one of 1, 2, 3, 4, 6,
                                8, 12, 16, else BQD_ERR_PATH */
+    BQD_PATH_TILES = 5,     /* NVFP4 only: warp tiles of 8 weight rows x 16 token slots on the tensor cores
+                               (mma.sync m16n8k16, exact f16 or bf16 operands, fp32 accumulation), weights
+                               streamed straight into registers as for BQD_PATH_DIRECT, a CTA's tiles shared
+                               by its warps with a fixed-order sum; 2 <= N <= 16, K a multiple of 1024 and
+                               N * K <= 32768, else BQD_ERR_PATH. q8_0_gemv_path returns BQD_ERR_PATH */
     BQD_PATH_MMA = 3        /* NVFP4 only: weights decoded exactly to f16 (or bf16) in tensor memory and
                                multiplied on the tensor cores (tcgen05.mma, fp32 accumulation), the
                                (row tile, k) work split over thread-block clusters with a fixed-order
@@ -139,8 +144,9 @@ bqd_status nvfp4_gemv(const uint8_t* codes, const uint8_t* scales, float tensor_
 /* nvfp4_gemv with an explicit compute path (BQD_PATH_*), to compare paths.
  * AUTO takes, for N == 1, BQD_PATH_DIRECT where it applies, else
  * BQD_PATH_STREAM where it applies; for N >= 2 BQD_PATH_MMA where it
- * applies; else BQD_PATH_CUDA_CORE. q8_0_gemv_path's AUTO is the same
- * without the MMA path. */
+ * applies; else BQD_PATH_CUDA_CORE (BQD_PATH_TILES only when asked for:
+ * on the verify shapes it is slower than BQD_PATH_MMA). q8_0_gemv_path's
+ * AUTO is the same without the tensor-core paths. */
 bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
                            float* y, int64_t M, int64_t K, int N, int path, cudaStream_t stream);
 
