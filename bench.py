@@ -669,6 +669,23 @@ def run_profile_row(args):
     torch.cuda.synchronize()
 
 
+def run_profile_step(args):
+    """Run --steps decode steps (every row once per step, in step order) and
+    nothing else: the launch list of the timed region, for profilers."""
+    import torch
+
+    import block_quantized_decode_nvfp4_gb300 as bqd
+    from block_quantized_decode_nvfp4_gb300 import build as _build
+
+    _build.build()
+    bqd.set_launch_flags(bqd.BQD_LAUNCH_PDL if args.launch_pdl == "on" else 0)
+    rows = [Row(n, k, p, host_inputs(k, p, seed=0), torch, bqd) for n, k, p in rows_spec()]
+    for _ in range(args.steps):
+        for r in rows:
+            r.run()
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -685,6 +702,8 @@ def main():
                     help="only call this row of the step (e.g. 'q8_0 151936x4096 N=1') --profile-calls times, "
                          "for profilers; prints no JSON line")
     ap.add_argument("--profile-calls", type=int, default=3)
+    ap.add_argument("--profile-step", action="store_true",
+                    help="only run --steps decode steps (no per-row timings, no JSON line), for profilers")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -692,6 +711,9 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     if args.profile_row is not None:
         run_profile_row(args)
+        return
+    if args.profile_step:
+        run_profile_step(args)
         return
     if args.impl == "reference":
         run_reference(args, rank)
