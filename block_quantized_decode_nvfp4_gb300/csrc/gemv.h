@@ -83,11 +83,13 @@ cudaError_t launch_moe_stream_layer(const uint8_t* gu_codes, const uint8_t* gu_s
                                     int H, int I, int T, int topk, cudaStream_t stream);
 cudaError_t read_and_clear_moe_stream_error(unsigned int* out);
 
-// Small-batch MoE kernels (moe_small.cu): T <= 4, T * topk <= 32, E <= 512,
-// H % 1024 == 0, I in {256, 512, 1024}. With logits != nullptr every CTA
-// routes the tokens itself (the list arguments are ignored); otherwise the
-// caller's expert-major list is checked and used. Writes the workspace's
-// status word, h, and y (the combine is part of the down kernel).
+// Small-batch MoE kernels (moe_small.cu): the limits of moe_small_supported
+// (T <= 16, T * topk <= 128, E <= 512, H in {1024, ..., 8192}, I in {256,
+// 512, 1024}). With logits != nullptr every gate_up CTA routes the tokens
+// itself (the list arguments are ignored); otherwise the caller's
+// expert-major list is checked and used. Writes the workspace's status
+// word, per-(token, slot) list, h and h' (for the down kernel), and y (the
+// combine is part of the down kernel).
 bool moe_small_supported(int E, int H, int I, int T, int topk);
 cudaError_t launch_moe_small_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales,
                                    const float* gu_ts, const uint8_t* dn_codes, const uint8_t* dn_scales,

@@ -255,12 +255,15 @@ bqd_status moe_grouped_gemv(const uint8_t* gu_codes, const uint8_t* gu_scales, c
  *   256-byte aligned, owned by the caller, not shared by calls that may
  *   overlap. Its first int32 is the status word, h starts where
  *   moe_grouped_gemv puts it.
- *   For a few tokens (T <= 4, T * topk <= 32, E <= 512, H % 1024 == 0, I one
- *   of 256, 512, 1024) the routing is computed inside the two layer kernels
- *   (no route kernel, no list in memory; the down kernel folds in the
- *   weighted combine); otherwise moe_route_topk writes the list into the
- *   workspace and moe_grouped_gemv follows. Limits as moe_grouped_gemv plus
- *   those of moe_route_topk. NaN logits are outside the contract.
+ *   For decode and verify batches (T <= 16, T * topk <= 128, topk <= 32,
+ *   E <= 512, H one of 1024, 2048, 4096, 8192, I one of 256, 512, 1024,
+ *   H >= 2 I, topk * I <= 8192, T * H <= 32768) the layer is two kernels:
+ *   the gate_up kernel routes the tokens in every CTA (no route kernel) and
+ *   leaves the per-(token, slot) list and h for the down kernel, which
+ *   folds in the weighted combine; otherwise moe_route_topk writes the list
+ *   into the workspace and moe_grouped_gemv follows. Limits as
+ *   moe_grouped_gemv plus those of moe_route_topk. NaN logits are outside
+ *   the contract.
  */
 bqd_status moe_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales, const float* gu_ts,
                      const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts, const uint16_t* x,
