@@ -681,8 +681,10 @@ __global__ void __launch_bounds__(kThG, 1)
         s_emin[threadIdx.x] = INT_MAX;
     }
     pdl_wait();  // logits, the list and x may come from the previous kernel
-    // x, copied to shared memory asynchronously (its latency overlaps the routing)
-    const int npc = T * (H / 8);  // 16-byte pieces
+    // x, copied to shared memory asynchronously (its latency overlaps the
+    // routing), then staged in one pass through registers
+    constexpr int kXP = kMaxTH / 8 / kThG;  // 16-byte pieces per thread
+    const int npc = T * (H / 8);
     for (int pc = threadIdx.x; pc < npc; pc += kThG) cp_async16(xraw + pc * 8, x + pc * 8);
     if (logits)
         route_in_cta(logits, T, E, topk, NT, L, s_mask, s_eoff, s_scan);
@@ -710,35 +712,41 @@ __global__ void __launch_bounds__(kThG, 1)
     auto stage_x = [&]() -> bool {
         cp_async_wait_all();
         __syncthreads();
+        uint4 xv[kXP];  // piece threadIdx.x + r kThG (consecutive per warp: no bank conflicts)
+#pragma unroll
+        for (int r = 0; r < kXP; ++r) {
+            const int pc = threadIdx.x + r * kThG;
+            if (pc < npc) xv[r] = *reinterpret_cast<const uint4*>(xraw + pc * 8);
+        }
         // |x| bit patterns (sign cleared) order like the values: the largest
         // and the smallest nonzero pattern per token give its exponent range
         // (and show an infinity or NaN, 0x7F80 and up, or a subnormal, below
-        // 0x0080), two halfword max/min per 32-bit word
-        for (int k = 0; k * kThG < npc; ++k) {
-            const int pc = threadIdx.x + k * kThG;
-            if (k * kThG + warp * kWarp < npc) {  // warp-uniform
-                const uint4 xq = *reinterpret_cast<const uint4*>(xraw + pc * 8);
-                const uint32_t w4[4] = {xq.x, xq.y, xq.z, xq.w};
+        // 0x0080), a halfword max and min per 32-bit word; a warp's 32
+        // pieces lie in one token
+#pragma unroll
+        for (int r = 0; r < kXP; ++r) {
+            if (r * kThG + warp * kWarp < npc) {  // warp-uniform
+                const uint32_t w4[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
                 uint32_t hmax = 0u, hmin = 0xFFFFFFFFu;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const uint32_t m = w4[q] & 0x7FFF7FFFu;
                     hmax = __vmaxu2(hmax, m);
-                    hmin = __vminu2(hmin, m | __vcmpeq2(m, 0u));  // zero halves count as 0xFFFF
+                    hmin = __vminu2(hmin, __vsub2(m, 0x00010001u));  // a zero half wraps to 0xFFFF
                 }
                 const uint32_t bmax = __reduce_max_sync(0xFFFFFFFFu, max(hmax & 0xFFFFu, hmax >> 16));
-                const uint32_t bmin = __reduce_min_sync(0xFFFFFFFFu, min(hmin & 0xFFFFu, hmin >> 16));
+                const uint32_t bmin = __reduce_min_sync(0xFFFFFFFFu, min(hmin & 0xFFFFu, hmin >> 16)) + 1u;
                 if (lane == 0) {
-                    const int t = pc / (H / 8);
+                    const int t = (r * kThG + warp * kWarp) / (H / 8);
                     atomicMax(&s_emax[t], static_cast<int>(bmax));
-                    atomicMin(&s_emin[t], static_cast<int>(bmin));
+                    atomicMin(&s_emin[t], static_cast<int>(bmin));  // 0x10000: no nonzero element
                 }
             }
         }
         __syncthreads();
         if (threadIdx.x < T) {  // patterns to exponents (a token of zeros keeps emin = INT_MAX)
             const int bmax = s_emax[threadIdx.x], bmin = s_emin[threadIdx.x];
-            const bool any = bmin < 0xFFFF;
+            const bool any = bmin < 0x10000;
             if (bmax >= 0x7F80 || (any && bmin < 0x0080) || (any && (bmax >> 7) - (bmin >> 7) > 31))
                 atomicOr(&s_flags, 1);
             s_emax[threadIdx.x] = bmax >> 7;
@@ -751,9 +759,12 @@ __global__ void __launch_bounds__(kThG, 1)
                                       ? s_emax[threadIdx.x] - 127 - 14
                                       : 0;
         __syncthreads();
-        for (int pc = threadIdx.x; pc < npc; pc += kThG) {
+#pragma unroll
+        for (int r = 0; r < kXP; ++r) {
+            const int pc = threadIdx.x + r * kThG;
+            if (pc >= npc) continue;
             const int t = pc / (H / 8), v = pc - t * (H / 8);
-            uint4 uu = *reinterpret_cast<const uint4*>(xraw + pc * 8);
+            uint4 uu = xv[r];
             if (fast) {
                 // x * 2^-s as two exact multiplies by normal powers of two
                 const int se = s_sexp[t], e1 = max(-126, min(127, -se));
