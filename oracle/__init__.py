@@ -135,6 +135,44 @@ def q8_0_gemv(q, d, x, M, K, rows=None):
     return y, a
 
 
+# ---------------------------------------------------------------- decode-path epilogues
+def _gemv(fmt, w, x, M, K, rows):
+    if fmt == "nvfp4":
+        codes, scales, ts = w
+        return nvfp4_gemv(codes, scales, ts, x, M, K, rows=rows)
+    q, d = w
+    return q8_0_gemv(q, d, x, M, K, rows=rows)
+
+
+def gemv_add(fmt, w, x, r, M, K, rows=None):
+    """y = W x + r for a residual r (fp32 [N][M]), the dense GEMV's residual
+    epilogue ("Vemloir/LumenLLM" README, Kernels bullet: the decode path's
+    fused epilogues). fmt "nvfp4" with w = (codes, scales, ts) or "q8_0" with
+    w = (q, d). Returns (y, a): y fp64 [N][len(rows) or M], a = sum|w x|."""
+    y, a = _gemv(fmt, w, x, M, K, rows)
+    r = np.asarray(r, dtype=np.float32).reshape(y.shape[0], -1).astype(np.float64)
+    if rows is not None:
+        r = r[:, np.asarray(rows)]
+    return y + r, a
+
+
+def silu(g):
+    """SiLU(g) = g / (1 + e^-g), fp64."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def gemv_silu_mul(fmt, w, x, I, K, rows=None):
+    """h_i = SiLU(g_i) u_i with g = rows 0..I-1 and u = rows I..2I-1 of the
+    gate_up weight times x: a dense MLP's first projection with its
+    activation fused ("Vemloir/LumenLLM" README, Kernels bullet). Returns
+    (h, g, u, ag, au), fp64 [N][len(rows) or I]."""
+    rows = np.arange(I) if rows is None else np.asarray(rows, dtype=np.int64)
+    g, ag = _gemv(fmt, w, x, 2 * I, K, rows)
+    u, au = _gemv(fmt, w, x, 2 * I, K, rows + I)
+    return silu(g) * u, g, u, ag, au
+
+
 # ---------------------------------------------------------------- MoE
 def moe_route(logits, topk):
     logits = _c(logits, np.float32)
