@@ -98,15 +98,24 @@ def rows_spec():
 
 def extra_rows_spec():
     """Rows reported beside the step but not part of it: the tiny 256 x 512
-    NVFP4 workload (ts = 1.0), whose time is launch latency, not bandwidth."""
-    return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1))]
+    NVFP4 workload (ts = 1.0), whose time is launch latency, not bandwidth;
+    and the decode-path epilogue fusions on the layer shapes (gate_up with
+    SiLU * up on the 12288 x 4096 gate/up weight, I = 6144; down with the
+    residual add on 4096 x 12288)."""
+    return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1)),
+            ("nvfp4 gate_up+SiLU 12288x4096 N=1", "nvfp4_silu", dict(M=12288, K=4096, N=1)),
+            ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1))]
 
 
 def host_inputs(kind, p, seed=0):
     if kind == "nvfp4_tiny":
         return syn.tiny_nvfp4(seed=seed)
-    if kind == "nvfp4":
+    if kind in ("nvfp4", "nvfp4_silu"):
         return syn.dense_nvfp4(p["M"], p["K"], N=p["N"], seed=seed)
+    if kind == "nvfp4_add":
+        h = syn.dense_nvfp4(p["M"], p["K"], N=p["N"], seed=seed)
+        h["r"] = np.random.default_rng(seed + 1).standard_normal((p["N"], p["M"])).astype(np.float32)
+        return h
     if kind == "q8_0":
         return syn.dense_q8_0(p["M"], p["K"], N=p["N"], seed=seed)
     return syn.moe_layer(T=p["T"], E=p["E"], H=p["H"], I=p["I"], topk=p["topk"], seed=seed)
@@ -115,6 +124,10 @@ def host_inputs(kind, p, seed=0):
 def row_bytes(kind, p, host):
     if kind in ("nvfp4", "nvfp4_tiny"):
         return nvfp4_bytes(p["M"], p["K"], p["N"])
+    if kind == "nvfp4_silu":  # the output is h, half the rows
+        return nvfp4_bytes(p["M"], p["K"], p["N"]) - 4 * p["N"] * p["M"] // 2
+    if kind == "nvfp4_add":  # the residual is read
+        return nvfp4_bytes(p["M"], p["K"], p["N"]) + 4 * p["N"] * p["M"]
     if kind == "q8_0":
         return q8_0_bytes(p["M"], p["K"], p["N"])
     return moe_bytes(p["T"], p["E"], p["H"], p["I"], p["topk"], host["logits"])
@@ -245,7 +258,7 @@ class Row:
         self.torch, self.bqd = torch, bqd
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
         self.launches = 1
-        if kind in ("nvfp4", "q8_0", "nvfp4_tiny"):
+        if kind in ("nvfp4", "q8_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add"):
             M, K, N = p["M"], p["K"], p["N"]
             if kind != "q8_0":
                 self.w = (d(host["codes"]), d(host["scales"]))
@@ -256,6 +269,9 @@ class Row:
             self.x = d(host["x"])
             self.y = torch.empty(N * M, dtype=torch.float32, device="cuda")
             self.in_bytes = self.x.numel() * 2
+            if kind == "nvfp4_add":
+                self.r = d(host["r"])
+                self.in_bytes += self.r.numel() * 4
         else:
             T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
             self.w = tuple(d(host[n]) for n in ("gu_codes", "gu_scales", "gu_ts", "dn_codes", "dn_scales", "dn_ts"))
@@ -287,6 +303,10 @@ class Row:
         w = self.copies[copy]
         if self.kind in ("nvfp4", "nvfp4_tiny"):
             b.nvfp4_gemv(w[0], w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"])
+        elif self.kind == "nvfp4_silu":
+            b.nvfp4_gemv_silu_mul(w[0], w[1], self.ts, self.x, self.y, p["M"] // 2, p["K"], p["N"])
+        elif self.kind == "nvfp4_add":
+            b.nvfp4_gemv_add(w[0], w[1], self.ts, self.x, self.r, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "q8_0":
             b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         else:

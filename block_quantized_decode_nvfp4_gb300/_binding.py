@@ -47,6 +47,10 @@ SIGNATURES = {
     "nvfp4_gemv_path": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "nvfp4_gemv_add": (_i32, [_vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "q8_0_gemv_add": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "nvfp4_gemv_silu_mul": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "q8_0_gemv_silu_mul": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "bqd_device_error": (_i32, [C.POINTER(C.c_uint)]),
     "bqd_debug_stream_fault": (_i32, [_i32, C.c_longlong]),
     "nvfp4_dequant": (_i32, [_vp, _vp, _f32, _vp, _i64, _i64, _vp]),
@@ -129,6 +133,26 @@ def q8_0_gemv(q, d, x, y, M, K, N, stream=None):
 def q8_0_gemv_path(q, d, x, y, M, K, N, path, stream=None):
     _check(lib().q8_0_gemv_path(_ptr(q), _ptr(d), _ptr(x), _ptr(y), M, K, N, path, _stream(stream)),
            "q8_0_gemv_path")
+
+
+def nvfp4_gemv_add(codes, scales, tensor_scale, x, residual, y, M, K, N=1, stream=None):
+    _check(lib().nvfp4_gemv_add(_ptr(codes), _ptr(scales), tensor_scale, _ptr(x), _ptr(residual), _ptr(y), M, K, N,
+                                _stream(stream)), "nvfp4_gemv_add")
+
+
+def q8_0_gemv_add(q, d, x, residual, y, M, K, N=1, stream=None):
+    _check(lib().q8_0_gemv_add(_ptr(q), _ptr(d), _ptr(x), _ptr(residual), _ptr(y), M, K, N, _stream(stream)),
+           "q8_0_gemv_add")
+
+
+def nvfp4_gemv_silu_mul(codes, scales, tensor_scale, x, h, I, K, N=1, stream=None):
+    _check(lib().nvfp4_gemv_silu_mul(_ptr(codes), _ptr(scales), tensor_scale, _ptr(x), _ptr(h), I, K, N,
+                                     _stream(stream)), "nvfp4_gemv_silu_mul")
+
+
+def q8_0_gemv_silu_mul(q, d, x, h, I, K, N=1, stream=None):
+    _check(lib().q8_0_gemv_silu_mul(_ptr(q), _ptr(d), _ptr(x), _ptr(h), I, K, N, _stream(stream)),
+           "q8_0_gemv_silu_mul")
 
 
 def bqd_device_error() -> int:

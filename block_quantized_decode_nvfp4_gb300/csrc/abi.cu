@@ -165,6 +165,58 @@ bqd_status q8_0_gemv(const int8_t* q, const uint16_t* d, const uint16_t* x, floa
     return q8_0_gemv_path(q, d, x, y, M, K, N, BQD_PATH_AUTO, stream);
 }
 
+// ---------------------------------------------------------------- decode-path epilogues
+namespace {
+
+// The fused-epilogue GEMVs run the direct kernel: N == 1, M >= 1, K a
+// multiple of 1024 with K / 1024 in {1, 2, 3, 4, 6, 8, 12, 16}.
+bqd_status check_epilogue(const void* a, const void* b, const void* x, const void* out, const float* r, bool has_r,
+                          int64_t rows, int64_t K, int N, int kdiv)
+{
+    bqd_status st = check_dense(a, b, x, out, rows, K, N, kdiv, true);
+    if (st != BQD_OK) return st;
+    if (N != 1 || rows < 1 || !bqd::direct_gemv_supported(rows, K, 1)) return BQD_ERR_SHAPE;
+    if (has_r && !r) return BQD_ERR_NULL;
+    if (has_r && !aligned16(r)) return BQD_ERR_ALIGN;
+    return check_arch();
+}
+
+}  // namespace
+
+bqd_status nvfp4_gemv_add(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
+                          const float* residual, float* y, int64_t M, int64_t K, int N, cudaStream_t stream)
+{
+    const bqd_status st = check_epilogue(codes, scales, x, y, residual, true, M, K, N, 16);
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_nvfp4_gemv_direct_add(codes, scales, tensor_scale, x, residual, y, M, K, stream));
+}
+
+bqd_status q8_0_gemv_add(const int8_t* q, const uint16_t* d, const uint16_t* x, const float* residual, float* y,
+                         int64_t M, int64_t K, int N, cudaStream_t stream)
+{
+    const bqd_status st = check_epilogue(q, d, x, y, residual, true, M, K, N, 32);
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_q8_0_gemv_direct_add(q, d, x, residual, y, M, K, stream));
+}
+
+bqd_status nvfp4_gemv_silu_mul(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
+                               float* h, int64_t I, int64_t K, int N, cudaStream_t stream)
+{
+    if (I < 1 || I > (int64_t(1) << 38)) return BQD_ERR_SHAPE;
+    const bqd_status st = check_epilogue(codes, scales, x, h, nullptr, false, 2 * I, K, N, 16);
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_nvfp4_gemv_direct_silu_mul(codes, scales, tensor_scale, x, h, I, K, stream));
+}
+
+bqd_status q8_0_gemv_silu_mul(const int8_t* q, const uint16_t* d, const uint16_t* x, float* h, int64_t I, int64_t K,
+                              int N, cudaStream_t stream)
+{
+    if (I < 1 || I > (int64_t(1) << 38)) return BQD_ERR_SHAPE;
+    const bqd_status st = check_epilogue(q, d, x, h, nullptr, false, 2 * I, K, N, 32);
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_q8_0_gemv_direct_silu_mul(q, d, x, h, I, K, stream));
+}
+
 bqd_status bqd_device_error(unsigned int* bits_out)
 {
     if (!bits_out) return BQD_ERR_NULL;

@@ -29,6 +29,17 @@ cudaError_t launch_nvfp4_gemv_direct(const uint8_t* codes, const uint8_t* scales
                                      float* y, int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
                                     int64_t K, cudaStream_t s);
+// The same kernel with a fused epilogue: y = W x + r (y may be r); and, on a
+// gate_up weight of 2I rows (gate rows 0..I-1, up rows I..2I-1),
+// h = SiLU(gate . x) * (up . x).
+cudaError_t launch_nvfp4_gemv_direct_add(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                         const float* r, float* y, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_q8_0_gemv_direct_add(const int8_t* q, const uint16_t* d, const uint16_t* x, const float* r,
+                                        float* y, int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_nvfp4_gemv_direct_silu_mul(const uint8_t* codes, const uint8_t* scales, float ts,
+                                              const uint16_t* x, float* h, int64_t I, int64_t K, cudaStream_t s);
+cudaError_t launch_q8_0_gemv_direct_silu_mul(const int8_t* q, const uint16_t* d, const uint16_t* x, float* h,
+                                             int64_t I, int64_t K, cudaStream_t s);
 
 // Warp-tile tensor-core GEMV for a few tokens (gemv_tiles.cu): 2 <= N <= 16,
 // K a multiple of 1024, N * K <= 32768 (the activations pass through

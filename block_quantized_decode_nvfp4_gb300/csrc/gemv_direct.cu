@@ -177,11 +177,29 @@ struct DirQ8 {
 // g % CPL) lives in buf[g % D]; D divides CPL or is a multiple of it, so
 // with U = max(1, D / CPL) rows unrolled per body the slot, the chunk and
 // the row offset of every item are compile-time constants.
-template <class F, int CPL, int D, bool FAST>
+// Epilogues of a row's dot product v (the row's output is ts * 2^sexp * v):
+// kEpiPlain writes it; kEpiAdd adds the residual r[row] (y may be r);
+// kEpiSiluMul takes the rows in pairs (virtual row 2i: gate row i, 2i + 1:
+// up row half + i) and writes SiLU(g) * u to y[i].
+constexpr int kEpiPlain = 0, kEpiAdd = 1, kEpiSiluMul = 2;
+
+// Physical weight row of virtual row v.
+template <int EPI>
+__device__ __forceinline__ int64_t phys_row(int64_t v, int64_t half)
+{
+    if constexpr (EPI == kEpiSiluMul)
+        return (v & 1) ? half + (v >> 1) : (v >> 1);
+    else
+        return v;
+}
+
+template <class F, int CPL, int D, bool FAST, int EPI>
 __device__ __forceinline__ void direct_rows(typename F::Item (&buf)[D], const uint8_t* cp, const uint8_t* sp,
                                             int64_t cpitch, int64_t spitch, const uint16_t* xl, int sw, float* y,
-                                            int64_t r_lo, int64_t r_hi, float ts, int sexp, int lane)
+                                            const float* r, int64_t half, int64_t r_lo, int64_t r_hi, float ts,
+                                            int sexp, int lane)
 {
+    float gsave = 0.f;  // kEpiSiluMul: the gate row's output, until its up row is done
     static_assert(CPL % D == 0 || D % CPL == 0, "the ring depth must divide a row or be a multiple of one");
     constexpr int U = D > CPL ? D / CPL : 1;
     for (int64_t row0 = r_lo; row0 < r_hi; row0 += U) {
@@ -194,26 +212,39 @@ __device__ __forceinline__ void direct_rows(typename F::Item (&buf)[D], const ui
                     const int g = u * CPL + i;
                     const typename F::Item cur = buf[g % D];
                     const int nr = (g + D) / CPL, nc = (g + D) % CPL;
-                    if (row0 + nr < r_hi)
-                        buf[g % D] = F::load(cp + (row0 + nr) * cpitch + nc * 32 * F::kCodeBytes,
-                                             sp + (row0 + nr) * spitch + nc * 64);
+                    if (row0 + nr < r_hi) {
+                        const int64_t pr = phys_row<EPI>(row0 + nr, half);
+                        buf[g % D] = F::load(cp + pr * cpitch + nc * 32 * F::kCodeBytes, sp + pr * spitch + nc * 64);
+                    }
                     F::template dot<FAST>(cur, xl + i * 1024, sw, acc);
                     // keep the next chunk's shared-memory loads after this chunk's arithmetic
                     asm volatile("" ::: "memory");
                 }
-                const float v = warp_sum(acc);
-                if (lane == 0) y[row0 + u] = ldexpf(v * ts, sexp);
+                const float v = ldexpf(warp_sum(acc) * ts, sexp);
+                const int64_t row = row0 + u;
+                if constexpr (EPI == kEpiPlain) {
+                    if (lane == 0) y[row] = v;
+                } else if constexpr (EPI == kEpiAdd) {
+                    if (lane == 0) y[row] = v + r[row];
+                } else {
+                    if (!(row & 1))
+                        gsave = v;
+                    else if (lane == 0)
+                        y[row >> 1] = gsave / (1.0f + expf(-gsave)) * v;
+                }
             }
         }
     }
 }
 
-// Dynamic shared memory: K f16 (or bf16) activations.
-template <class F, int CPL, int THREADS, int D>
+// Dynamic shared memory: K f16 (or bf16) activations. M is the number of
+// virtual rows (2 * half for kEpiSiluMul, whose warps take whole pairs).
+template <class F, int CPL, int THREADS, int D, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     gemv_direct_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, float ts,
-                       const uint16_t* __restrict__ x, float* __restrict__ y, int64_t M)
+                       const uint16_t* __restrict__ x, float* y, const float* r, int64_t M)
 {
+    const int64_t half = M / 2;
     constexpr int W = THREADS / kWarp;
     constexpr int64_t K = 1024 * CPL;
     constexpr int64_t cpitch = K / 32 * F::kCodeBytes, spitch = K / 16;
@@ -225,13 +256,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     // this warp's rows: an even split of [0, M) over all warps of the grid
     const uint32_t gw = blockIdx.x * W + warp, nw = gridDim.x * W;
     int64_t r_lo, r_hi;
-    if (M * nw < (int64_t(1) << 32)) {  // 32-bit division when it is exact
-        const uint32_t m = static_cast<uint32_t>(M);
+    const int64_t units = EPI == kEpiSiluMul ? half : M;  // rows, or row pairs
+    if (units * nw < (int64_t(1) << 32)) {  // 32-bit division when it is exact
+        const uint32_t m = static_cast<uint32_t>(units);
         r_lo = m * gw / nw;
         r_hi = m * (gw + 1) / nw;
     } else {
-        r_lo = M * gw / nw;
-        r_hi = M * (gw + 1) / nw;
+        r_lo = units * gw / nw;
+        r_hi = units * (gw + 1) / nw;
+    }
+    if constexpr (EPI == kEpiSiluMul) {
+        r_lo *= 2;
+        r_hi *= 2;
     }
     const uint8_t* cp = codes + lane * F::kCodeBytes;
     const uint8_t* sp = scales + lane * 2;
@@ -245,7 +281,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
     for (int d = 0; d < D; ++d) {
         const int64_t row = r_lo + d / CPL;
-        if (row < r_hi) buf[d] = F::load(cp + row * cpitch + (d % CPL) * 32 * F::kCodeBytes, sp + row * spitch + (d % CPL) * 64);
+        if (row < r_hi) {
+            const int64_t pr = phys_row<EPI>(row, half);
+            buf[d] = F::load(cp + pr * cpitch + (d % CPL) * 32 * F::kCodeBytes, sp + pr * spitch + (d % CPL) * 64);
+        }
     }
     pdl_trigger();
     __syncthreads();
@@ -310,9 +349,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint16_t* xl = xs + lane * 32;
     const int sw = (lane >> 1) & 3;
     if (fast)
-        direct_rows<F, CPL, D, true>(buf, cp, sp, cpitch, spitch, xl, sw, y, r_lo, r_hi, ts, sexp, lane);
+        direct_rows<F, CPL, D, true, EPI>(buf, cp, sp, cpitch, spitch, xl, sw, y, r, half, r_lo, r_hi, ts, sexp,
+                                          lane);
     else
-        direct_rows<F, CPL, D, false>(buf, cp, sp, cpitch, spitch, xl, sw, y, r_lo, r_hi, ts, sexp, lane);
+        direct_rows<F, CPL, D, false, EPI>(buf, cp, sp, cpitch, spitch, xl, sw, y, r, half, r_lo, r_hi, ts, sexp,
+                                           lane);
 }
 
 // Launch shape per format, from back-to-back timings of 12288 x 4096 and
@@ -341,13 +382,13 @@ struct DirCfg<DirQ8> {
     static constexpr int depth() { return CPL == 3 ? 3 : 2; }
 };
 
-template <class F, int CPL>
-cudaError_t launch_cpl(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y, int64_t M,
-                       cudaStream_t stream)
+template <class F, int CPL, int EPI>
+cudaError_t launch_cpl(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
+                       const float* r, int64_t M, cudaStream_t stream)
 {
     constexpr int T = DirCfg<F>::template threads<CPL>();
     constexpr int D = DirCfg<F>::template depth<CPL>();
-    auto kern = gemv_direct_kernel<F, CPL, T, D>;
+    auto kern = gemv_direct_kernel<F, CPL, T, D, EPI>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -367,22 +408,22 @@ cudaError_t launch_cpl(const uint8_t* codes, const uint8_t* scales, float ts, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = launch_flags() & kLaunchPdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, codes, scales, ts, x, y, M);
+    return cudaLaunchKernelEx(&cfg, kern, codes, scales, ts, x, y, r, M);
 }
 
-template <class F>
+template <class F, int EPI>
 cudaError_t launch_direct(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
-                          int64_t M, int64_t K, cudaStream_t s)
+                          const float* r, int64_t M, int64_t K, cudaStream_t s)
 {
     switch (K / 1024) {
-        case 1: return launch_cpl<F, 1>(codes, scales, ts, x, y, M, s);
-        case 2: return launch_cpl<F, 2>(codes, scales, ts, x, y, M, s);
-        case 3: return launch_cpl<F, 3>(codes, scales, ts, x, y, M, s);
-        case 4: return launch_cpl<F, 4>(codes, scales, ts, x, y, M, s);
-        case 6: return launch_cpl<F, 6>(codes, scales, ts, x, y, M, s);
-        case 8: return launch_cpl<F, 8>(codes, scales, ts, x, y, M, s);
-        case 12: return launch_cpl<F, 12>(codes, scales, ts, x, y, M, s);
-        case 16: return launch_cpl<F, 16>(codes, scales, ts, x, y, M, s);
+        case 1: return launch_cpl<F, 1, EPI>(codes, scales, ts, x, y, r, M, s);
+        case 2: return launch_cpl<F, 2, EPI>(codes, scales, ts, x, y, r, M, s);
+        case 3: return launch_cpl<F, 3, EPI>(codes, scales, ts, x, y, r, M, s);
+        case 4: return launch_cpl<F, 4, EPI>(codes, scales, ts, x, y, r, M, s);
+        case 6: return launch_cpl<F, 6, EPI>(codes, scales, ts, x, y, r, M, s);
+        case 8: return launch_cpl<F, 8, EPI>(codes, scales, ts, x, y, r, M, s);
+        case 12: return launch_cpl<F, 12, EPI>(codes, scales, ts, x, y, r, M, s);
+        case 16: return launch_cpl<F, 16, EPI>(codes, scales, ts, x, y, r, M, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -401,14 +442,40 @@ bool direct_gemv_supported(int64_t M, int64_t K, int N)
 cudaError_t launch_nvfp4_gemv_direct(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
                                      float* y, int64_t M, int64_t K, cudaStream_t s)
 {
-    return launch_direct<DirNvfp4>(codes, scales, ts, x, y, M, K, s);
+    return launch_direct<DirNvfp4, kEpiPlain>(codes, scales, ts, x, y, nullptr, M, K, s);
 }
 
 cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
                                     int64_t K, cudaStream_t s)
 {
-    return launch_direct<DirQ8>(reinterpret_cast<const uint8_t*>(q), reinterpret_cast<const uint8_t*>(d), 1.0f, x, y,
-                                M, K, s);
+    return launch_direct<DirQ8, kEpiPlain>(reinterpret_cast<const uint8_t*>(q), reinterpret_cast<const uint8_t*>(d),
+                                           1.0f, x, y, nullptr, M, K, s);
+}
+
+cudaError_t launch_nvfp4_gemv_direct_add(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
+                                         const float* r, float* y, int64_t M, int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirNvfp4, kEpiAdd>(codes, scales, ts, x, y, r, M, K, s);
+}
+
+cudaError_t launch_q8_0_gemv_direct_add(const int8_t* q, const uint16_t* d, const uint16_t* x, const float* r,
+                                        float* y, int64_t M, int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirQ8, kEpiAdd>(reinterpret_cast<const uint8_t*>(q), reinterpret_cast<const uint8_t*>(d),
+                                         1.0f, x, y, r, M, K, s);
+}
+
+cudaError_t launch_nvfp4_gemv_direct_silu_mul(const uint8_t* codes, const uint8_t* scales, float ts,
+                                              const uint16_t* x, float* h, int64_t I, int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirNvfp4, kEpiSiluMul>(codes, scales, ts, x, h, nullptr, 2 * I, K, s);
+}
+
+cudaError_t launch_q8_0_gemv_direct_silu_mul(const int8_t* q, const uint16_t* d, const uint16_t* x, float* h,
+                                             int64_t I, int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirQ8, kEpiSiluMul>(reinterpret_cast<const uint8_t*>(q), reinterpret_cast<const uint8_t*>(d),
+                                             1.0f, x, h, nullptr, 2 * I, K, s);
 }
 
 }  // namespace bqd

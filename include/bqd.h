@@ -161,6 +161,41 @@ bqd_status nvfp4_gemv_path(const uint8_t* codes, const uint8_t* scales, float te
 bqd_status q8_0_gemv(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K, int N,
                      cudaStream_t stream);
 
+/*
+ * nvfp4_gemv_add -- y[m] = ts * sum_k e2m1(c[m][k]) * e4m3(s[m][k/16]) * x[k]
+ *                   + residual[m]: the GEMV with the residual add of a decode
+ * layer fused into its epilogue ("Vemloir/LumenLLM" README, Kernels bullet:
+ * the decode path's fused epilogues, next to the warp-shuffle GEMVs).
+ *   Arguments as nvfp4_gemv plus residual fp32 [M] (device, 16-byte aligned;
+ *   it may be y itself: each output is read, then written, by one thread).
+ *   The sum is rounded to fp32 once, then the residual added (one more fp32
+ *   rounding). N == 1 (the decode path), M >= 1, K a multiple of 1024 with
+ *   K / 1024 in {1, 2, 3, 4, 6, 8, 12, 16}; else BQD_ERR_SHAPE. Runs the
+ *   direct kernel (BQD_PATH_DIRECT) with its launch options.
+ */
+bqd_status nvfp4_gemv_add(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
+                          const float* residual, float* y, int64_t M, int64_t K, int N, cudaStream_t stream);
+
+/* q8_0_gemv_add -- q8_0_gemv plus residual[m], as nvfp4_gemv_add. */
+bqd_status q8_0_gemv_add(const int8_t* q, const uint16_t* d, const uint16_t* x, const float* residual, float* y,
+                         int64_t M, int64_t K, int N, cudaStream_t stream);
+
+/*
+ * nvfp4_gemv_silu_mul -- h[i] = SiLU(g[i]) * u[i], g = W[i] . x (gate),
+ * u = W[I + i] . x (up): a dense MLP's gate_up projection with its
+ * activation fused, so g and u never reach memory ("Vemloir/LumenLLM"
+ * README, Kernels bullet). W is NVFP4 [2I][K] (codes [2I][K/2], scales
+ * [2I][K/16], rows 0..I-1 gate, I..2I-1 up, as the MoE experts' gate_up);
+ * h fp32 [I]. g and u are the GEMV's fp32 outputs; SiLU(g) = g / (1 +
+ * e^-g) in fp32. N == 1, I >= 1, K as nvfp4_gemv_add; else BQD_ERR_SHAPE.
+ */
+bqd_status nvfp4_gemv_silu_mul(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x,
+                               float* h, int64_t I, int64_t K, int N, cudaStream_t stream);
+
+/* q8_0_gemv_silu_mul -- the same on a Q8_0 gate_up weight (q [2I][K], d [2I][K/32]). */
+bqd_status q8_0_gemv_silu_mul(const int8_t* q, const uint16_t* d, const uint16_t* x, float* h, int64_t I, int64_t K,
+                              int N, cudaStream_t stream);
+
 /* q8_0_gemv with an explicit compute path (BQD_PATH_*). */
 bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K,
                           int N, int path, cudaStream_t stream);
