@@ -209,3 +209,82 @@ def moe_layer(layer: dict, sel=None, weights=None, want_parts: bool = False):
     if want_parts:
         return y, parts
     return y
+
+
+# ---------------------------------------------------------------- encoders (bf16 -> NVFP4 / Q8_0)
+# Re-encoding bf16 weights at load ("robertbfuentes7-cloud/bw24" README,
+# safetensors loader bullet: large tensors re-encode to Q8_0 / NVFP4 at
+# load). Every decision is taken on fp32 values computed with IEEE fp32
+# operations (round to nearest even), as the GPU encoder takes them; the
+# conversions to E4M3, E2M1 and fp16 round to nearest, ties to even, and
+# saturate (E4M3 at 448, E2M1 at 6).
+
+def _rn_grid(v, grid):
+    """Index of the nearest grid value to |v| (grid ascending, nonnegative),
+    ties to the even index; |v| above the grid's top saturates to it."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    g = np.asarray(grid, dtype=np.float64)
+    d = np.abs(a[..., None] - g)
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    idx = np.argmax(cand, axis=-1)  # the lowest index at the minimum distance
+    two = cand.sum(axis=-1) > 1  # a tie (two grid values at the same distance)
+    idx = np.where(two & (idx % 2 == 1), idx + 1, idx)
+    return np.where(a >= g[-1], len(g) - 1, idx)
+
+
+def e4m3_positive_grid():
+    """The 127 nonnegative finite E4M3 values, code order (code = index)."""
+    return np.array([e4m3(c) for c in range(0x7F)])
+
+
+def e2m1_positive_grid():
+    return np.array([e2m1(c) for c in range(8)])
+
+
+def e4m3_encode(v):
+    """E4M3 codes of nonnegative fp32 values (RN-even, saturating at 448)."""
+    return _rn_grid(v, e4m3_positive_grid()).astype(np.uint8)
+
+
+def e2m1_encode(v):
+    """E2M1 codes of fp32 values (RN-even, saturating at 6; the sign bit
+    follows the value's sign, so a negative value that rounds to zero is -0)."""
+    v = np.asarray(v, dtype=np.float32)
+    mag = _rn_grid(v, e2m1_positive_grid()).astype(np.uint8)
+    return (np.signbit(v).astype(np.uint8) << 3) | mag
+
+
+def nvfp4_encode(w, ts, M, K):
+    """(codes u8 [M][K/2], scales u8 [M][K/16]) of bf16 bits w [M][K]:
+    per 16-element block, s = E4M3(amax / 6 / ts) and element code =
+    E2M1(w / (e4m3(s) * ts)), all in fp32; a zero scale gives zero codes."""
+    x = np.asarray(w, dtype=np.uint16).reshape(M, K // 16, 16)
+    wf = (x.astype(np.uint32) << 16).view(np.float32)
+    ts = np.float32(ts)
+    amax = np.abs(wf).max(axis=-1)
+    s32 = (amax / np.float32(6)) / ts
+    sc = e4m3_encode(s32)
+    sdec = np.array([e4m3(c) for c in range(256)], dtype=np.float64).astype(np.float32)[sc]
+    den = (sdec * ts).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (wf / den[..., None]).astype(np.float32)
+    codes = np.where(sdec[..., None] == 0, np.uint8(0), e2m1_encode(q))
+    codes = codes.reshape(M, K // 2, 2)
+    packed = (codes[..., 0] | (codes[..., 1] << 4)).astype(np.uint8)
+    return packed, sc.astype(np.uint8)
+
+
+def q8_0_encode(w, M, K):
+    """(q i8 [M][K], d fp16 bits [M][K/32]) of bf16 bits w [M][K]: per
+    32-element block d = fp16(amax / 127) and q = rint(w / d) in [-127, 127],
+    all in fp32; a zero d gives q = 0."""
+    x = np.asarray(w, dtype=np.uint16).reshape(M, K // 32, 32)
+    wf = (x.astype(np.uint32) << 16).view(np.float32)
+    amax = np.abs(wf).max(axis=-1)
+    d16 = (amax / np.float32(127)).astype(np.float16)
+    d32 = d16.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint(wf / d32[..., None])
+    q = np.where(d32[..., None] == 0, 0, np.clip(q, -127, 127)).astype(np.int8)
+    return q.reshape(M, K), d16.view(np.uint16).reshape(M, K // 32)
