@@ -28,11 +28,13 @@ from ._binding import (  # noqa: F401
     moe_route_topk,
     moe_workspace_bytes,
     nvfp4_dequant,
+    nvfp4_encode,
     nvfp4_gemv,
     nvfp4_gemv_add,
     nvfp4_gemv_path,
     nvfp4_gemv_silu_mul,
     q8_0_dequant,
+    q8_0_encode,
     q8_0_gemv,
     q8_0_gemv_add,
     q8_0_gemv_path,

@@ -48,6 +48,8 @@ SIGNATURES = {
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "nvfp4_gemv_add": (_i32, [_vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "nvfp4_encode": (_i32, [_vp, _f32, _vp, _vp, _i64, _i64, _vp]),
+    "q8_0_encode": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
     "q8_0_gemv_add": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nvfp4_gemv_silu_mul": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_silu_mul": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
@@ -153,6 +155,15 @@ def nvfp4_gemv_silu_mul(codes, scales, tensor_scale, x, h, I, K, N=1, stream=Non
 def q8_0_gemv_silu_mul(q, d, x, h, I, K, N=1, stream=None):
     _check(lib().q8_0_gemv_silu_mul(_ptr(q), _ptr(d), _ptr(x), _ptr(h), I, K, N, _stream(stream)),
            "q8_0_gemv_silu_mul")
+
+
+def nvfp4_encode(w, tensor_scale, codes, scales, M, K, stream=None):
+    _check(lib().nvfp4_encode(_ptr(w), tensor_scale, _ptr(codes), _ptr(scales), M, K, _stream(stream)),
+           "nvfp4_encode")
+
+
+def q8_0_encode(w, q, d, M, K, stream=None):
+    _check(lib().q8_0_encode(_ptr(w), _ptr(q), _ptr(d), M, K, _stream(stream)), "q8_0_encode")
 
 
 def bqd_device_error() -> int:

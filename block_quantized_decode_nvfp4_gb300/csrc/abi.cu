@@ -165,6 +165,31 @@ bqd_status q8_0_gemv(const int8_t* q, const uint16_t* d, const uint16_t* x, floa
     return q8_0_gemv_path(q, d, x, y, M, K, N, BQD_PATH_AUTO, stream);
 }
 
+// ---------------------------------------------------------------- encoders
+bqd_status nvfp4_encode(const uint16_t* w, float tensor_scale, uint8_t* codes, uint8_t* scales, int64_t M, int64_t K,
+                        cudaStream_t stream)
+{
+    if (M < 0 || K < 0 || K % 16 != 0 || (M > 0 && K > 0 && M > (int64_t(1) << 62) / K)) return BQD_ERR_SHAPE;
+    if (!(tensor_scale >= 0x1p-100f && tensor_scale <= 0x1p100f)) return BQD_ERR_SHAPE;  // also rejects NaN
+    if (M == 0 || K == 0) return BQD_OK;
+    if (!w || !codes || !scales) return BQD_ERR_NULL;
+    if (!aligned16(w) || !aligned16(codes)) return BQD_ERR_ALIGN;
+    const bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_nvfp4_encode(w, tensor_scale, codes, scales, M, K, stream));
+}
+
+bqd_status q8_0_encode(const uint16_t* w, int8_t* q, uint16_t* d, int64_t M, int64_t K, cudaStream_t stream)
+{
+    if (M < 0 || K < 0 || K % 32 != 0 || (M > 0 && K > 0 && M > (int64_t(1) << 62) / K)) return BQD_ERR_SHAPE;
+    if (M == 0 || K == 0) return BQD_OK;
+    if (!w || !q || !d) return BQD_ERR_NULL;
+    if (!aligned16(w) || !aligned16(q) || (reinterpret_cast<uintptr_t>(d) & 1u) != 0) return BQD_ERR_ALIGN;
+    const bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_q8_0_encode(w, q, d, M, K, stream));
+}
+
 // ---------------------------------------------------------------- decode-path epilogues
 namespace {
 

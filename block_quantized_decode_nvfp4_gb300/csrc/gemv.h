@@ -48,6 +48,11 @@ bool tiles_gemv_supported(int64_t M, int64_t K, int N);
 cudaError_t launch_nvfp4_gemv_tiles(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,
                                     float* y, int64_t M, int64_t K, int N, cudaStream_t s);
 
+// bf16 -> NVFP4 / Q8_0 encoders (encode.cu).
+cudaError_t launch_nvfp4_encode(const uint16_t* w, float ts, uint8_t* codes, uint8_t* scales, int64_t M, int64_t K,
+                                cudaStream_t s);
+cudaError_t launch_q8_0_encode(const uint16_t* w, int8_t* q, uint16_t* d, int64_t M, int64_t K, cudaStream_t s);
+
 // Bulk-copy streaming GEMV (gemv_stream.cu): N == 1, K % 256 == 0.
 bool stream_gemv_supported(int64_t M, int64_t K, int N);
 cudaError_t launch_nvfp4_gemv_stream(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x,

@@ -196,6 +196,34 @@ bqd_status nvfp4_gemv_silu_mul(const uint8_t* codes, const uint8_t* scales, floa
 bqd_status q8_0_gemv_silu_mul(const int8_t* q, const uint16_t* d, const uint16_t* x, float* h, int64_t I, int64_t K,
                               int N, cudaStream_t stream);
 
+/*
+ * nvfp4_encode -- NVFP4 codes and block scales of a bf16 weight, on the GPU
+ * (re-encoding large tensors at load: "robertbfuentes7-cloud/bw24" README,
+ * safetensors loader bullet). Per 16-element block b of a row:
+ *   s_b = E4M3(amax_b / 6 / ts),  code_k = E2M1(w_k / (e4m3(s_b) * ts)),
+ * every value an IEEE fp32 operation rounded to nearest even, E4M3 and E2M1
+ * rounded to nearest even and saturated (448, 6); a zero s_b gives zero
+ * codes; a negative w that rounds to zero is -0 (code 8). The integer
+ * outputs are a function of the input bits alone (deterministic).
+ *   w bf16 bits [M][K]; tensor_scale ts in [2^-100, 2^100] (the caller's
+ *   choice, e.g. amax(W) / (6 * 448)); codes u8 [M][K/2] (low nibble = even
+ *   k); scales u8 [M][K/16]. K % 16 == 0; w and codes 16-byte aligned.
+ *   NaN weights are outside the contract.
+ */
+bqd_status nvfp4_encode(const uint16_t* w, float tensor_scale, uint8_t* codes, uint8_t* scales, int64_t M, int64_t K,
+                        cudaStream_t stream);
+
+/*
+ * q8_0_encode -- Q8_0 of a bf16 weight, per 32-element block:
+ *   d_b = fp16(amax_b / 127),  q_k = rint(w_k / d_b) clamped to [-127, 127],
+ * fp32 operations and conversions rounded to nearest even; d_b = 0 gives
+ * q = 0. w bf16 bits [M][K]; q int8 [M][K]; d fp16 bits [M][K/32] (planar,
+ * as q8_0_gemv takes them). K % 32 == 0; w and q 16-byte aligned, d 2-byte
+ * aligned. Blocks with amax above 65504 * 127, and NaN weights, are outside
+ * the contract.
+ */
+bqd_status q8_0_encode(const uint16_t* w, int8_t* q, uint16_t* d, int64_t M, int64_t K, cudaStream_t stream);
+
 /* q8_0_gemv with an explicit compute path (BQD_PATH_*). */
 bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K,
                           int N, int path, cudaStream_t stream);
