@@ -99,12 +99,15 @@ def rows_spec():
 def extra_rows_spec():
     """Rows reported beside the step but not part of it: the tiny 256 x 512
     NVFP4 workload (ts = 1.0), whose time is launch latency, not bandwidth;
-    and the decode-path epilogue fusions on the layer shapes (gate_up with
+    the decode-path epilogue fusions on the layer shapes (gate_up with
     SiLU * up on the 12288 x 4096 gate/up weight, I = 6144; down with the
-    residual add on 4096 x 12288)."""
+    residual add on 4096 x 12288); and the bf16 -> NVFP4 / Q8_0 encoders on
+    a 12288 x 4096 weight (bytes: bf16 read, codes and scales written)."""
     return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1)),
             ("nvfp4 gate_up+SiLU 12288x4096 N=1", "nvfp4_silu", dict(M=12288, K=4096, N=1)),
-            ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1))]
+            ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1)),
+            ("nvfp4 encode 12288x4096", "nvfp4_encode", dict(M=12288, K=4096, N=1)),
+            ("q8_0 encode 12288x4096", "q8_0_encode", dict(M=12288, K=4096, N=1))]
 
 
 def host_inputs(kind, p, seed=0):
@@ -112,6 +115,8 @@ def host_inputs(kind, p, seed=0):
         return syn.tiny_nvfp4(seed=seed)
     if kind in ("nvfp4", "nvfp4_silu"):
         return syn.dense_nvfp4(p["M"], p["K"], N=p["N"], seed=seed)
+    if kind in ("nvfp4_encode", "q8_0_encode"):
+        return {"x": syn.bf16_normal((p["M"], p["K"]), np.random.default_rng(seed + 7))}
     if kind == "nvfp4_add":
         h = syn.dense_nvfp4(p["M"], p["K"], N=p["N"], seed=seed)
         h["r"] = np.random.default_rng(seed + 1).standard_normal((p["N"], p["M"])).astype(np.float32)
@@ -128,6 +133,10 @@ def row_bytes(kind, p, host):
         return nvfp4_bytes(p["M"], p["K"], p["N"]) - 4 * p["N"] * p["M"] // 2
     if kind == "nvfp4_add":  # the residual is read
         return nvfp4_bytes(p["M"], p["K"], p["N"]) + 4 * p["N"] * p["M"]
+    if kind == "nvfp4_encode":
+        return p["M"] * p["K"] * 2 + p["M"] * p["K"] // 2 + p["M"] * p["K"] // 16
+    if kind == "q8_0_encode":
+        return p["M"] * p["K"] * 2 + p["M"] * p["K"] + p["M"] * p["K"] // 16
     if kind == "q8_0":
         return q8_0_bytes(p["M"], p["K"], p["N"])
     return moe_bytes(p["T"], p["E"], p["H"], p["I"], p["topk"], host["logits"])
@@ -258,7 +267,20 @@ class Row:
         self.torch, self.bqd = torch, bqd
         d = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
         self.launches = 1
-        if kind in ("nvfp4", "q8_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add"):
+        if kind in ("nvfp4_encode", "q8_0_encode"):
+            M, K = p["M"], p["K"]
+            self.w = (d(host["x"]),)  # the bf16 weight being encoded
+            self.x_host, self.x = host["x"][:1], self.w[0]
+            self.ts = float(self.w[0].view(torch.bfloat16).float().abs().max().item() / (6 * 448))
+            if kind == "nvfp4_encode":
+                self.out = (torch.empty(M * K // 2, dtype=torch.uint8, device="cuda"),
+                            torch.empty(M * K // 16, dtype=torch.uint8, device="cuda"))
+            else:
+                self.out = (torch.empty(M * K, dtype=torch.int8, device="cuda"),
+                            torch.empty(M * K // 32, dtype=torch.int16, device="cuda"))
+            self.y = self.out[0]
+            self.in_bytes = M * K * 2
+        elif kind in ("nvfp4", "q8_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add"):
             M, K, N = p["M"], p["K"], p["N"]
             if kind != "q8_0":
                 self.w = (d(host["codes"]), d(host["scales"]))
@@ -282,7 +304,7 @@ class Row:
             self.y = torch.empty(T * H, dtype=torch.float32, device="cuda")
             self.launches = moe_launches(T, E, H, I, k)
             self.in_bytes = self.x.numel() * 2 + self.logits.numel() * 4
-        self.out_bytes = self.y.numel() * 4
+        self.out_bytes = self.y.numel() * self.y.element_size()
         self.weight_bytes = sum(t.numel() * t.element_size() for t in self.w)
         self.copies = [self.w]
 
@@ -307,6 +329,10 @@ class Row:
             b.nvfp4_gemv_silu_mul(w[0], w[1], self.ts, self.x, self.y, p["M"] // 2, p["K"], p["N"])
         elif self.kind == "nvfp4_add":
             b.nvfp4_gemv_add(w[0], w[1], self.ts, self.x, self.r, self.y, p["M"], p["K"], p["N"])
+        elif self.kind == "nvfp4_encode":
+            b.nvfp4_encode(w[0], self.ts, self.out[0], self.out[1], p["M"], p["K"])
+        elif self.kind == "q8_0_encode":
+            b.q8_0_encode(w[0], self.out[0], self.out[1], p["M"], p["K"])
         elif self.kind == "q8_0":
             b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         else:
