@@ -818,38 +818,54 @@ __global__ void __launch_bounds__(kThG, 1)
 // ------------------------------------------------------------------ down + combine
 // Output (t, j) is the dot product of h'_t = [h'_{t,0} .. h'_{t,topk-1}] (the
 // token's slots side by side, K' = topk * I elements) with row j of each of
-// its experts, gathered. Lane l takes the chunks l + 32 i (i < CPLD) of that
-// gathered row: slot s = (l + 32 i) / CS (CS = I / 32 chunks per slot),
-// chunk (l + 32 i) % CS = l % CS of the slot's expert row (CS divides 32).
+// its experts, gathered. A warp computes R adjacent outputs (t, j) ..
+// (t, j + R - 1) together (R = 2 when there are enough row pairs to keep
+// every warp busy), so every h' value it reads from shared memory serves R
+// rows. Lane l takes the chunks l + 32 i (i < CPLD) of the gathered rows:
+// slot s = (l + 32 i) / CS (CS = I / 32 chunks per slot), chunk
+// (l + 32 i) % CS = l % CS of the slot's expert rows (CS divides 32).
 constexpr int kThD = 768;  // down kernel threads (24 warps), one CTA per SM
 constexpr int kWpD = kThD / kWarp;
 constexpr int kDDepth = 2;  // 32-element chunks in flight per lane
 
+template <int R>
+struct ItemRows {  // the same chunk of R adjacent rows
+    Item r[R];
+};
+
 // hc: the chunk's staged h' (32 fp32; 16-byte piece p at ho[p] floats from
-// hc: the lane's swizzle). One fp32 pair accumulator per scale block.
-__device__ __forceinline__ float dn_dot(const Item& it, const float* hc, const int (&ho)[8])
+// hc: the lane's swizzle), read once for all R rows. One fp32 pair
+// accumulator per row and scale block.
+template <int R>
+__device__ __forceinline__ void dn_dot(const ItemRows<R>& it, const float* hc, const int (&ho)[8], float (&acc)[R])
 {
-    const float2 sc = e4m3x2_to_float2(it.s);
-    const uint32_t w[4] = {it.c.x, it.c.y, it.c.z, it.c.w};
-    float acc = 0.f;
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
-        float2 a = make_float2(0.f, 0.f);
+        float2 a[R];
+#pragma unroll
+        for (int k = 0; k < R; ++k) a[k] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
             const int wi = 2 * b + jj;  // elements 8 wi .. 8 wi + 7 = h' pieces 2 wi, 2 wi + 1
-            uint32_t hw[4];
-            e2m1x8_to_f16x2(w[wi], hw);
             const float4 h0 = *reinterpret_cast<const float4*>(hc + ho[2 * wi]);
             const float4 h1 = *reinterpret_cast<const float4*>(hc + ho[2 * wi + 1]);
-            a = __ffma2_rn(f16x2_to_float2(hw[0]), make_float2(h0.x, h0.y), a);
-            a = __ffma2_rn(f16x2_to_float2(hw[1]), make_float2(h0.z, h0.w), a);
-            a = __ffma2_rn(f16x2_to_float2(hw[2]), make_float2(h1.x, h1.y), a);
-            a = __ffma2_rn(f16x2_to_float2(hw[3]), make_float2(h1.z, h1.w), a);
+            const float2 xp[4] = {make_float2(h0.x, h0.y), make_float2(h0.z, h0.w), make_float2(h1.x, h1.y),
+                                  make_float2(h1.z, h1.w)};
+#pragma unroll
+            for (int k = 0; k < R; ++k) {
+                const uint32_t w[4] = {it.r[k].c.x, it.r[k].c.y, it.r[k].c.z, it.r[k].c.w};
+                uint32_t hw[4];
+                e2m1x8_to_f16x2(w[wi], hw);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) a[k] = __ffma2_rn(f16x2_to_float2(hw[q]), xp[q], a[k]);
+            }
         }
-        acc = fmaf(b ? sc.y : sc.x, a.x + a.y, acc);
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            const float2 sc = e4m3x2_to_float2(it.r[k].s);
+            acc[k] = fmaf(b ? sc.y : sc.x, a[k].x + a[k].y, acc[k]);
+        }
     }
-    return acc;
 }
 
 // Dynamic shared memory: h' of the tokens whose rows the CTA computes, topk
@@ -857,7 +873,7 @@ __device__ __forceinline__ float dn_dot(const Item& it, const float* hc, const i
 // piece p at slot p ^ (c & 7)). The pair list (the workspace count, one
 // entry per (token, slot)) and h' (the workspace partial area, (token,
 // slot) order) come from the gate_up kernel: nothing is routed here.
-template <int CPLD, int CS>
+template <int CPLD, int CS, int R>
 __global__ void __launch_bounds__(kThD, 1)
     moe_small_dn_kernel(const uint8_t* __restrict__ dn_codes, const uint8_t* __restrict__ dn_scales,
                         float* __restrict__ y, MoeWorkspace ws, int H, int T, int topk)
@@ -880,15 +896,17 @@ __global__ void __launch_bounds__(kThD, 1)
     __syncthreads();
     const bool ok = s_ok != 0;
 
-    // rows (t, j), t = r / H: an even split over the CTAs, then over the warps;
-    // the CTA stages h' only for the tokens its rows belong to
-    const int nr = ok ? T * H : 0;
+    // units u = rows R u .. R u + R - 1 (all of token t = R u / H, as R divides
+    // H): an even split over the CTAs, then over the warps; the CTA stages h'
+    // only for the tokens its rows belong to
+    const int nr = ok ? T * H / R : 0;
     const int c_lo = static_cast<int>(static_cast<int64_t>(nr) * blockIdx.x / gridDim.x);
     const int c_hi = static_cast<int>(static_cast<int64_t>(nr) * (blockIdx.x + 1) / gridDim.x);
-    const int t_first = c_lo / H, t_end = c_hi > c_lo ? (c_hi - 1) / H + 1 : t_first;  // tokens [t_first, t_end)
+    const int hsh = __ffs(H) - 1;  // H is a power of two
+    const int t_first = (R * c_lo) >> hsh;
+    const int t_end = c_hi > c_lo ? ((R * (c_hi - 1)) >> hsh) + 1 : t_first;  // tokens [t_first, t_end)
     const int r_lo = c_lo + static_cast<int>(static_cast<int64_t>(c_hi - c_lo) * warp / kWpD);
     const int r_hi = c_lo + static_cast<int>(static_cast<int64_t>(c_hi - c_lo) * (warp + 1) / kWpD);
-    const int hsh = __ffs(H) - 1;  // H is a power of two
     // the gathered row's expert rows for this lane's chunks, per token
     int eh[CPLD];
     int cur_t = -1;
@@ -903,21 +921,25 @@ __global__ void __launch_bounds__(kThD, 1)
     // (expert * H + j) * cp < 2^32 for every supported shape (E <= 512, H <= 8192, I <= 1024)
     const uint8_t* cbase = dn_codes + (lane % CS) * 16;
     const uint8_t* sbase = dn_scales + (lane % CS) * 2;
-    auto load_at = [&](int r, int i) -> Item {
-        Item it;
-        it.c = make_uint4(0u, 0u, 0u, 0u);
-        it.s = 0u;
-        const int t = r >> hsh, j = r & (H - 1);
+    auto load_at = [&](int u, int i) -> ItemRows<R> {
+        ItemRows<R> it;
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+            it.r[k].c = make_uint4(0u, 0u, 0u, 0u);
+            it.r[k].s = 0u;
+        }
+        const int r = R * u, t = r >> hsh, j = r & (H - 1);
         if (t != cur_t) set_token(t);
         if (eh[i] >= 0) {
             const uint32_t row = static_cast<uint32_t>(eh[i] + j);
-            it = load_item(cbase + row * cp, sbase + row * sp);
+#pragma unroll
+            for (int k = 0; k < R; ++k) it.r[k] = load_item(cbase + (row + k) * cp, sbase + (row + k) * sp);
         }
         return it;
     };
     static_assert(CPLD % kDDepth == 0 || kDDepth % CPLD == 0, "ring depth must divide a row or be a multiple of one");
     constexpr int U = kDDepth > CPLD ? kDDepth / CPLD : 1;
-    Item buf[kDDepth];
+    ItemRows<R> buf[kDDepth];
 #pragma unroll
     for (int d = 0; d < kDDepth; ++d)
         if (r_lo + d / CPLD < r_hi) buf[d] = load_at(r_lo + d / CPLD, d % CPLD);
@@ -942,23 +964,28 @@ __global__ void __launch_bounds__(kThD, 1)
     for (int r0 = r_lo; r0 < r_hi; r0 += U) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int r = r0 + u;
+            const int r = r0 + u;  // unit: rows R r .. R r + R - 1 = t * H + j ..
             if (r < r_hi) {
-                const int t = r >> hsh;
+                const int t = (R * r) >> hsh;
                 const float* hrow = hs + (t - t_first) * KC * 32;
-                float acc = 0.f;
+                float acc[R];
+#pragma unroll
+                for (int k = 0; k < R; ++k) acc[k] = 0.f;
 #pragma unroll
                 for (int i = 0; i < CPLD; ++i) {
                     const int g = u * CPLD + i;
-                    const Item it = buf[g % kDDepth];
+                    const ItemRows<R> it = buf[g % kDDepth];
                     const int rn = r0 + (g + kDDepth) / CPLD;
                     if (rn < r_hi) buf[g % kDDepth] = load_at(rn, (g + kDDepth) % CPLD);
                     const int c = lane + 32 * i;
-                    if (c < KC) acc += dn_dot(it, hrow + c * 32, ho);
+                    if (c < KC) dn_dot<R>(it, hrow + c * 32, ho, acc);
                     asm volatile("" ::: "memory");
                 }
-                const float v = warp_sum(acc);
-                if (lane == 0) y[r] = v;  // r = t * H + j
+#pragma unroll
+                for (int k = 0; k < R; ++k) {
+                    const float v = warp_sum(acc[k]);
+                    if (lane == 0) y[R * r + k] = v;
+                }
             }
         }
     }
@@ -983,11 +1010,11 @@ cudaError_t launch_gu(cudaLaunchConfig_t& cfg, int dev, const float* logits, con
                               gu_ts, x, dn_ts, ws, E, I, T, topk);
 }
 
-template <int CPLD, int CS>
-cudaError_t launch_dn(cudaLaunchConfig_t& cfg, int dev, const uint8_t* dn_codes, const uint8_t* dn_scales, float* y,
-                      const MoeWorkspace& ws, int H, int T, int topk)
+template <int CPLD, int CS, int R>
+cudaError_t launch_dn_r(cudaLaunchConfig_t& cfg, int dev, const uint8_t* dn_codes, const uint8_t* dn_scales,
+                        float* y, const MoeWorkspace& ws, int H, int T, int topk)
 {
-    auto kern = moe_small_dn_kernel<CPLD, CS>;
+    auto kern = moe_small_dn_kernel<CPLD, CS, R>;
     static OccCache occ;
     // a CTA's rows span at most rows_per_cta / H + 2 tokens
     const int64_t rows_per_cta = (static_cast<int64_t>(T) * H + cfg.gridDim.x - 1) / cfg.gridDim.x;
@@ -997,6 +1024,19 @@ cudaError_t launch_dn(cudaLaunchConfig_t& cfg, int dev, const uint8_t* dn_codes,
     cfg.blockDim = dim3(kThD);
     blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, kThD, cfg.dynamicSmemBytes);
     return cudaLaunchKernelEx(&cfg, kern, dn_codes, dn_scales, y, ws, H, T, topk);
+}
+
+// Two rows per warp unit halve the shared-memory reads of h' once there are
+// at least as many row pairs as warps (T = 16 with H = 2048: 53.2 against
+// 54.8 us a layer back to back); below that, single rows keep more warps
+// streaming (T = 1: 15.2 against 16.7 us).
+template <int CPLD, int CS>
+cudaError_t launch_dn(cudaLaunchConfig_t& cfg, int dev, const uint8_t* dn_codes, const uint8_t* dn_scales, float* y,
+                      const MoeWorkspace& ws, int H, int T, int topk)
+{
+    if (CPLD <= 4 && static_cast<int64_t>(T) * H / 2 >= static_cast<int64_t>(cfg.gridDim.x) * kWpD)
+        return launch_dn_r<CPLD, CS, (CPLD <= 4 ? 2 : 1)>(cfg, dev, dn_codes, dn_scales, y, ws, H, T, topk);
+    return launch_dn_r<CPLD, CS, 1>(cfg, dev, dn_codes, dn_scales, y, ws, H, T, topk);
 }
 
 }  // namespace
