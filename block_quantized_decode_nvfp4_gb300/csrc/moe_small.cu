@@ -669,6 +669,7 @@ __global__ void __launch_bounds__(kThG, 1)
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ PairList L;
     __shared__ int s_emax[kMaxT], s_emin[kMaxT], s_sexp[kMaxT], s_flags;
+    __shared__ int s_need[kMaxT], s_nneed;  // the tokens whose activations this CTA stages
     __shared__ uint32_t s_mask[kMaxE];
     __shared__ int s_eoff[kMaxE], s_scan[kWpG + 1];
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
@@ -709,14 +710,20 @@ __global__ void __launch_bounds__(kThG, 1)
     // [2^14, 2^15). Otherwise (or with a subnormal, infinite or NaN element)
     // the raw bf16 values are staged and the kernel computes in fp32 (rows)
     // or with bf16 operands (tiles).
+    // Only the tokens in s_need[0 .. s_nneed) are staged (piece pc of the
+    // compact order is piece pc % (H / 8) of token s_need[pc / (H / 8)]).
     auto stage_x = [&]() -> bool {
         cp_async_wait_all();
         __syncthreads();
+        const int nps = s_nneed * (H / 8);
         uint4 xv[kXP];  // piece threadIdx.x + r kThG (consecutive per warp: no bank conflicts)
 #pragma unroll
         for (int r = 0; r < kXP; ++r) {
             const int pc = threadIdx.x + r * kThG;
-            if (pc < npc) xv[r] = *reinterpret_cast<const uint4*>(xraw + pc * 8);
+            if (pc < nps) {
+                const int t = s_need[pc / (H / 8)], v = pc % (H / 8);
+                xv[r] = *reinterpret_cast<const uint4*>(xraw + (t * (H / 8) + v) * 8);
+            }
         }
         // |x| bit patterns (sign cleared) order like the values: the largest
         // and the smallest nonzero pattern per token give its exponent range
@@ -725,7 +732,7 @@ __global__ void __launch_bounds__(kThG, 1)
         // pieces lie in one token
 #pragma unroll
         for (int r = 0; r < kXP; ++r) {
-            if (r * kThG + warp * kWarp < npc) {  // warp-uniform
+            if (r * kThG + warp * kWarp < nps) {  // warp-uniform
                 const uint32_t w4[4] = {xv[r].x, xv[r].y, xv[r].z, xv[r].w};
                 uint32_t hmax = 0u, hmin = 0xFFFFFFFFu;
 #pragma unroll
@@ -737,7 +744,7 @@ __global__ void __launch_bounds__(kThG, 1)
                 const uint32_t bmax = __reduce_max_sync(0xFFFFFFFFu, max(hmax & 0xFFFFu, hmax >> 16));
                 const uint32_t bmin = __reduce_min_sync(0xFFFFFFFFu, min(hmin & 0xFFFFu, hmin >> 16)) + 1u;
                 if (lane == 0) {
-                    const int t = (r * kThG + warp * kWarp) / (H / 8);
+                    const int t = s_need[(r * kThG + warp * kWarp) / (H / 8)];
                     atomicMax(&s_emax[t], static_cast<int>(bmax));
                     atomicMin(&s_emin[t], static_cast<int>(bmin));  // 0x10000: no nonzero element
                 }
@@ -762,8 +769,8 @@ __global__ void __launch_bounds__(kThG, 1)
 #pragma unroll
         for (int r = 0; r < kXP; ++r) {
             const int pc = threadIdx.x + r * kThG;
-            if (pc >= npc) continue;
-            const int t = pc / (H / 8), v = pc - t * (H / 8);
+            if (pc >= nps) continue;
+            const int t = s_need[pc / (H / 8)], v = pc % (H / 8);
             uint4 uu = xv[r];
             if (fast) {
                 // x * 2^-s as two exact multiplies by normal powers of two
@@ -792,6 +799,27 @@ __global__ void __launch_bounds__(kThG, 1)
         const int ntile = L.n_act << tsh;
         const int t_lo = static_cast<int>(ntile * gw / nw), t_hi = static_cast<int>(ntile * (gw + 1) / nw);
         TileIo<CPL> io{gu_codes, gu_scales, &L, I, tsh, lane >> 2, lane & 3};
+        // the tokens of the CTA's tiles' groups (a group's tiles share its tokens)
+        const int64_t gw0 = static_cast<int64_t>(blockIdx.x) * kWpG;
+        const int c_lo = static_cast<int>(ntile * gw0 / nw), c_hi = static_cast<int>(ntile * (gw0 + kWpG) / nw);
+        if (threadIdx.x == 0) s_nneed = 0;
+        if (threadIdx.x < kMaxT) s_need[threadIdx.x] = 0;
+        __syncthreads();
+        if (c_lo < c_hi) {
+            const int a_lo = c_lo >> tsh, a_hi = (c_hi - 1) >> tsh;
+            for (int k = threadIdx.x; k < (a_hi - a_lo + 1) * NT; k += kThG) {
+                const int a = a_lo + k / NT, p = L.act_p0[a] + k % NT;
+                if (p < L.act_p0[a + 1] && L.pt[p] >= 0) s_need[L.pt[p]] = 1;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < kWarp) {  // compact, ascending
+            const bool nd = threadIdx.x < T && s_need[threadIdx.x] != 0;
+            const uint32_t m = __ballot_sync(0xFFFFFFFFu, nd);
+            __syncwarp();
+            if (nd) s_need[__popc(m & ((1u << threadIdx.x) - 1u))] = threadIdx.x;
+            if (threadIdx.x == 0) s_nneed = __popc(m);
+        }
         MSlot ring[kMDepth];
         if (t_lo < t_hi) {
             const TilePtr first = io.ptrs(t_lo);
@@ -806,6 +834,8 @@ __global__ void __launch_bounds__(kThG, 1)
         // this warp's rows: an even split of all groups' gate/up row pairs
         const int nv2 = L.n_act * I;
         const int v_lo = 2 * static_cast<int>(nv2 * gw / nw), v_hi = 2 * static_cast<int>(nv2 * (gw + 1) / nw);
+        if (threadIdx.x < T) s_need[threadIdx.x] = threadIdx.x;
+        if (threadIdx.x == 0) s_nneed = T;
         Item buf[kGDepth];
         gu_rows_prologue<CPL>(buf, gu_codes, gu_scales, L, I, v_lo, v_hi, lane);
         if (stage_x())
