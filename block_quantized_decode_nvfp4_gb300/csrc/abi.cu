@@ -247,11 +247,12 @@ bqd_status bqd_device_error(unsigned int* bits_out)
     if (!bits_out) return BQD_ERR_NULL;
     bqd_status st = check_arch();
     if (st != BQD_OK) return st;
-    unsigned int v = 0, w = 0, m = 0;
+    unsigned int v = 0, w = 0, m = 0, n = 0;
     if (bqd::read_and_clear_stream_error(&v) != cudaSuccess || bqd::read_and_clear_mma_error(&w) != cudaSuccess ||
-        bqd::read_and_clear_moe_stream_error(&m) != cudaSuccess)
+        bqd::read_and_clear_moe_stream_error(&m) != cudaSuccess ||
+        bqd::read_and_clear_moe_small_error(&n) != cudaSuccess)
         return BQD_ERR_LAUNCH;
-    v |= w | m;
+    v |= w | m | n;
     *bits_out = v;
     return v ? BQD_ERR_DEVICE : BQD_OK;
 }

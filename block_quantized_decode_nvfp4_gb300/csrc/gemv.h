@@ -98,6 +98,7 @@ cudaError_t launch_moe_stream_layer(const uint8_t* gu_codes, const uint8_t* gu_s
                                     const float* pair_weight, const int32_t* pair_slot, const MoeWorkspace& ws, int E,
                                     int H, int I, int T, int topk, cudaStream_t stream);
 cudaError_t read_and_clear_moe_stream_error(unsigned int* out);
+cudaError_t read_and_clear_moe_small_error(unsigned int* out);
 
 // Small-batch MoE kernels (moe_small.cu): the limits of moe_small_supported
 // (T <= 16, T * topk <= 128, E <= 512, H in {1024, ..., 8192}, I in {256,

@@ -42,8 +42,14 @@
 #include "gemv.h"
 #include "host_util.h"
 #include "moe_route.cuh"
+#include "stream.cuh"
 
 namespace bqd {
+
+// Device error word of the small-batch MoE kernels (kErrWaitTimeout: the
+// activations' copy did not land in time); read and cleared by
+// read_and_clear_moe_small_error().
+__device__ unsigned int g_moe_small_error = 0;
 
 namespace {
 
@@ -64,13 +70,6 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // 2^e for a normal exponent e (-126 .. 127).
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
-// 16-byte asynchronous copy global -> shared (both 16-byte aligned).
-__device__ __forceinline__ void cp_async16(void* dst, const void* src)
-{
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Two fp32 accumulators += (lo, hi) f16 halves of w2 times those of x2
 // (exact products, one fp32 rounding each).
@@ -675,18 +674,27 @@ __global__ void __launch_bounds__(kThG, 1)
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem);  // staged activations
     uint16_t* xraw = xs + T * H;                          // x as given
+    __shared__ uint64_t s_xbar;                           // x's bulk copy landed
 
-    if (threadIdx.x == 0) s_flags = 0;  // ordered before their use by the barriers of the routing
+    if (threadIdx.x == 0) {  // ordered before their use by the barriers of the routing
+        s_flags = 0;
+        mbar_init(&s_xbar, 1);
+        fence_barrier_init();
+    }
     if (threadIdx.x < kMaxT) {
         s_emax[threadIdx.x] = 0;
         s_emin[threadIdx.x] = INT_MAX;
     }
     pdl_wait();  // logits, the list and x may come from the previous kernel
-    // x, copied to shared memory asynchronously (its latency overlaps the
-    // routing), then staged in one pass through registers
+    // x, copied to shared memory by one bulk copy (its latency overlaps the
+    // routing; an mbarrier tracks it, so waiting for it never waits for the
+    // weight loads in flight), then staged in one pass through registers
     constexpr int kXP = kMaxTH / 8 / kThG;  // 16-byte pieces per thread
-    const int npc = T * (H / 8);
-    for (int pc = threadIdx.x; pc < npc; pc += kThG) cp_async16(xraw + pc * 8, x + pc * 8);
+    if (threadIdx.x == 0) {
+        const uint32_t xb = static_cast<uint32_t>(T) * H * 2;
+        mbar_arrive_expect_tx(&s_xbar, xb);
+        bulk_g2s(xraw, x, xb, &s_xbar);
+    }
     if (logits)
         route_in_cta(logits, T, E, topk, NT, L, s_mask, s_eoff, s_scan);
     else
@@ -713,7 +721,7 @@ __global__ void __launch_bounds__(kThG, 1)
     // Only the tokens in s_need[0 .. s_nneed) are staged (piece pc of the
     // compact order is piece pc % (H / 8) of token s_need[pc / (H / 8)]).
     auto stage_x = [&]() -> bool {
-        cp_async_wait_all();
+        mbar_wait(&s_xbar, 0, &g_moe_small_error);  // bounded; on time-out the outputs are unspecified
         __syncthreads();
         const int nps = s_nneed * (H / 8);
         uint4 xv[kXP];  // piece threadIdx.x + r kThG (consecutive per warp: no bank conflicts)
@@ -1136,6 +1144,19 @@ cudaError_t launch_moe_small_layer(const float* logits, const uint8_t* gu_codes,
         default: return BQD_DN(8);
     }
 #undef BQD_DN
+}
+
+cudaError_t read_and_clear_moe_small_error(unsigned int* out)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_moe_small_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    *out = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_moe_small_error, &zero, sizeof(zero));
+    }
+    return e;
 }
 
 }  // namespace bqd

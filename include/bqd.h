@@ -230,9 +230,10 @@ bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x,
 
 /*
  * bqd_device_error -- waits for the device, copies the device error words of
- * the streaming and tensor-core GEMV kernels (BQD_PATH_STREAM, BQD_PATH_MMA)
- * and of the MoE stream kernels to *bits_out (OR of the three) and clears
- * them. Bit 0: a pipeline wait ran out
+ * the streaming and tensor-core GEMV kernels (BQD_PATH_STREAM, BQD_PATH_MMA),
+ * of the MoE stream kernels and of the small-batch MoE kernels (the
+ * activations' copy in moe_layer / moe_grouped_gemv at T <= 16) to
+ * *bits_out (OR of the four) and clears them. Bit 0: a wait ran out
  * (the kernel gave up instead of hanging; its outputs are unspecified).
  * Returns BQD_ERR_DEVICE if any bit was set. Synchronising: do not call it
  * inside a stream capture.
