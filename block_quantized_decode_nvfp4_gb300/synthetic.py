@@ -32,14 +32,17 @@ __all__ = [
     "streams",
     "nvfp4_weight",
     "q8_0_weight",
+    "q4_0_weight",
     "bf16_normal",
     "router_logits",
     "tiny_nvfp4",
     "dense_nvfp4",
     "dense_q8_0",
+    "dense_q4_0",
     "moe_layer",
     "NVFP4_SHAPES",
     "Q8_0_SHAPES",
+    "Q4_0_SHAPES",
     "VERIFY_SHAPES",
 ]
 
@@ -47,6 +50,8 @@ __all__ = [
 NVFP4_SHAPES = [(12288, 4096), (4096, 12288), (4096, 4096)]
 # (M, K) of the Q8_0 weights (gate/up, down, LM head).
 Q8_0_SHAPES = [(12288, 4096), (4096, 12288), (151936, 4096)]
+# (M, K) of the Q4_0 weights (gate/up, down).
+Q4_0_SHAPES = [(12288, 4096), (4096, 12288)]
 # (M, K) of the speculative-verify weights; N in {4, 8}.
 VERIFY_SHAPES = [(4096, 4096), (12288, 4096)]
 
@@ -85,6 +90,16 @@ def q8_0_weight(M: int, K: int, rng_q, rng_d) -> dict:
     return {"q": q, "d": d, "M": M, "K": K}
 
 
+def q4_0_weight(M: int, K: int, rng_c, rng_d) -> dict:
+    """Q4_0 planes: codes u8[M][K/2] (16 bytes per 32-element block, uniform
+    over all bytes), d fp16 bits u16[M][K/32]."""
+    if K % 32:
+        raise ValueError("Q4_0 needs K % 32 == 0")
+    codes = rng_c.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    d = rng_d.uniform(1e-3, 1e-1, size=(M, K // 32)).astype(np.float16).view(np.uint16)
+    return {"codes": codes, "d": d, "M": M, "K": K}
+
+
 def bf16_normal(shape, rng) -> np.ndarray:
     """bf16 bits of N(0,1) draws (fp32 draw, then round-to-nearest-even)."""
     return _to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
@@ -119,6 +134,14 @@ def dense_q8_0(M: int, K: int, N: int = 1, seed: int = 0) -> dict:
     """Q8_0 weight with N bf16 columns. Streams: 0 q, 1 d, 2 x."""
     rq, rd, rx = streams(seed, 3)
     w = q8_0_weight(M, K, rq, rd)
+    w["x"] = bf16_normal((N, K), rx)
+    return w
+
+
+def dense_q4_0(M: int, K: int, N: int = 1, seed: int = 0) -> dict:
+    """Q4_0 weight with N bf16 columns. Streams: 0 codes, 1 d, 2 x."""
+    rc, rd, rx = streams(seed, 3)
+    w = q4_0_weight(M, K, rc, rd)
     w["x"] = bf16_normal((N, K), rx)
     return w
 

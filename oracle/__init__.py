@@ -37,6 +37,9 @@ def lib():
             ("oracle_nvfp4_gemv", None, [u8p, u8p, C.c_float, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
             ("oracle_nvfp4_gemv_f64x", None, [u8p, u8p, C.c_float, f64p, i64, i64, i64, f64p, f64p]),
             ("oracle_q8_0_gemv", None, [i8p, u16p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
+            ("oracle_q4_0_dequant_f64", None, [u8p, u16p, i64, i64, f64p]),
+            ("oracle_q4_0_dequant_f32", None, [u8p, u16p, i64, i64, f32p]),
+            ("oracle_q4_0_gemv", None, [u8p, u16p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
             ("oracle_moe_route", None, [f32p, i64, i64, i64, i32p, f64p]),
             ("oracle_moe_layer", None, [u8p, u8p, f32p, u8p, u8p, f32p, u16p, i32p, f64p,
                                         i64, i64, i64, i64] + [f64p] * 8),
@@ -97,6 +100,19 @@ def q8_0_dequant(q, d, M, K, dtype=np.float64):
     return w
 
 
+def q4_0_dequant(codes, d, M, K, dtype=np.float64):
+    """Q4_0 weight [M][K]: fp16(d) * (q - 8), q from the GGUF block order
+    (element j < 16 of a 32-block: low nibble of code byte j; j >= 16: high
+    nibble of byte j - 16)."""
+    codes, d = _c(codes, np.uint8), _c(d, np.uint16)
+    w = np.empty((M, K), dtype=dtype)
+    if dtype == np.float64:
+        lib().oracle_q4_0_dequant_f64(_p(codes, C.c_uint8), _p(d, C.c_uint16), M, K, _p(w, C.c_double))
+    else:
+        lib().oracle_q4_0_dequant_f32(_p(codes, C.c_uint8), _p(d, C.c_uint16), M, K, _p(w, C.c_float))
+    return w
+
+
 # ---------------------------------------------------------------- GEMV
 def nvfp4_gemv(codes, scales, ts, x, M, K, rows=None):
     """(y, a) as fp64 arrays [N][len(rows) or M]; x is bf16 bits [N][K]."""
@@ -130,6 +146,19 @@ def q8_0_gemv(q, d, x, M, K, rows=None):
     R = M if r is None else len(r)
     y = np.empty((N, R)); a = np.empty((N, R))
     lib().oracle_q8_0_gemv(_p(q, C.c_int8), _p(d, C.c_uint16), _p(x, C.c_uint16), M, K, N,
+                           _p(r, C.c_int64), 0 if r is None else len(r),
+                           _p(y, C.c_double), _p(a, C.c_double))
+    return y, a
+
+
+def q4_0_gemv(codes, d, x, M, K, rows=None):
+    codes, d = _c(codes, np.uint8), _c(d, np.uint16)
+    x = _c(x, np.uint16).reshape(-1, K)
+    N = x.shape[0]
+    r = None if rows is None else _c(rows, np.int64)
+    R = M if r is None else len(r)
+    y = np.empty((N, R)); a = np.empty((N, R))
+    lib().oracle_q4_0_gemv(_p(codes, C.c_uint8), _p(d, C.c_uint16), _p(x, C.c_uint16), M, K, N,
                            _p(r, C.c_int64), 0 if r is None else len(r),
                            _p(y, C.c_double), _p(a, C.c_double))
     return y, a

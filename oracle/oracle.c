@@ -15,7 +15,9 @@
  *    (block-scaled FP4 matvec); MoE bullet: expert-major batching of routed
  *    tokens with experts decoded once; speculative bullet: K+1 tokens verified
  *    in one batched target forward (N = K+1 columns).
- *  - "avifenesh/memra" README, Decode kernels bullet: NVFP4 / Q8_0 matvecs.
+ *  - "avifenesh/memra" README, Decode kernels bullet: NVFP4 / Q4_0 / Q8_0
+ *    matvecs; "robertbfuentes7-cloud/bw24" README, GGUF bullet: files mix
+ *    BF16, Q8_0, Q4_0, Q4_1 and the K-quants.
  *  The pages never print the bit layouts. The element formats are the public
  *  closed forms: E2M1 and E4M3 from the OCP Microscaling (MX) v1.0 and OCP
  *  8-bit Floating Point v1.0 specifications, binary16 from IEEE 754-2008,
@@ -129,6 +131,22 @@ static double q8_0_elem(const int8_t *q, const uint16_t *d, int64_t K, int64_t m
     return oracle_fp16(d[m * (K / 32) + k / 32]) * (double)q[m * K + k];
 }
 
+/* Q4_0 element (m, k): fp16(d of block k/32) * (q - 8), q the 4-bit code
+ * of element j = k % 32 of the block: the low nibble of the block's code
+ * byte j for j < 16, the high nibble of byte j - 16 otherwise (the order of
+ * a GGUF Q4_0 block, whose two fields are the two planes here). */
+static int q4_0_code(const uint8_t *codes, int64_t K, int64_t m, int64_t k)
+{
+    int64_t j = k % 32;
+    uint8_t byte = codes[m * (K / 2) + (k / 32) * 16 + (j % 16)];
+    return j < 16 ? (byte & 0x0F) : (byte >> 4);
+}
+
+static double q4_0_elem(const uint8_t *codes, const uint16_t *d, int64_t K, int64_t m, int64_t k)
+{
+    return oracle_fp16(d[m * (K / 32) + k / 32]) * (double)(q4_0_code(codes, K, m, k) - 8);
+}
+
 /* ------------------------------------------------------------ dequantisation */
 
 /* w[m][k] = e2m1 * e4m3 * ts as a real number (fp64, exact: at most 30
@@ -163,6 +181,21 @@ void oracle_q8_0_dequant_f32(const int8_t *q, const uint16_t *d, int64_t M, int6
     for (int64_t m = 0; m < M; ++m)
         for (int64_t k = 0; k < K; ++k)
             w[m * K + k] = (float)q8_0_elem(q, d, K, m, k);
+}
+
+/* Q4_0 dequantised weight, fp64 and fp32 (both exact: 11 + 4 bits). */
+void oracle_q4_0_dequant_f64(const uint8_t *codes, const uint16_t *d, int64_t M, int64_t K, double *w)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            w[m * K + k] = q4_0_elem(codes, d, K, m, k);
+}
+
+void oracle_q4_0_dequant_f32(const uint8_t *codes, const uint16_t *d, int64_t M, int64_t K, float *w)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            w[m * K + k] = (float)q4_0_elem(codes, d, K, m, k);
 }
 
 /* ------------------------------------------------------------ GEMV */
@@ -206,6 +239,27 @@ void oracle_q8_0_gemv(const int8_t *q, const uint16_t *d, const uint16_t *x,
             double sum = 0.0, abs_sum = 0.0;
             for (int64_t k = 0; k < K; ++k) {
                 double p = q8_0_elem(q, d, K, m, k) * oracle_bf16(x[n * K + k]);
+                sum += p;
+                abs_sum += fabs(p);
+            }
+            y[n * R + i] = sum;
+            if (a)
+                a[n * R + i] = abs_sum;
+        }
+    }
+}
+
+void oracle_q4_0_gemv(const uint8_t *codes, const uint16_t *d, const uint16_t *x,
+                      int64_t M, int64_t K, int64_t N,
+                      const int64_t *rows, int64_t nrows, double *y, double *a)
+{
+    int64_t R = rows ? nrows : M;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t i = 0; i < R; ++i) {
+            int64_t m = rows ? rows[i] : i;
+            double sum = 0.0, abs_sum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = q4_0_elem(codes, d, K, m, k) * oracle_bf16(x[n * K + k]);
                 sum += p;
                 abs_sum += fabs(p);
             }

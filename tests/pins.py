@@ -48,3 +48,16 @@ def nvfp4_weight_lib(codes, scales, ts) -> np.ndarray:
 
 def q8_0_weight_lib(q, d) -> np.ndarray:
     return q.astype(np.float64) * np.repeat(fp16_lib(d), 32, axis=1)
+
+
+def q4_0_codes_unpacked(codes: np.ndarray) -> np.ndarray:
+    """[M][K/2] bytes -> [M][K] 4-bit codes in the GGUF Q4_0 block order: the
+    16 low nibbles of a block's bytes are its elements 0..15, the 16 high
+    nibbles its elements 16..31."""
+    M = codes.shape[0]
+    b = codes.reshape(M, -1, 16)
+    return np.concatenate([b & 0x0F, b >> 4], axis=-1).reshape(M, -1)
+
+
+def q4_0_weight_lib(codes, d) -> np.ndarray:
+    return (q4_0_codes_unpacked(codes).astype(np.float64) - 8.0) * np.repeat(fp16_lib(d), 32, axis=1)
