@@ -101,11 +101,14 @@ def extra_rows_spec():
     NVFP4 workload (ts = 1.0), whose time is launch latency, not bandwidth;
     the decode-path epilogue fusions on the layer shapes (gate_up with
     SiLU * up on the 12288 x 4096 gate/up weight, I = 6144; down with the
-    residual add on 4096 x 12288); and the bf16 -> NVFP4 / Q8_0 encoders on
-    a 12288 x 4096 weight (bytes: bf16 read, codes and scales written)."""
+    residual add on 4096 x 12288); the Q4_0 GEMV on the two layer shapes;
+    and the bf16 -> NVFP4 / Q8_0 encoders on a 12288 x 4096 weight (bytes:
+    bf16 read, codes and scales written)."""
     return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1)),
             ("nvfp4 gate_up+SiLU 12288x4096 N=1", "nvfp4_silu", dict(M=12288, K=4096, N=1)),
             ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1)),
+            ("q4_0 12288x4096 N=1", "q4_0", dict(M=12288, K=4096, N=1)),
+            ("q4_0 4096x12288 N=1", "q4_0", dict(M=4096, K=12288, N=1)),
             ("nvfp4 encode 12288x4096", "nvfp4_encode", dict(M=12288, K=4096, N=1)),
             ("q8_0 encode 12288x4096", "q8_0_encode", dict(M=12288, K=4096, N=1))]
 
@@ -123,6 +126,8 @@ def host_inputs(kind, p, seed=0):
         return h
     if kind == "q8_0":
         return syn.dense_q8_0(p["M"], p["K"], N=p["N"], seed=seed)
+    if kind == "q4_0":
+        return syn.dense_q4_0(p["M"], p["K"], N=p["N"], seed=seed)
     return syn.moe_layer(T=p["T"], E=p["E"], H=p["H"], I=p["I"], topk=p["topk"], seed=seed)
 
 
@@ -139,6 +144,8 @@ def row_bytes(kind, p, host):
         return p["M"] * p["K"] * 2 + p["M"] * p["K"] + p["M"] * p["K"] // 16
     if kind == "q8_0":
         return q8_0_bytes(p["M"], p["K"], p["N"])
+    if kind == "q4_0":  # 16 code bytes and a 2-byte scale per 32 weights
+        return p["M"] * p["K"] // 2 + p["M"] * (p["K"] // 32) * 2 + 2 * p["N"] * p["K"] + 4 * p["N"] * p["M"]
     return moe_bytes(p["T"], p["E"], p["H"], p["I"], p["topk"], host["logits"])
 
 
@@ -280,13 +287,15 @@ class Row:
                             torch.empty(M * K // 32, dtype=torch.int16, device="cuda"))
             self.y = self.out[0]
             self.in_bytes = M * K * 2
-        elif kind in ("nvfp4", "q8_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add"):
+        elif kind in ("nvfp4", "q8_0", "q4_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add"):
             M, K, N = p["M"], p["K"], p["N"]
-            if kind != "q8_0":
+            if kind == "q8_0":
+                self.w = (d(host["q"]), d(host["d"]))
+            elif kind == "q4_0":
+                self.w = (d(host["codes"]), d(host["d"]))
+            else:
                 self.w = (d(host["codes"]), d(host["scales"]))
                 self.ts = host["ts"]
-            else:
-                self.w = (d(host["q"]), d(host["d"]))
             self.x_host = host["x"]
             self.x = d(host["x"])
             self.y = torch.empty(N * M, dtype=torch.float32, device="cuda")
@@ -335,6 +344,8 @@ class Row:
             b.q8_0_encode(w[0], self.out[0], self.out[1], p["M"], p["K"])
         elif self.kind == "q8_0":
             b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
+        elif self.kind == "q4_0":
+            b.q4_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         else:
             T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
             b.moe_layer(self.logits, *w, self.x, self.y, self.ws, self.wsb, E, H, I, T, k)

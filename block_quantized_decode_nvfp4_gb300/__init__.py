@@ -38,6 +38,9 @@ from ._binding import (  # noqa: F401
     q8_0_gemv,
     q8_0_gemv_add,
     q8_0_gemv_path,
+    q4_0_gemv,
+    q4_0_gemv_path,
+    q4_0_dequant,
     q8_0_gemv_silu_mul,
     version,
 )

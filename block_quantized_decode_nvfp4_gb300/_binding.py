@@ -47,6 +47,9 @@ SIGNATURES = {
     "nvfp4_gemv_path": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "q4_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "q4_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "q4_0_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
     "nvfp4_gemv_add": (_i32, [_vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nvfp4_encode": (_i32, [_vp, _f32, _vp, _vp, _i64, _i64, _vp]),
     "q8_0_encode": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
@@ -188,6 +191,19 @@ def nvfp4_dequant(codes, scales, tensor_scale, w, M, K, stream=None):
 
 def q8_0_dequant(q, d, w, M, K, stream=None):
     _check(lib().q8_0_dequant(_ptr(q), _ptr(d), _ptr(w), M, K, _stream(stream)), "q8_0_dequant")
+
+
+def q4_0_gemv(codes, d, x, y, M, K, N, stream=None):
+    _check(lib().q4_0_gemv(_ptr(codes), _ptr(d), _ptr(x), _ptr(y), M, K, N, _stream(stream)), "q4_0_gemv")
+
+
+def q4_0_gemv_path(codes, d, x, y, M, K, N, path, stream=None):
+    _check(lib().q4_0_gemv_path(_ptr(codes), _ptr(d), _ptr(x), _ptr(y), M, K, N, path, _stream(stream)),
+           "q4_0_gemv_path")
+
+
+def q4_0_dequant(codes, d, w, M, K, stream=None):
+    _check(lib().q4_0_dequant(_ptr(codes), _ptr(d), _ptr(w), M, K, _stream(stream)), "q4_0_dequant")
 
 
 def moe_route_topk(logits, T, E, topk, expert_offsets, pair_token, pair_weight, pair_slot, stream=None):

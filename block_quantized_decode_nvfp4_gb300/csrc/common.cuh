@@ -109,6 +109,19 @@ __device__ __forceinline__ void s8x4_to_float(uint32_t w, float2& lo, float2& hi
     hi = __fadd2_rn(b, make_float2(-bias.x, -bias.y));
 }
 
+// Four bytes holding 4-bit codes q (0..15) to fp32 q - 8, exactly: the byte
+// is the low mantissa byte of 2^23, so the float reads 2^23 + q.
+__device__ __forceinline__ void u4x4_to_float(uint32_t w, float2& lo, float2& hi)
+{
+    const float2 bias = make_float2(8388616.0f, 8388616.0f);  // 2^23 + 8
+    float2 a = make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540)),
+                           __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7541)));
+    float2 b = make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7542)),
+                           __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7543)));
+    lo = __fadd2_rn(a, make_float2(-bias.x, -bias.y));
+    hi = __fadd2_rn(b, make_float2(-bias.x, -bias.y));
+}
+
 // ------------------------------------------------------------------ formats
 // A "chunk" is the unit one lane loads and multiplies per row: a run of
 // consecutive k of one weight row, with its block scales.
@@ -341,6 +354,63 @@ struct Q8_0Fmt {
     }
 };
 
+// Q4_0: a 32-element chunk is one block, 16 code bytes (byte j: element j
+// in the low nibble, element j + 16 in the high nibble, the GGUF block
+// order) and one fp16 scale; element = d * (q - 8).
+struct Q4_0Fmt {
+    static constexpr int kElems = 32;
+    __device__ static __forceinline__ int swz(int c) { return c & 7; }
+    struct Chunk {
+        uint4 c;
+        uint32_t d;
+    };
+    __device__ static __forceinline__ Chunk load(const uint8_t* codes_row, const uint8_t* d_row, int c)
+    {
+        Chunk ch;
+        ch.c = ld_stream_v4(codes_row + 16 * c);
+        ch.d = ld_stream_u16(d_row + 2 * c);
+        return ch;
+    }
+    template <int RPW, int NC>
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride, int sw,
+                                               float2 (&acc)[RPW][NC])
+    {
+        float2 part[RPW][NC];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int n = 0; n < NC; ++n) part[r][n] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // code word j: elements 4j .. 4j+3 (low nibbles), 16+4j .. (high)
+            float2 l01[RPW], l23[RPW], h01[RPW], h23[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const uint32_t words[4] = {ch[r].c.x, ch[r].c.y, ch[r].c.z, ch[r].c.w};
+                u4x4_to_float(words[j] & 0x0F0F0F0Fu, l01[r], l23[r]);
+                u4x4_to_float((words[j] >> 4) & 0x0F0F0F0Fu, h01[r], h23[r]);
+            }
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                const float4 xl = *reinterpret_cast<const float4*>(xs + n * xstride + ((j ^ sw) << 2));
+                const float4 xh = *reinterpret_cast<const float4*>(xs + n * xstride + (((4 + j) ^ sw) << 2));
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    part[r][n] = __ffma2_rn(l01[r], make_float2(xl.x, xl.y), part[r][n]);
+                    part[r][n] = __ffma2_rn(l23[r], make_float2(xl.z, xl.w), part[r][n]);
+                    part[r][n] = __ffma2_rn(h01[r], make_float2(xh.x, xh.y), part[r][n]);
+                    part[r][n] = __ffma2_rn(h23[r], make_float2(xh.z, xh.w), part[r][n]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float d = fp16_to_float(ch[r].d);
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[r][n].x = fmaf(d, part[r][n].x + part[r][n].y, acc[r][n].x);
+        }
+    }
+};
+
 // Bytes of the codes plane and of the scales plane per weight row.
 template <class F>
 struct RowPitch;
@@ -357,6 +427,11 @@ struct RowPitch<Nvfp4Narrow> {
 template <>
 struct RowPitch<Q8_0Fmt> {
     __host__ __device__ static int64_t codes(int64_t K) { return K; }
+    __host__ __device__ static int64_t scales(int64_t K) { return (K / 32) * 2; }
+};
+template <>
+struct RowPitch<Q4_0Fmt> {
+    __host__ __device__ static int64_t codes(int64_t K) { return K / 2; }
     __host__ __device__ static int64_t scales(int64_t K) { return (K / 32) * 2; }
 };
 

@@ -171,6 +171,24 @@ __global__ void q8_0_dequant_kernel(const int8_t* __restrict__ q, const uint16_t
     }
 }
 
+// w[m][k] = fp16(d) * (q - 8) in fp32 (exact), q from the GGUF Q4_0 block
+// order (element j of a 32-block: low nibble of byte j for j < 16, high
+// nibble of byte j - 16 otherwise). One thread per code byte.
+__global__ void q4_0_dequant_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ d,
+                                    float* __restrict__ w, int64_t M, int64_t K)
+{
+    const int64_t nbytes = M * (K / 2);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nbytes;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / (K / 2), bi = i - m * (K / 2);  // byte index within the row
+        const int64_t k0 = (bi / 16) * 32 + bi % 16;          // element of the low nibble
+        const float s = fp16_to_float(d[m * (K / 32) + k0 / 32]);
+        const int c = codes[i];
+        w[m * K + k0] = s * static_cast<float>((c & 15) - 8);
+        w[m * K + k0 + 16] = s * static_cast<float>((c >> 4) - 8);
+    }
+}
+
 // ------------------------------------------------------------------ host
 // Launch one (RPW, D) instantiation over a balanced grid filling every SM.
 template <class F, int RPW, int NC, int D>
@@ -248,6 +266,12 @@ cudaError_t launch_q8_0_gemv_cuda_core(const int8_t* q, const uint16_t* d, const
                                 y, M, K, N, s);
 }
 
+cudaError_t launch_q4_0_gemv_cuda_core(const uint8_t* codes, const uint16_t* d, const uint16_t* x, float* y,
+                                       int64_t M, int64_t K, int N, cudaStream_t s)
+{
+    return launch_gemv<Q4_0Fmt>(codes, reinterpret_cast<const uint8_t*>(d), 1.0f, x, y, M, K, N, s);
+}
+
 static unsigned dequant_grid(int64_t work)
 {
     int64_t g = (work + 255) / 256;
@@ -266,6 +290,13 @@ cudaError_t launch_nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, fl
 cudaError_t launch_q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t s)
 {
     q8_0_dequant_kernel<<<dequant_grid(M * K), 256, 0, s>>>(q, d, w, M, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64_t M, int64_t K,
+                                cudaStream_t s)
+{
+    q4_0_dequant_kernel<<<dequant_grid(M * K / 2), 256, 0, s>>>(codes, d, w, M, K);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,14 @@ cudaError_t launch_nvfp4_gemv_direct(const uint8_t* codes, const uint8_t* scales
                                      float* y, int64_t M, int64_t K, cudaStream_t s);
 cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
                                     int64_t K, cudaStream_t s);
+cudaError_t launch_q4_0_gemv_direct(const uint8_t* codes, const uint16_t* d, const uint16_t* x, float* y,
+                                    int64_t M, int64_t K, cudaStream_t s);
+// Q4_0 on the CUDA-core path (any M, K % 32 == 0, 1 <= N <= 16) and its
+// dequantisation.
+cudaError_t launch_q4_0_gemv_cuda_core(const uint8_t* codes, const uint16_t* d, const uint16_t* x, float* y,
+                                       int64_t M, int64_t K, int N, cudaStream_t s);
+cudaError_t launch_q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64_t M, int64_t K,
+                                cudaStream_t s);
 // The same kernel with a fused epilogue: y = W x + r (y may be r); and, on a
 // gate_up weight of 2I rows (gate rows 0..I-1, up rows I..2I-1),
 // h = SiLU(gate . x) * (up . x).

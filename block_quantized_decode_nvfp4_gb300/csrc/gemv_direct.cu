@@ -3,13 +3,14 @@
 //
 // y[m] = ts * sum_b scale[m][b] * sum_{k in b} elem[m][k] * x[k]
 // ("robertbfuentes7-cloud/bw24" README, NVFP4 (W4) decode path;
-// "avifenesh/memra" README, Decode kernels: NVFP4 and Q8_0 matvecs;
+// "avifenesh/memra" README, Decode kernels: NVFP4, Q4_0 and Q8_0 matvecs;
 // "Vemloir/LumenLLM" README, Kernels: warp-shuffle GEMVs).
 //
 // Every warp owns a contiguous, balanced range of rows and reads each row
 // with fully coalesced 16-byte loads: lane l takes the 32-element chunks
 // l, l + 32, ... of the row (16 code bytes and 2 scale bytes each for NVFP4,
-// 32 int8 and one fp16 scale for Q8_0). K is a multiple of 1024, so a row is
+// 16 code bytes and one fp16 scale for Q4_0, 32 int8 and one fp16 scale for
+// Q8_0). K is a multiple of 1024, so a row is
 // CPL = K / 1024 such chunks per lane, a compile-time constant: the loop
 // over a row is unrolled and every load offset and every activation offset
 // is an immediate. D chunks per lane stay in flight in registers (a ring
@@ -128,6 +129,59 @@ struct DirNvfp4 {
             }
             acc = fmaf(b ? sc.y : sc.x, a0 + a1, acc);
         }
+    }
+};
+
+// Q4_0: the chunk is one block; code byte j holds element j (low nibble) and
+// element j + 16 (high nibble), the GGUF order, so word w of the chunk holds
+// elements 4w .. 4w + 3 and 16 + 4w .. 16 + 4w + 3: activation pieces w / 2
+// and 2 + w / 2. q - 8 is exact in f16 (1024 + q from the byte's mantissa
+// bits, minus 1032).
+struct DirQ4 {
+    using Item = Nvfp4Item;  // 16 code bytes, the fp16 scale
+    static constexpr int kCodeBytes = 16;
+    __device__ static __forceinline__ Item load(const uint8_t* c, const uint8_t* s)
+    {
+        Item it;
+        it.c = ld_stream_v4(c);
+        it.s = ld_stream_u16(s);
+        return it;
+    }
+    template <bool FAST>
+    __device__ static __forceinline__ void dot(const Item& it, const uint16_t* xc, int sw, float& acc)
+    {
+        const uint32_t words[4] = {it.c.x, it.c.y, it.c.z, it.c.w};
+        uint4 xq[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) xq[p] = *reinterpret_cast<const uint4*>(xc + ((p ^ sw) << 3));
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t nib[2] = {words[w] & 0x0F0F0F0Fu, (words[w] >> 4) & 0x0F0F0F0Fu};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // h = 0: elements 4w.., piece w / 2; h = 1: 16 + 4w.., piece 2 + w / 2
+                const uint4 xv = xq[2 * h + w / 2];
+                const uint32_t xp[4] = {xv.x, xv.y, xv.z, xv.w};
+                const uint32_t x01 = xp[(w % 2) * 2], x23 = xp[(w % 2) * 2 + 1];
+                uint32_t p01 = __byte_perm(nib[h], 0x64646464u, 0x4140);
+                uint32_t p23 = __byte_perm(nib[h], 0x64646464u, 0x4342);
+                __half2 q01 = __hsub2(*reinterpret_cast<__half2*>(&p01), bias);
+                __half2 q23 = __hsub2(*reinterpret_cast<__half2*>(&p23), bias);
+                const uint32_t w01 = *reinterpret_cast<uint32_t*>(&q01), w23 = *reinterpret_cast<uint32_t*>(&q23);
+                if constexpr (FAST) {
+                    fma_f16x2(w01, x01, a0, a1);
+                    fma_f16x2(w23, x23, a0, a1);
+                } else {
+                    const float2 f01 = f16x2_to_float2(w01), f23 = f16x2_to_float2(w23);
+                    a0 = fmaf(f01.x, bf16_lo(x01), a0);
+                    a1 = fmaf(f01.y, bf16_hi(x01), a1);
+                    a0 = fmaf(f23.x, bf16_lo(x23), a0);
+                    a1 = fmaf(f23.y, bf16_hi(x23), a1);
+                }
+            }
+        }
+        acc = fmaf(fp16_to_float(it.s), a0 + a1, acc);
     }
 };
 
@@ -375,6 +429,8 @@ struct DirCfg<DirNvfp4> {
     static constexpr int depth() { return CPL == 4 ? 4 : (CPL == 12 ? 6 : (CPL == 3 ? 3 : 2)); }
 };
 template <>
+struct DirCfg<DirQ4> : DirCfg<DirNvfp4> {};
+template <>
 struct DirCfg<DirQ8> {
     template <int CPL>
     static constexpr int threads() { return 896; }
@@ -443,6 +499,12 @@ cudaError_t launch_nvfp4_gemv_direct(const uint8_t* codes, const uint8_t* scales
                                      float* y, int64_t M, int64_t K, cudaStream_t s)
 {
     return launch_direct<DirNvfp4, kEpiPlain>(codes, scales, ts, x, y, nullptr, M, K, s);
+}
+
+cudaError_t launch_q4_0_gemv_direct(const uint8_t* codes, const uint16_t* d, const uint16_t* x, float* y,
+                                    int64_t M, int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirQ4, kEpiPlain>(codes, reinterpret_cast<const uint8_t*>(d), 1.0f, x, y, nullptr, M, K, s);
 }
 
 cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,

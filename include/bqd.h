@@ -266,6 +266,36 @@ bqd_status nvfp4_dequant(const uint8_t* codes, const uint8_t* scales, float tens
 bqd_status q8_0_dequant(const int8_t* q, const uint16_t* d, float* w, int64_t M, int64_t K, cudaStream_t stream);
 
 /*
+ * q4_0_gemv -- y[n][m] = sum_k fp16(d[m][k/32]) * (q[m][k] - 8) * x[n][k]
+ * ("avifenesh/memra" README, Decode kernels bullet: NVFP4 / Q4_0 / Q8_0
+ * matvecs; "robertbfuentes7-cloud/bw24" README, GGUF bullet: Q4_0 among the
+ * file formats).
+ *   codes u8 [M][K/2]: 16 bytes per 32-element block; byte j of a block
+ *         holds element j (low nibble) and element j + 16 (high nibble), the
+ *         order of a GGUF Q4_0 block, whose fp16 field is the d plane:
+ *   d     fp16 bits [M][K/32]. The planes are a GGUF block's two fields,
+ *         split (planar), so a loader copies them byte for byte.
+ *   x bf16 bits [N][K]; y fp32 [N][M]. K % 32 == 0, 1 <= N <= 16; M == 0 and
+ *   K == 0 behave as in nvfp4_gemv. codes, d, x, y 16-byte aligned.
+ *   AUTO: BQD_PATH_DIRECT for N == 1 and the K it takes (K a multiple of
+ *   1024 with K / 1024 in {1, 2, 3, 4, 6, 8, 12, 16}), else
+ *   BQD_PATH_CUDA_CORE. Products are exact (q - 8 and the prescaled
+ *   activations are f16 values, or fp32 FMAs outside that range); sums fp32.
+ */
+bqd_status q4_0_gemv(const uint8_t* codes, const uint16_t* d, const uint16_t* x, float* y, int64_t M, int64_t K,
+                     int N, cudaStream_t stream);
+
+/* q4_0_gemv with an explicit compute path: BQD_PATH_AUTO, BQD_PATH_DIRECT or
+ * BQD_PATH_CUDA_CORE (others: BQD_ERR_PATH). */
+bqd_status q4_0_gemv_path(const uint8_t* codes, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
+                          int64_t K, int N, int path, cudaStream_t stream);
+
+/* q4_0_dequant -- w[m][k] = fp16(d[m][k/32]) * (q[m][k] - 8) (exact in
+ * fp32); layout and shape rules as q4_0_gemv. */
+bqd_status q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64_t M, int64_t K,
+                        cudaStream_t stream);
+
+/*
  * moe_route_topk -- router and expert-major list of a top-k routed MoE layer
  * ("robertbfuentes7-cloud/bw24" README, MoE bullet: expert-major batching).
  *   logits fp32 [T][E]. For each token: softmax over the E logits, keep the
