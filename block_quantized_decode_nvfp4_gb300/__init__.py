@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     moe_workspace_bytes,
     nvfp4_dequant,
     nvfp4_encode,
+    nvfp4_gemm,
     nvfp4_gemv,
     nvfp4_gemv_add,
     nvfp4_gemv_path,

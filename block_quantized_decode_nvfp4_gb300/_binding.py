@@ -47,6 +47,7 @@ SIGNATURES = {
     "nvfp4_gemv_path": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "nvfp4_gemm": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i64, _vp]),
     "q4_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q4_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q4_0_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
@@ -191,6 +192,11 @@ def nvfp4_dequant(codes, scales, tensor_scale, w, M, K, stream=None):
 
 def q8_0_dequant(q, d, w, M, K, stream=None):
     _check(lib().q8_0_dequant(_ptr(q), _ptr(d), _ptr(w), M, K, _stream(stream)), "q8_0_dequant")
+
+
+def nvfp4_gemm(codes, scales, tensor_scale, x, y, M, K, T, stream=None):
+    _check(lib().nvfp4_gemm(_ptr(codes), _ptr(scales), tensor_scale, _ptr(x), _ptr(y), M, K, T, _stream(stream)),
+           "nvfp4_gemm")
 
 
 def q4_0_gemv(codes, d, x, y, M, K, N, stream=None):

@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "bqd.h"
+#include "gemm.h"
 #include "gemv.h"
 #include "host_util.h"
 
@@ -185,6 +186,24 @@ bqd_status q4_0_gemv(const uint8_t* codes, const uint16_t* d, const uint16_t* x,
     return q4_0_gemv_path(codes, d, x, y, M, K, N, BQD_PATH_AUTO, stream);
 }
 
+// ---------------------------------------------------------------- prefill GEMM
+bqd_status nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x, float* y,
+                      int64_t M, int64_t K, int64_t T, cudaStream_t stream)
+{
+    if (M < 0 || K < 0 || T < 0 || K % 64 != 0) return BQD_ERR_SHAPE;
+    if (M > 0 && K > 0 && M > (int64_t(1) << 62) / K) return BQD_ERR_SHAPE;
+    if (M == 0 || T == 0) return BQD_OK;
+    if (!y) return BQD_ERR_NULL;
+    if (!aligned16(y)) return BQD_ERR_ALIGN;
+    bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    if (K == 0) return zero_output(y, M * T, stream);
+    if (!codes || !scales || !x) return BQD_ERR_NULL;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(x)) return BQD_ERR_ALIGN;
+    if (!bqd::gemm_supported(M, K, T)) return BQD_ERR_SHAPE;
+    return from_cuda(bqd::launch_nvfp4_gemm(codes, scales, tensor_scale, x, y, M, K, T, stream));
+}
+
 // ---------------------------------------------------------------- encoders
 bqd_status nvfp4_encode(const uint16_t* w, float tensor_scale, uint8_t* codes, uint8_t* scales, int64_t M, int64_t K,
                         cudaStream_t stream)
@@ -267,12 +286,12 @@ bqd_status bqd_device_error(unsigned int* bits_out)
     if (!bits_out) return BQD_ERR_NULL;
     bqd_status st = check_arch();
     if (st != BQD_OK) return st;
-    unsigned int v = 0, w = 0, m = 0, n = 0;
+    unsigned int v = 0, w = 0, m = 0, n = 0, g = 0;
     if (bqd::read_and_clear_stream_error(&v) != cudaSuccess || bqd::read_and_clear_mma_error(&w) != cudaSuccess ||
         bqd::read_and_clear_moe_stream_error(&m) != cudaSuccess ||
-        bqd::read_and_clear_moe_small_error(&n) != cudaSuccess)
+        bqd::read_and_clear_moe_small_error(&n) != cudaSuccess || bqd::read_and_clear_gemm_error(&g) != cudaSuccess)
         return BQD_ERR_LAUNCH;
-    v |= w | m | n;
+    v |= w | m | n | g;
     *bits_out = v;
     return v ? BQD_ERR_DEVICE : BQD_OK;
 }

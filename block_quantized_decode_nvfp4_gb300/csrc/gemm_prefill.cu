@@ -1,0 +1,375 @@
+// gemm_prefill.cu -- NVFP4 weights times many bf16 tokens (prefill) on the
+// 5th-generation tensor cores: Y[t][m] = ts * sum_k W[m][k] * x[t][k].
+//
+// The pages' prefill runs its NVFP4 weights through GEMMs over many tokens
+// ("Vemloir/LumenLLM" README, Kernels bullet: NVFP4 grouped-MoE prefill, a
+// per-expert variable-grid NVFP4 GEMM). This is that GEMM for one weight
+// matrix; a grouped MoE prefill runs it per expert on the expert's gathered
+// tokens.
+//
+// A CTA computes a 128 x 256 tile of Y (128 weight rows, 256 tokens) with
+// tcgen05.mma kind::f16 (M = 128, N = 256, K = 16, bf16 operands, fp32
+// accumulators in 256 columns of tensor memory), both operands in shared
+// memory, K-major, no swizzle (core matrices of 8 rows x 16 bytes; 128 bytes
+// between row groups, the whole 16-byte column of a k group between k
+// groups). Each ring stage holds 64 k:
+//  - B, 256 tokens x 64 k of x, comes in by eight 2-D tensor copies (one per
+//    8-k group, 256 rows x 16 bytes; tokens past T read as zero);
+//  - A, 128 rows x 64 k of W, is written by four decoder warps, one row per
+//    thread: E2M1 codes to f16, times the block's E4M3 scale (exact: the
+//    product has at most 6 significant bits and lies in [2^-10, 2688]), to
+//    bf16 (exact for the same reason), so every product of the MMA is
+//    exact and only the fp32 accumulation rounds.
+// Warp 0 issues the copies, warp 1 the MMAs (one elected lane), warps 2..5
+// decode and, at the end, read the accumulators (warp w owns tensor-memory
+// lanes 32 (w % 4) .. + 31, its rows) and store ts * D. Every wait is
+// bounded; a wait that runs out sets the kernel's device error word and the
+// outputs are unspecified.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "host_util.h"
+#include "stream.cuh"
+
+namespace bqd {
+
+// Device error word of the prefill GEMM (kErrWaitTimeout); read and cleared
+// by read_and_clear_gemm_error().
+__device__ unsigned int g_gemm_error = 0;
+
+namespace {
+
+constexpr int kGM = 128;                    // weight rows per tile (MMA M)
+constexpr int kGN = 256;                    // tokens per tile (MMA N)
+constexpr int kGK = 64;                     // k per ring stage
+constexpr int kGS = 4;                      // ring stages
+constexpr int kGDec = 4;                    // decoder warps, one row per thread
+constexpr int kGThreads = (2 + kGDec) * kWarp;
+constexpr int kALoads = 4;                  // stages of a row's codes in flight per decoder thread
+constexpr int kAStage = kGM * kGK * 2;      // 16 KiB of bf16
+constexpr int kBStage = kGN * kGK * 2;      // 32 KiB of bf16
+constexpr int kGSmem = kGS * (kAStage + kBStage) + 1024;  // + alignment slack
+constexpr int kGTmemCols = kGN;             // fp32 accumulators, one column per token
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, no swizzle: start address, the
+// byte distance between core matrices adjacent in k (lbo) and adjacent in
+// rows (sbo), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+
+// D[tmem_d] (+)= A[adesc] * B[bdesc]^T, both operands in shared memory.
+__device__ __forceinline__ void mma_ss(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(pred));
+    return pred != 0;
+}
+
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h)
+{
+    const float2 f = f16x2_to_float2(h);
+    __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);  // exact: E2M1 x E4M3 products fit in bf16
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// 64 consecutive k of one row (32 code bytes c0, c1; the 4 block scales in
+// s4) to 32 bf16 pairs, pair j = elements 2j (low half) and 2j + 1.
+__device__ __forceinline__ void decode64(const uint4& c0, const uint4& c1, uint32_t s4, uint32_t (&a)[32])
+{
+    const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xFFFFu), s23 = e4m3x2_to_f16x2(s4 >> 16);
+    const uint32_t sb[4] = {__byte_perm(s01, 0, 0x1010), __byte_perm(s01, 0, 0x3232), __byte_perm(s23, 0, 0x1010),
+                            __byte_perm(s23, 0, 0x3232)};
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {  // word i = k 8i .. 8i + 7, block i / 2
+        uint32_t h[4];
+        e2m1x8_to_f16x2(w[i], h);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[4 * i + j] = f16x2_to_bf16x2(hmul2_bits(h[j], sb[i >> 1]));
+    }
+}
+
+struct RowLoad {  // 64 k of one weight row
+    uint4 c0, c1;
+    uint32_t s4;
+};
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ codes,
+                      const uint8_t* __restrict__ scales, float ts, float* __restrict__ y, int64_t M, int K, int T)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bfull[kGS], afull[kGS], empty[kGS], dfull;
+    __shared__ uint32_t s_tmem;
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* astage = sm;
+    uint8_t* bstage = sm + kGS * kAStage;
+    const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kGM;
+    const int n0 = blockIdx.y * kGN;
+    const int nk = K / kGK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kGS; ++s) {
+            mbar_init(&bfull[s], 1);
+            mbar_init(&afull[s], kGDec);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&dfull, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(kGTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    pdl_trigger();
+    pdl_wait();  // x may come from the previous kernel in the stream; y may be read by it
+
+    bool ok = true;
+    if (warp == 0) {
+        // ------------------------------------------------ B: x tiles
+        if (lane == 0) {
+            for (int s = 0; s < nk && ok; ++s) {
+                const int st = s % kGS;
+                if (s >= kGS) ok = mbar_wait(&empty[st], static_cast<uint32_t>(((s / kGS) & 1) ^ 1), &g_gemm_error);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&bfull[st], kBStage);
+#pragma unroll
+                for (int g = 0; g < kGK / 8; ++g)
+                    tma_load_2d(bstage + st * kBStage + g * (kGN * 16), &map_x, s * kGK + 8 * g, n0, &bfull[st]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issue
+        const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kGN >> 3) << 17) |
+                               (static_cast<uint32_t>(kGM >> 4) << 24);  // f32 D, bf16 A and B, N, M
+        for (int s = 0; s < nk && ok; ++s) {
+            const int st = s % kGS;
+            const uint32_t ph = static_cast<uint32_t>((s / kGS) & 1);
+            ok = mbar_wait_warp(&bfull[st], ph, &g_gemm_error) && mbar_wait_warp(&afull[st], ph, &g_gemm_error);
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t a0 = smem_u32(astage + st * kAStage), b0 = smem_u32(bstage + st * kBStage);
+#pragma unroll
+                for (int j = 0; j < kGK / 16; ++j) {  // 16 k = two 8-k groups
+                    const uint64_t ad = smem_desc(a0 + 2 * j * (kGM * 16), kGM * 16, 128);
+                    const uint64_t bd = smem_desc(b0 + 2 * j * (kGN * 16), kGN * 16, 128);
+                    mma_ss(tmem, ad, bd, idesc, (s | j) != 0 ? 1u : 0u);
+                }
+                mma_commit(&empty[st]);  // the stage is free once these MMAs have read it
+            }
+            __syncwarp();
+        }
+        if (ok && elect_one()) mma_commit(&dfull);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ A: decode, then the epilogue
+        const int q = warp % 4;                 // tensor-memory lane quarter of this warp
+        const int r = 32 * q + lane;            // row of the tile
+        const int64_t m = m0 + r;
+        const bool live = m < M;
+        const uint8_t* crow = codes + (live ? m : 0) * static_cast<int64_t>(K / 2);
+        const uint8_t* srow = scales + (live ? m : 0) * static_cast<int64_t>(K / 16);
+        RowLoad ring[kALoads];
+        auto load = [&](int s) -> RowLoad {
+            RowLoad v;
+            if (live && s < nk) {
+                v.c0 = ld_stream_v4(crow + s * 32);
+                v.c1 = ld_stream_v4(crow + s * 32 + 16);
+                v.s4 = *reinterpret_cast<const uint32_t*>(srow + s * 4);
+            } else {
+                v.c0 = v.c1 = make_uint4(0u, 0u, 0u, 0u);
+                v.s4 = 0u;
+            }
+            return v;
+        };
+#pragma unroll
+        for (int d = 0; d < kALoads; ++d) ring[d] = load(d);
+        for (int s0 = 0; s0 < nk && ok; s0 += kALoads) {
+#pragma unroll
+            for (int d = 0; d < kALoads; ++d) {
+                const int s = s0 + d;
+                if (s < nk && ok) {
+                    const int st = s % kGS;
+                    const RowLoad cur = ring[d];
+                    ring[d] = load(s + kALoads);
+                    uint32_t a[32];
+                    decode64(cur.c0, cur.c1, cur.s4, a);
+                    if (s >= kGS)
+                        ok = mbar_wait_warp(&empty[st], static_cast<uint32_t>(((s / kGS) & 1) ^ 1), &g_gemm_error);
+                    if (ok) {
+                        uint8_t* dst = astage + st * kAStage + r * 16;
+#pragma unroll
+                        for (int g = 0; g < kGK / 8; ++g)
+                            *reinterpret_cast<uint4*>(dst + g * (kGM * 16)) =
+                                make_uint4(a[4 * g], a[4 * g + 1], a[4 * g + 2], a[4 * g + 3]);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor cores
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&afull[st]);
+                    }
+                }
+            }
+        }
+        // ---- epilogue: this warp's 32 rows, 16 tokens per tensor-memory load
+        if (ok) ok = mbar_wait_warp(&dfull, 0, &g_gemm_error);
+        tc_fence_after();
+        if (ok) {
+            const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+#pragma unroll 1
+            for (int c = 0; c < kGN / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld_x16(tmem + lane_base + 16 * c, v);
+                if (live) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = n0 + 16 * c + j;
+                        if (n < T) y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[j]) * ts;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGTmemCols) : "memory");
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool gemm_supported(int64_t M, int64_t K, int64_t T)
+{
+    return M >= 1 && K >= kGK && K % kGK == 0 && K <= (int64_t(1) << 24) && T >= 1 && T <= (int64_t(1) << 24) &&
+           M <= (int64_t(1) << 31) && (M + kGM - 1) / kGM <= 0x7FFFFFFF && (T + kGN - 1) / kGN <= 65535;
+}
+
+cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
+                              int64_t M, int64_t K, int64_t T, cudaStream_t s)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    // x [T][K] bf16, read in boxes of 8 k x 256 tokens; tokens past T read as zero
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {8, static_cast<cuuint32_t>(kGN)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static OccCache occ;
+    blocks_per_sm(occ, reinterpret_cast<const void*>(nvfp4_gemm_kernel), dev, kGThreads, kGSmem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((M + kGM - 1) / kGM), static_cast<unsigned>((T + kGN - 1) / kGN));
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kGSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = launch_flags() & kLaunchPdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, map, codes, scales, ts, y, M, static_cast<int>(K),
+                              static_cast<int>(T));
+}
+
+cudaError_t read_and_clear_gemm_error(unsigned int* out)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(v));
+    if (e != cudaSuccess) return e;
+    *out = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(zero));
+    }
+    return e;
+}
+
+}  // namespace bqd

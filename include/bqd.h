@@ -231,9 +231,9 @@ bqd_status q8_0_gemv_path(const int8_t* q, const uint16_t* d, const uint16_t* x,
 /*
  * bqd_device_error -- waits for the device, copies the device error words of
  * the streaming and tensor-core GEMV kernels (BQD_PATH_STREAM, BQD_PATH_MMA),
- * of the MoE stream kernels and of the small-batch MoE kernels (the
- * activations' copy in moe_layer / moe_grouped_gemv at T <= 16) to
- * *bits_out (OR of the four) and clears them. Bit 0: a wait ran out
+ * of the MoE stream kernels, of the small-batch MoE kernels (the
+ * activations' copy in moe_layer / moe_grouped_gemv at T <= 16) and of the
+ * prefill GEMM (nvfp4_gemm) to *bits_out (OR of the five) and clears them. Bit 0: a wait ran out
  * (the kernel gave up instead of hanging; its outputs are unspecified).
  * Returns BQD_ERR_DEVICE if any bit was set. Synchronising: do not call it
  * inside a stream capture.
@@ -289,6 +289,23 @@ bqd_status q4_0_gemv(const uint8_t* codes, const uint16_t* d, const uint16_t* x,
  * BQD_PATH_CUDA_CORE (others: BQD_ERR_PATH). */
 bqd_status q4_0_gemv_path(const uint8_t* codes, const uint16_t* d, const uint16_t* x, float* y, int64_t M,
                           int64_t K, int N, int path, cudaStream_t stream);
+
+/*
+ * nvfp4_gemm -- Y[t][m] = ts * sum_k e2m1(c[m][k]) * e4m3(s[m][k/16]) * x[t][k]
+ * for many tokens (prefill) on the tensor cores ("Vemloir/LumenLLM" README,
+ * Kernels bullet: NVFP4 grouped-MoE prefill, a per-expert variable-grid
+ * NVFP4 GEMM; this is the GEMM of one weight matrix, which a grouped MoE
+ * prefill runs per expert on its gathered tokens).
+ *   codes, scales, tensor_scale as nvfp4_gemv; x bf16 bits [T][K]; y fp32
+ *   [T][M] (written, never read). K % 64 == 0, T >= 0, M >= 0; M == 0 or
+ *   T == 0: BQD_OK without touching the GPU; K == 0: y set to zero. All
+ *   pointers 16-byte aligned. Every product is exact (the dequantised
+ *   weight and x are bf16 values); the sums are fp32 in the tensor cores'
+ *   order, so |y - y_exact| stays within the GEMV tolerance. Tiles of 128
+ *   weight rows x 256 tokens, one CTA each (up to 65535 token tiles).
+ */
+bqd_status nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x, float* y,
+                      int64_t M, int64_t K, int64_t T, cudaStream_t stream);
 
 /* q4_0_dequant -- w[m][k] = fp16(d[m][k/32]) * (q[m][k] - 8) (exact in
  * fp32); layout and shape rules as q4_0_gemv. */
