@@ -7,24 +7,29 @@
 // matrix; a grouped MoE prefill runs it per expert on the expert's gathered
 // tokens.
 //
-// A CTA computes a 128 x 256 tile of Y (128 weight rows, 256 tokens) with
-// tcgen05.mma kind::f16 (M = 128, N = 256, K = 16, bf16 operands, fp32
-// accumulators in 256 columns of tensor memory), both operands in shared
-// memory, K-major, no swizzle (core matrices of 8 rows x 16 bytes; 128 bytes
-// between row groups, the whole 16-byte column of a k group between k
-// groups). Each ring stage holds 64 k:
-//  - B, 256 tokens x 64 k of x, comes in by eight 2-D tensor copies (one per
-//    8-k group, 256 rows x 16 bytes; tokens past T read as zero);
-//  - A, 128 rows x 64 k of W, is written by four decoder warps, one row per
-//    thread: E2M1 codes to f16, times the block's E4M3 scale (exact: the
-//    product has at most 6 significant bits and lies in [2^-10, 2688]), to
-//    bf16 (exact for the same reason), so every product of the MMA is
-//    exact and only the fp32 accumulation rounds.
-// Warp 0 issues the copies, warp 1 the MMAs (one elected lane), warps 2..5
+// A CTA computes a 256 x 256 tile of Y (256 weight rows, 256 tokens) as two
+// halves of 128 rows with tcgen05.mma kind::f16 (M = 128, N = 256, K = 16,
+// bf16 operands, fp32 accumulators: all 512 columns of tensor memory), both
+// operands in shared memory, K-major; the two halves share every tile of B,
+// which halves B's traffic per flop against a 128-row tile. Each ring stage
+// holds 64 k:
+//  - B, 256 tokens x 64 k of x (128 bytes a token), comes in by one 2-D
+//    tensor copy with the 128-byte swizzle (tokens past T read as zero) and
+//    is read through a matching descriptor (8-row atoms of 1024 bytes, the
+//    16 k of an MMA at 32 bytes into the atom). Narrower, unswizzled boxes of
+//    16 bytes a row moved twice the bytes through the memory system;
+//  - A, 2 x 128 rows x 64 k of W, is written by eight decoder warps, one row
+//    per thread, K-major without swizzle (core matrices of 8 rows x 16 bytes;
+//    128 bytes between row groups, 2 KiB between 8-k groups): E2M1 codes to
+//    f16, times the block's E4M3 scale (exact: the product has at most 6
+//    significant bits and lies in [2^-10, 2688]), to bf16 (exact for the
+//    same reason), so every product of the MMA is exact and only the fp32
+//    accumulation rounds.
+// Warp 0 issues the copies, warp 1 the MMAs (one elected lane), warps 2..9
 // decode and, at the end, read the accumulators (warp w owns tensor-memory
-// lanes 32 (w % 4) .. + 31, its rows) and store ts * D. Every wait is
-// bounded; a wait that runs out sets the kernel's device error word and the
-// outputs are unspecified.
+// lanes 32 (w % 4) .. + 31 of half (w - 2) / 4, its rows) and store ts * D.
+// Every wait is bounded; a wait that runs out sets the kernel's device error
+// word and the outputs are unspecified.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -46,17 +51,19 @@ __device__ unsigned int g_gemm_error = 0;
 
 namespace {
 
-constexpr int kGM = 128;                    // weight rows per tile (MMA M)
+constexpr int kGH = 128;                    // rows per half (MMA M)
+constexpr int kGM = 2 * kGH;                // weight rows per tile
 constexpr int kGN = 256;                    // tokens per tile (MMA N)
 constexpr int kGK = 64;                     // k per ring stage
-constexpr int kGS = 4;                      // ring stages
-constexpr int kGDec = 4;                    // decoder warps, one row per thread
+constexpr int kGS = 3;                      // ring stages
+constexpr int kGDec = kGM / kWarp;          // decoder warps, one row per thread
 constexpr int kGThreads = (2 + kGDec) * kWarp;
-constexpr int kALoads = 4;                  // stages of a row's codes in flight per decoder thread
-constexpr int kAStage = kGM * kGK * 2;      // 16 KiB of bf16
+constexpr int kALoads = 8;                  // stages of a row's codes in flight per decoder thread
+constexpr int kAHalf = kGH * kGK * 2;       // 16 KiB of bf16
+constexpr int kAStage = 2 * kAHalf;
 constexpr int kBStage = kGN * kGK * 2;      // 32 KiB of bf16
 constexpr int kGSmem = kGS * (kAStage + kBStage) + 1024;  // + alignment slack
-constexpr int kGTmemCols = kGN;             // fp32 accumulators, one column per token
+constexpr int kGTmemCols = 2 * kGN;         // fp32 accumulators: half h in columns [256 h, 256 h + 256)
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -79,6 +86,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 {
     return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+
+// The same for K-major operands with the 128-byte swizzle, as a 2-D tensor
+// copy with CU_TENSOR_MAP_SWIZZLE_128B leaves them: 8-row atoms of 1024
+// bytes (sbo), the leading offset unused (1), layout type 2.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
+{
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) | (static_cast<uint64_t>(2) << 61);
 }
 
 // D[tmem_d] (+)= A[adesc] * B[bdesc]^T, both operands in shared memory.
@@ -192,16 +208,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 if (s >= kGS) ok = mbar_wait(&empty[st], static_cast<uint32_t>(((s / kGS) & 1) ^ 1), &g_gemm_error);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&bfull[st], kBStage);
-#pragma unroll
-                for (int g = 0; g < kGK / 8; ++g)
-                    tma_load_2d(bstage + st * kBStage + g * (kGN * 16), &map_x, s * kGK + 8 * g, n0, &bfull[st]);
+                tma_load_2d(bstage + st * kBStage, &map_x, s * kGK, n0, &bfull[st]);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue
         const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kGN >> 3) << 17) |
-                               (static_cast<uint32_t>(kGM >> 4) << 24);  // f32 D, bf16 A and B, N, M
+                               (static_cast<uint32_t>(kGH >> 4) << 24);  // f32 D, bf16 A and B, N, M
         for (int s = 0; s < nk && ok; ++s) {
             const int st = s % kGS;
             const uint32_t ph = static_cast<uint32_t>((s / kGS) & 1);
@@ -211,10 +225,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
             if (elect_one()) {
                 const uint32_t a0 = smem_u32(astage + st * kAStage), b0 = smem_u32(bstage + st * kBStage);
 #pragma unroll
-                for (int j = 0; j < kGK / 16; ++j) {  // 16 k = two 8-k groups
-                    const uint64_t ad = smem_desc(a0 + 2 * j * (kGM * 16), kGM * 16, 128);
-                    const uint64_t bd = smem_desc(b0 + 2 * j * (kGN * 16), kGN * 16, 128);
-                    mma_ss(tmem, ad, bd, idesc, (s | j) != 0 ? 1u : 0u);
+                for (int j = 0; j < kGK / 16; ++j) {  // 16 k = two 8-k groups of A, 32 bytes of B's rows
+                    const uint64_t bd = smem_desc_sw128(b0 + 32 * j);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t ad = smem_desc(a0 + h * kAHalf + 2 * j * (kGH * 16), kGH * 16, 128);
+                        mma_ss(tmem + h * kGN, ad, bd, idesc, (s | j) != 0 ? 1u : 0u);
+                    }
                 }
                 mma_commit(&empty[st]);  // the stage is free once these MMAs have read it
             }
@@ -225,7 +242,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     } else {
         // ------------------------------------------------ A: decode, then the epilogue
         const int q = warp % 4;                 // tensor-memory lane quarter of this warp
-        const int r = 32 * q + lane;            // row of the tile
+        const int hf = (warp - 2) / 4;          // half of the tile
+        const int r = kGH * hf + 32 * q + lane;  // row of the tile
         const int64_t m = m0 + r;
         const bool live = m < M;
         const uint8_t* crow = codes + (live ? m : 0) * static_cast<int64_t>(K / 2);
@@ -258,10 +276,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     if (s >= kGS)
                         ok = mbar_wait_warp(&empty[st], static_cast<uint32_t>(((s / kGS) & 1) ^ 1), &g_gemm_error);
                     if (ok) {
-                        uint8_t* dst = astage + st * kAStage + r * 16;
+                        uint8_t* dst = astage + st * kAStage + hf * kAHalf + (r - kGH * hf) * 16;
 #pragma unroll
                         for (int g = 0; g < kGK / 8; ++g)
-                            *reinterpret_cast<uint4*>(dst + g * (kGM * 16)) =
+                            *reinterpret_cast<uint4*>(dst + g * (kGH * 16)) =
                                 make_uint4(a[4 * g], a[4 * g + 1], a[4 * g + 2], a[4 * g + 3]);
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // read by the tensor cores
                         __syncwarp();
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < kGN / 16; ++c) {
                 uint32_t v[16];
-                tmem_ld_x16(tmem + lane_base + 16 * c, v);
+                tmem_ld_x16(tmem + lane_base + hf * kGN + 16 * c, v);
                 if (live) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -330,14 +348,15 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
-    // x [T][K] bf16, read in boxes of 8 k x 256 tokens; tokens past T read as zero
+    // x [T][K] bf16, read in boxes of 64 k x 256 tokens (128 bytes a token,
+    // 128-byte swizzle); tokens past T read as zero
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {8, static_cast<cuuint32_t>(kGN)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGK), static_cast<cuuint32_t>(kGN)};
     const cuuint32_t estr[2] = {1, 1};
     if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     int dev = 0;
