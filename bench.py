@@ -47,6 +47,7 @@ WORKLOAD = ("decode step: NVFP4 N=1 {12288x4096, 4096x12288, 4096x4096}; Q8_0 N=
             "151936x4096}; NVFP4 verify N=4,8 {4096x4096, 12288x4096}; MoE E=256 H=2048 I=512 top-8 T=1,16")
 L2_BYTES_FALLBACK = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------- workload
@@ -102,6 +103,8 @@ def extra_rows_spec():
     the decode-path epilogue fusions on the layer shapes (gate_up with
     SiLU * up on the 12288 x 4096 gate/up weight, I = 6144; down with the
     residual add on 4096 x 12288); the Q4_0 GEMV on the two layer shapes;
+    the tensor-core prefill GEMM of the 12288 x 4096 weight over 2048
+    tokens (reported in TFLOP/s against the measured bf16 peak);
     and the bf16 -> NVFP4 / Q8_0 encoders on a 12288 x 4096 weight (bytes:
     bf16 read, codes and scales written)."""
     return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1)),
@@ -109,6 +112,7 @@ def extra_rows_spec():
             ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1)),
             ("q4_0 12288x4096 N=1", "q4_0", dict(M=12288, K=4096, N=1)),
             ("q4_0 4096x12288 N=1", "q4_0", dict(M=4096, K=12288, N=1)),
+            ("nvfp4 prefill GEMM 12288x4096 T=2048", "nvfp4_gemm", dict(M=12288, K=4096, N=2048)),
             ("nvfp4 encode 12288x4096", "nvfp4_encode", dict(M=12288, K=4096, N=1)),
             ("q8_0 encode 12288x4096", "q8_0_encode", dict(M=12288, K=4096, N=1))]
 
@@ -116,7 +120,7 @@ def extra_rows_spec():
 def host_inputs(kind, p, seed=0):
     if kind == "nvfp4_tiny":
         return syn.tiny_nvfp4(seed=seed)
-    if kind in ("nvfp4", "nvfp4_silu"):
+    if kind in ("nvfp4", "nvfp4_silu", "nvfp4_gemm"):
         return syn.dense_nvfp4(p["M"], p["K"], N=p["N"], seed=seed)
     if kind in ("nvfp4_encode", "q8_0_encode"):
         return {"x": syn.bf16_normal((p["M"], p["K"]), np.random.default_rng(seed + 7))}
@@ -132,7 +136,7 @@ def host_inputs(kind, p, seed=0):
 
 
 def row_bytes(kind, p, host):
-    if kind in ("nvfp4", "nvfp4_tiny"):
+    if kind in ("nvfp4", "nvfp4_tiny", "nvfp4_gemm"):
         return nvfp4_bytes(p["M"], p["K"], p["N"])
     if kind == "nvfp4_silu":  # the output is h, half the rows
         return nvfp4_bytes(p["M"], p["K"], p["N"]) - 4 * p["N"] * p["M"] // 2
@@ -157,6 +161,15 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s of a kernel timed alone (the burst figure)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return FALLBACK_BF16_TFLOPS
 
 
 class ClockSampler:
@@ -287,7 +300,7 @@ class Row:
                             torch.empty(M * K // 32, dtype=torch.int16, device="cuda"))
             self.y = self.out[0]
             self.in_bytes = M * K * 2
-        elif kind in ("nvfp4", "q8_0", "q4_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add"):
+        elif kind in ("nvfp4", "q8_0", "q4_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add", "nvfp4_gemm"):
             M, K, N = p["M"], p["K"], p["N"]
             if kind == "q8_0":
                 self.w = (d(host["q"]), d(host["d"]))
@@ -346,6 +359,8 @@ class Row:
             b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "q4_0":
             b.q4_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
+        elif self.kind == "nvfp4_gemm":
+            b.nvfp4_gemm(w[0], w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"])
         else:
             T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
             b.moe_layer(self.logits, *w, self.x, self.y, self.ws, self.wsb, E, H, I, T, k)
@@ -595,6 +610,7 @@ def run_ours(args, rank, world):
 
     # ---- headline: K full steps, inputs resident in HBM
     peak, peak_kind = measured_peaks()
+    tensor_peak = measured_tensor_peak()
     sampler = ClockSampler(local)
     if world > 1:
         dist.barrier()
@@ -674,6 +690,12 @@ def run_ours(args, rank, world):
         tr = profiled_traffic(r.name)
         ent["traffic"] = tr
         ent["traffic_ratio"] = None if tr is None else round(tr / r.bytes, 4)
+        if r.kind == "nvfp4_gemm":  # a contraction: flops against the measured bf16 tensor peak
+            fl = 2.0 * r.p["M"] * r.p["K"] * r.p["N"]
+            ent["TFLOP_s"] = round(fl / us / 1e6, 1)
+            ent["b2b_TFLOP_s"] = round(fl / bus / 1e6, 1)
+            ent["frac_tensor"] = round(fl / bus / 1e6 / tensor_peak, 4)
+            ent["tensor_peak_TFLOP_s"] = tensor_peak
         if r.kind == "moe":
             ent["us_per_token"] = round(us / r.p["T"], 3)
             ent["b2b_us_per_token"] = round(bus / r.p["T"], 3)

@@ -69,8 +69,10 @@ def test_traffic_record_lookup():
         kind, p = rows[name]
         if kind == "q8_0":
             assert ent["algorithmic_bytes"] == bench.q8_0_bytes(p["M"], p["K"], p["N"])
-        elif kind.startswith("nvfp4"):
+        elif kind in ("nvfp4", "nvfp4_tiny"):
             assert ent["algorithmic_bytes"] == bench.nvfp4_bytes(p["M"], p["K"], p["N"])
+        if kind != "moe":  # every other row: the bench's own byte count of the row
+            assert ent["algorithmic_bytes"] == bench.row_bytes(kind, p, None)
         # per-call means, each rounded to a byte
         assert abs(ent["dram_bytes_per_launch"] - (ent["dram_read"] + ent["dram_write"])) <= 1
         # the hash covers the named sources in a fixed order
