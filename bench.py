@@ -104,7 +104,9 @@ def extra_rows_spec():
     SiLU * up on the 12288 x 4096 gate/up weight, I = 6144; down with the
     residual add on 4096 x 12288); the Q4_0 GEMV on the two layer shapes;
     the tensor-core prefill GEMM of the 12288 x 4096 weight over 2048
-    tokens (reported in TFLOP/s against the measured bf16 peak);
+    tokens and its grouped form over 256 experts (the MoE gate_up, 2I = 1024
+    rows, H = 2048) for 2048 tokens routed top-8 (16384 pairs, multinomial
+    expert counts), both reported in TFLOP/s against the measured bf16 peak;
     and the bf16 -> NVFP4 / Q8_0 encoders on a 12288 x 4096 weight (bytes:
     bf16 read, codes and scales written)."""
     return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1)),
@@ -113,6 +115,8 @@ def extra_rows_spec():
             ("q4_0 12288x4096 N=1", "q4_0", dict(M=12288, K=4096, N=1)),
             ("q4_0 4096x12288 N=1", "q4_0", dict(M=4096, K=12288, N=1)),
             ("nvfp4 prefill GEMM 12288x4096 T=2048", "nvfp4_gemm", dict(M=12288, K=4096, N=2048)),
+            ("nvfp4 grouped prefill GEMM E=256 1024x2048 P=16384", "nvfp4_gemm_grouped",
+             dict(E=256, M=1024, K=2048, N=16384)),
             ("nvfp4 encode 12288x4096", "nvfp4_encode", dict(M=12288, K=4096, N=1)),
             ("q8_0 encode 12288x4096", "q8_0_encode", dict(M=12288, K=4096, N=1))]
 
@@ -122,6 +126,14 @@ def host_inputs(kind, p, seed=0):
         return syn.tiny_nvfp4(seed=seed)
     if kind in ("nvfp4", "nvfp4_silu", "nvfp4_gemm"):
         return syn.dense_nvfp4(p["M"], p["K"], N=p["N"], seed=seed)
+    if kind == "nvfp4_gemm_grouped":
+        rc, rs, rx, rn = syn.streams(seed, 4)
+        E, M, K, P = p["E"], p["M"], p["K"], p["N"]
+        w = syn.nvfp4_weight(E * M, K, 0.01, rc, rs)
+        counts = rn.multinomial(P, np.ones(E) / E)
+        return {"codes": w["codes"], "scales": w["scales"], "ts": np.full(E, 0.01, dtype=np.float32),
+                "offsets": np.concatenate([[0], np.cumsum(counts)]).astype(np.int32),
+                "x": syn.bf16_normal((P, K), rx)}
     if kind in ("nvfp4_encode", "q8_0_encode"):
         return {"x": syn.bf16_normal((p["M"], p["K"]), np.random.default_rng(seed + 7))}
     if kind == "nvfp4_add":
@@ -138,6 +150,8 @@ def host_inputs(kind, p, seed=0):
 def row_bytes(kind, p, host):
     if kind in ("nvfp4", "nvfp4_tiny", "nvfp4_gemm"):
         return nvfp4_bytes(p["M"], p["K"], p["N"])
+    if kind == "nvfp4_gemm_grouped":  # every expert's weight once, the tokens, the outputs
+        return p["E"] * p["M"] * p["K"] * 9 // 16 + 2 * p["N"] * p["K"] + 4 * p["N"] * p["M"]
     if kind == "nvfp4_silu":  # the output is h, half the rows
         return nvfp4_bytes(p["M"], p["K"], p["N"]) - 4 * p["N"] * p["M"] // 2
     if kind == "nvfp4_add":  # the residual is read
@@ -300,6 +314,12 @@ class Row:
                             torch.empty(M * K // 32, dtype=torch.int16, device="cuda"))
             self.y = self.out[0]
             self.in_bytes = M * K * 2
+        elif kind == "nvfp4_gemm_grouped":
+            self.w = (d(host["codes"]), d(host["scales"]))
+            self.tse, self.offs = d(host["ts"]), d(host["offsets"])
+            self.x_host, self.x = host["x"], d(host["x"])
+            self.y = torch.empty(p["N"] * p["M"], dtype=torch.float32, device="cuda")
+            self.in_bytes = self.x.numel() * 2
         elif kind in ("nvfp4", "q8_0", "q4_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add", "nvfp4_gemm"):
             M, K, N = p["M"], p["K"], p["N"]
             if kind == "q8_0":
@@ -361,6 +381,8 @@ class Row:
             b.q4_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "nvfp4_gemm":
             b.nvfp4_gemm(w[0], w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"])
+        elif self.kind == "nvfp4_gemm_grouped":
+            b.nvfp4_gemm_grouped(w[0], w[1], self.tse, self.x, self.offs, self.y, p["E"], p["M"], p["K"], p["N"])
         else:
             T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
             b.moe_layer(self.logits, *w, self.x, self.y, self.ws, self.wsb, E, H, I, T, k)
@@ -690,7 +712,7 @@ def run_ours(args, rank, world):
         tr = profiled_traffic(r.name)
         ent["traffic"] = tr
         ent["traffic_ratio"] = None if tr is None else round(tr / r.bytes, 4)
-        if r.kind == "nvfp4_gemm":  # a contraction: flops against the measured bf16 tensor peak
+        if r.kind in ("nvfp4_gemm", "nvfp4_gemm_grouped"):  # contractions: flops against the bf16 tensor peak
             fl = 2.0 * r.p["M"] * r.p["K"] * r.p["N"]
             ent["TFLOP_s"] = round(fl / us / 1e6, 1)
             ent["b2b_TFLOP_s"] = round(fl / bus / 1e6, 1)

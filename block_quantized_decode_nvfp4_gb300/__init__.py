@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     nvfp4_dequant,
     nvfp4_encode,
     nvfp4_gemm,
+    nvfp4_gemm_grouped,
     nvfp4_gemv,
     nvfp4_gemv_add,
     nvfp4_gemv_path,

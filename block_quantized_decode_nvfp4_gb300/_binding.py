@@ -48,6 +48,7 @@ SIGNATURES = {
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "nvfp4_gemm": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "nvfp4_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp]),
     "q4_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q4_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q4_0_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
@@ -197,6 +198,11 @@ def q8_0_dequant(q, d, w, M, K, stream=None):
 def nvfp4_gemm(codes, scales, tensor_scale, x, y, M, K, T, stream=None):
     _check(lib().nvfp4_gemm(_ptr(codes), _ptr(scales), tensor_scale, _ptr(x), _ptr(y), M, K, T, _stream(stream)),
            "nvfp4_gemm")
+
+
+def nvfp4_gemm_grouped(codes, scales, tensor_scales, x, expert_offsets, y, E, M, K, P, stream=None):
+    _check(lib().nvfp4_gemm_grouped(_ptr(codes), _ptr(scales), _ptr(tensor_scales), _ptr(x), _ptr(expert_offsets),
+                                    _ptr(y), E, M, K, P, _stream(stream)), "nvfp4_gemm_grouped")
 
 
 def q4_0_gemv(codes, d, x, y, M, K, N, stream=None):

@@ -204,6 +204,27 @@ bqd_status nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float tensor_
     return from_cuda(bqd::launch_nvfp4_gemm(codes, scales, tensor_scale, x, y, M, K, T, stream));
 }
 
+bqd_status nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const float* tensor_scales,
+                              const uint16_t* x, const int32_t* expert_offsets, float* y, int E, int64_t M, int64_t K,
+                              int64_t P, cudaStream_t stream)
+{
+    if (E < 1 || M < 0 || K < 0 || P < 0 || K % 64 != 0) return BQD_ERR_SHAPE;
+    if (M > 0 && K > 0 && static_cast<int64_t>(E) * M > (int64_t(1) << 62) / K) return BQD_ERR_SHAPE;
+    if (M == 0 || P == 0) return BQD_OK;
+    if (!y) return BQD_ERR_NULL;
+    if (!aligned16(y)) return BQD_ERR_ALIGN;
+    bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    if (K == 0) return zero_output(y, M * P, stream);
+    if (!codes || !scales || !tensor_scales || !x || !expert_offsets) return BQD_ERR_NULL;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(x) ||
+        (reinterpret_cast<uintptr_t>(tensor_scales) & 3u) != 0 || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) != 0)
+        return BQD_ERR_ALIGN;
+    if (!bqd::gemm_grouped_supported(E, M, K, P)) return BQD_ERR_SHAPE;
+    return from_cuda(
+        bqd::launch_nvfp4_gemm_grouped(codes, scales, tensor_scales, expert_offsets, E, x, y, M, K, P, stream));
+}
+
 // ---------------------------------------------------------------- encoders
 bqd_status nvfp4_encode(const uint16_t* w, float tensor_scale, uint8_t* codes, uint8_t* scales, int64_t M, int64_t K,
                         cudaStream_t stream)

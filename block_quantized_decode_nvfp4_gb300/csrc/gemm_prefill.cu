@@ -53,17 +53,26 @@ namespace {
 
 constexpr int kGH = 128;                    // rows per half (MMA M)
 constexpr int kGM = 2 * kGH;                // weight rows per tile
-constexpr int kGN = 256;                    // tokens per tile (MMA N)
 constexpr int kGK = 64;                     // k per ring stage
-constexpr int kGS = 3;                      // ring stages
+constexpr int kGSMax = 3;                   // ring stages (a fourth at BN = 128 measured no faster)
 constexpr int kGDec = kGM / kWarp;          // decoder warps, one row per thread
 constexpr int kGThreads = (2 + kGDec) * kWarp;
 constexpr int kALoads = 8;                  // stages of a row's codes in flight per decoder thread
 constexpr int kAHalf = kGH * kGK * 2;       // 16 KiB of bf16
 constexpr int kAStage = 2 * kAHalf;
-constexpr int kBStage = kGN * kGK * 2;      // 32 KiB of bf16
-constexpr int kGSmem = kGS * (kAStage + kBStage) + 1024;  // + alignment slack
-constexpr int kGTmemCols = 2 * kGN;         // fp32 accumulators: half h in columns [256 h, 256 h + 256)
+// BN tokens per tile (the MMA's N): 256 for one weight matrix, 128 for the
+// experts' token segments of a grouped call (an expert of a top-8 layer over
+// 256 experts sees ~64 of 2048 tokens, so its weights are read about once). B is BN x 64 k of bf16, and the two
+// halves' fp32 accumulators take 2 BN columns of tensor memory.
+// The ring has as many stages as fit in shared memory, at most kGSMax.
+template <int BN>
+struct GemmShape {
+    static constexpr int kBStage = BN * kGK * 2;
+    static constexpr int kStages = (226 * 1024) / (kAStage + kBStage) < kGSMax ? (226 * 1024) / (kAStage + kBStage)
+                                                                              : kGSMax;
+    static constexpr int kSmem = kStages * (kAStage + kBStage) + 1024;  // + alignment slack
+    static constexpr int kTmemCols = 2 * BN;
+};
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -162,20 +171,80 @@ struct RowLoad {  // 64 k of one weight row
     uint32_t s4;
 };
 
+// Grouped form (offsets != nullptr): E experts, weights [E][M][K], tokens
+// [P][K] gathered expert-major, expert e's tokens [offsets[e],
+// offsets[e + 1]), its tensor scale ts_e[e]; grid row blockIdx.y is the
+// slot-th BN-token tile of all experts' tiles in expert order (slots past
+// the last tile do nothing). Dense form: E = 1, tokens [0, T), scale ts.
+template <int BN>
 __global__ void __launch_bounds__(kGThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ codes,
-                      const uint8_t* __restrict__ scales, float ts, float* __restrict__ y, int64_t M, int K, int T)
+                      const uint8_t* __restrict__ scales, float ts, const float* __restrict__ ts_e,
+                      const int32_t* __restrict__ offsets, int E, float* __restrict__ y, int64_t M, int K, int T)
 {
+    using S = GemmShape<BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bfull[kGS], afull[kGS], empty[kGS], dfull;
+    constexpr int kGS = S::kStages;
+    __shared__ __align__(8) uint64_t bfull[kGSMax], afull[kGSMax], empty[kGSMax], dfull;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_e, s_n0, s_nend;
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* astage = sm;
     uint8_t* bstage = sm + kGS * kAStage;
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kGM;
-    const int n0 = blockIdx.y * kGN;
     const int nk = K / kGK;
+
+    // this CTA's expert and token range [n0, nend); an empty range: nothing to
+    // do. Grouped: the experts' tile counts are scanned a block of experts at
+    // a time (one per thread), and the thread whose expert holds the slot
+    // records it.
+    __shared__ int s_wsum[kGThreads / kWarp], s_base;
+    if (threadIdx.x == 0) {
+        s_e = 0;
+        s_n0 = static_cast<int>(blockIdx.y) * BN;
+        s_nend = offsets ? s_n0 : min(s_n0 + BN, T);
+        s_base = 0;
+    }
+    __syncthreads();
+    if (offsets) {
+        const int slot = static_cast<int>(blockIdx.y);
+        for (int c0 = 0; c0 < E; c0 += kGThreads) {
+            const int x = c0 + threadIdx.x;
+            int a = 0, b = 0;
+            if (x < E) {
+                a = max(0, min(offsets[x], T));  // clamped to [0, P]
+                b = max(a, min(offsets[x + 1], T));
+            }
+            const int tiles = (b - a + BN - 1) / BN;
+            int incl = tiles;  // inclusive scan of the tile counts over the block
+#pragma unroll
+            for (int d = 1; d < kWarp; d <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if ((threadIdx.x & 31) >= d) incl += v;
+            }
+            if ((threadIdx.x & 31) == 31) s_wsum[threadIdx.x / kWarp] = incl;
+            __syncthreads();
+            int before = s_base;
+            for (int w = 0; w < static_cast<int>(threadIdx.x / kWarp); ++w) before += s_wsum[w];
+            const int first = before + incl - tiles;  // this expert's first slot
+            if (x < E && slot >= first && slot < first + tiles) {
+                s_e = x;
+                s_n0 = a + (slot - first) * BN;
+                s_nend = min(s_n0 + BN, b);
+            }
+            __syncthreads();
+            if (threadIdx.x == kGThreads - 1) s_base = before + incl;
+            __syncthreads();
+        }
+    }
+    if (s_nend <= s_n0) return;  // uniform: before any barrier, copy or tensor-memory allocation
+    const int e_cta = s_e, n0 = s_n0, nend = s_nend;
+    if (offsets) {
+        codes += static_cast<int64_t>(e_cta) * M * (K / 2);
+        scales += static_cast<int64_t>(e_cta) * M * (K / 16);
+        ts = ts_e[e_cta];
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGS; ++s) {
@@ -188,7 +257,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                     "r"(kGTmemCols)
+                     "r"(S::kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -207,14 +276,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int st = s % kGS;
                 if (s >= kGS) ok = mbar_wait(&empty[st], static_cast<uint32_t>(((s / kGS) & 1) ^ 1), &g_gemm_error);
                 if (!ok) break;
-                mbar_arrive_expect_tx(&bfull[st], kBStage);
-                tma_load_2d(bstage + st * kBStage, &map_x, s * kGK, n0, &bfull[st]);
+                mbar_arrive_expect_tx(&bfull[st], S::kBStage);
+                tma_load_2d(bstage + st * S::kBStage, &map_x, s * kGK, n0, &bfull[st]);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue
-        const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(kGN >> 3) << 17) |
+        const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
                                (static_cast<uint32_t>(kGH >> 4) << 24);  // f32 D, bf16 A and B, N, M
         for (int s = 0; s < nk && ok; ++s) {
             const int st = s % kGS;
@@ -223,14 +292,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
             if (!ok) break;
             tc_fence_after();
             if (elect_one()) {
-                const uint32_t a0 = smem_u32(astage + st * kAStage), b0 = smem_u32(bstage + st * kBStage);
+                const uint32_t a0 = smem_u32(astage + st * kAStage), b0 = smem_u32(bstage + st * S::kBStage);
 #pragma unroll
                 for (int j = 0; j < kGK / 16; ++j) {  // 16 k = two 8-k groups of A, 32 bytes of B's rows
                     const uint64_t bd = smem_desc_sw128(b0 + 32 * j);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const uint64_t ad = smem_desc(a0 + h * kAHalf + 2 * j * (kGH * 16), kGH * 16, 128);
-                        mma_ss(tmem + h * kGN, ad, bd, idesc, (s | j) != 0 ? 1u : 0u);
+                        mma_ss(tmem + h * BN, ad, bd, idesc, (s | j) != 0 ? 1u : 0u);
                     }
                 }
                 mma_commit(&empty[st]);  // the stage is free once these MMAs have read it
@@ -294,14 +363,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (ok) {
             const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
 #pragma unroll 1
-            for (int c = 0; c < kGN / 16; ++c) {
+            for (int c = 0; c < BN / 16; ++c) {
                 uint32_t v[16];
-                tmem_ld_x16(tmem + lane_base + hf * kGN + 16 * c, v);
+                tmem_ld_x16(tmem + lane_base + hf * BN + 16 * c, v);
                 if (live) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int n = n0 + 16 * c + j;
-                        if (n < T) y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[j]) * ts;
+                        if (n < nend) y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[j]) * ts;
                     }
                 }
             }
@@ -311,7 +380,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGTmemCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(S::kTmemCols)
+                     : "memory");
     }
 }
 
@@ -337,45 +407,76 @@ EncodeTiledFn encode_fn()
 
 }  // namespace
 
-bool gemm_supported(int64_t M, int64_t K, int64_t T)
-{
-    return M >= 1 && K >= kGK && K % kGK == 0 && K <= (int64_t(1) << 24) && T >= 1 && T <= (int64_t(1) << 24) &&
-           M <= (int64_t(1) << 31) && (M + kGM - 1) / kGM <= 0x7FFFFFFF && (T + kGN - 1) / kGN <= 65535;
-}
+namespace {
 
-cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
-                              int64_t M, int64_t K, int64_t T, cudaStream_t s)
+// x [P][K] bf16, read in boxes of 64 k x BN tokens (128 bytes a token,
+// 128-byte swizzle); tokens past P read as zero.
+bool make_x_map(CUtensorMap* map, const uint16_t* x, int64_t K, int64_t P, int bn)
 {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    // x [T][K] bf16, read in boxes of 64 k x 256 tokens (128 bytes a token,
-    // 128-byte swizzle); tokens past T read as zero
-    CUtensorMap map;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(P)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGK), static_cast<cuuint32_t>(kGN)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kGK), static_cast<cuuint32_t>(bn)};
     const cuuint32_t estr[2] = {1, 1};
-    if (fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+cudaError_t launch_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const float* ts_e,
+                        const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M, int64_t K, int64_t P,
+                        int64_t tiles, cudaStream_t s)
+{
+    CUtensorMap map;
+    if (!make_x_map(&map, x, K, P, BN)) return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    auto kern = nvfp4_gemm_kernel<BN>;
     static OccCache occ;
-    blocks_per_sm(occ, reinterpret_cast<const void*>(nvfp4_gemm_kernel), dev, kGThreads, kGSmem);
+    blocks_per_sm(occ, reinterpret_cast<const void*>(kern), dev, kGThreads, GemmShape<BN>::kSmem);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((M + kGM - 1) / kGM), static_cast<unsigned>((T + kGN - 1) / kGN));
+    cfg.gridDim = dim3(static_cast<unsigned>((M + kGM - 1) / kGM), static_cast<unsigned>(tiles));
     cfg.blockDim = dim3(kGThreads);
-    cfg.dynamicSmemBytes = kGSmem;
+    cfg.dynamicSmemBytes = GemmShape<BN>::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = launch_flags() & kLaunchPdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, map, codes, scales, ts, y, M, static_cast<int>(K),
-                              static_cast<int>(T));
+    return cudaLaunchKernelEx(&cfg, kern, map, codes, scales, ts, ts_e, offsets, E, y, M, static_cast<int>(K),
+                              static_cast<int>(P));
+}
+
+}  // namespace
+
+bool gemm_supported(int64_t M, int64_t K, int64_t T)
+{
+    return M >= 1 && K >= kGK && K % kGK == 0 && K <= (int64_t(1) << 24) && T >= 1 && T <= (int64_t(1) << 24) &&
+           M <= (int64_t(1) << 31) && (M + kGM - 1) / kGM <= 0x7FFFFFFF && (T + 255) / 256 <= 65535;
+}
+
+bool gemm_grouped_supported(int64_t E, int64_t M, int64_t K, int64_t P)
+{
+    return E >= 1 && E <= 65535 && M >= 1 && K >= kGK && K % kGK == 0 && K <= (int64_t(1) << 24) && P >= 1 &&
+           P <= (int64_t(1) << 24) && E * M <= (int64_t(1) << 31) && (P + 127) / 128 + E <= 65535;
+}
+
+cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
+                              int64_t M, int64_t K, int64_t T, cudaStream_t s)
+{
+    return launch_gemm<256>(codes, scales, ts, nullptr, nullptr, 1, x, y, M, K, T, (T + 255) / 256, s);
+}
+
+cudaError_t launch_nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const float* ts,
+                                      const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M,
+                                      int64_t K, int64_t P, cudaStream_t s)
+{
+    // tile slots: sum over experts of ceil(n_e / 128) <= P / 128 + E
+    return launch_gemm<128>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 127) / 128 + E, s);
 }
 
 cudaError_t read_and_clear_gemm_error(unsigned int* out)

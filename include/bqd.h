@@ -307,6 +307,25 @@ bqd_status q4_0_gemv_path(const uint8_t* codes, const uint16_t* d, const uint16_
 bqd_status nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x, float* y,
                       int64_t M, int64_t K, int64_t T, cudaStream_t stream);
 
+/*
+ * nvfp4_gemm_grouped -- the per-expert variable-grid form of nvfp4_gemm for
+ * a MoE prefill ("Vemloir/LumenLLM" README, Kernels bullet): for every
+ * expert e and every gathered token p in [offsets[e], offsets[e + 1]),
+ *   Y[p][m] = ts[e] * sum_k e2m1(c[e][m][k]) * e4m3(s[e][m][k/16]) * x[p][k].
+ *   codes u8 [E][M][K/2]; scales u8 [E][M][K/16]; tensor_scales fp32 [E]
+ *   (device); x bf16 bits [P][K], the routed tokens gathered expert-major;
+ *   expert_offsets int32 [E + 1] (device), 0 = offsets[0] <= ... <=
+ *   offsets[E] = P; y fp32 [P][M]. K % 64 == 0, E >= 1; M == 0 or P == 0:
+ *   BQD_OK without touching the GPU; K == 0: y set to zero. codes, scales,
+ *   x, y 16-byte aligned; tensor_scales and expert_offsets 4-byte aligned.
+ *   One launch: tiles of 256 weight rows x 128 of an expert's tokens. Offsets
+ *   outside [0, P] are clamped (no access leaves the arrays; the outputs of
+ *   such a call are unspecified).
+ */
+bqd_status nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const float* tensor_scales,
+                              const uint16_t* x, const int32_t* expert_offsets, float* y, int E, int64_t M, int64_t K,
+                              int64_t P, cudaStream_t stream);
+
 /* q4_0_dequant -- w[m][k] = fp16(d[m][k/32]) * (q[m][k] - 8) (exact in
  * fp32); layout and shape rules as q4_0_gemv. */
 bqd_status q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64_t M, int64_t K,

@@ -77,3 +77,63 @@ def test_edge_cases_and_rejections():
         bqd.nvfp4_gemm(dev(w["codes"]), dev(w["scales"]), 1.0, dev(w["x"]).data_ptr() + 2, Guarded(256).ptr, 64,
                        128, 4)
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- grouped (per-expert) form
+def _grouped_case(E, M, K, counts, seed):
+    rng = np.random.default_rng(seed)
+    ws = [syn.dense_nvfp4(M, K, N=1, seed=seed + e) for e in range(E)]
+    codes = np.stack([w["codes"] for w in ws])
+    scales = np.stack([w["scales"] for w in ws])
+    ts = np.array([0.01 * (1 + e / 7) for e in range(E)], dtype=np.float32)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    P = int(offsets[-1])
+    x = syn.bf16_normal((P, K), rng)
+    return codes, scales, ts, offsets, x, P
+
+
+def run_grouped(codes, scales, ts, offsets, x, E, M, K, P):
+    out = Guarded(P * M)
+    bqd.nvfp4_gemm_grouped(dev(codes), dev(scales), dev(ts), dev(x), dev(offsets), out.ptr, E, M, K, P)
+    return out.get().reshape(P, M)
+
+
+@pytest.mark.parametrize("E,M,K,counts", [
+    (8, 384, 1024, [0, 1, 63, 64, 65, 200, 3, 130]),
+    (3, 256, 64, [17, 0, 300]),
+    (1, 100, 512, [129]),
+])
+def test_grouped_matches_oracle_per_expert(E, M, K, counts):
+    codes, scales, ts, offsets, x, P = _grouped_case(E, M, K, counts, seed=E * 10 + K)
+    y = run_grouped(codes, scales, ts, offsets, x, E, M, K, P)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if a == b:
+            continue
+        ref, tol = oracle.nvfp4_gemv(codes[e], scales[e], ts[e], x[a:b], M, K)
+        assert_within(y[a:b], ref, tol, f"expert {e}")
+
+
+def test_grouped_moe_gate_up_shape_sampled():
+    # the MoE layer's gate_up (2I = 1024 rows, H = 2048) over 32 experts and
+    # 2048 routed pairs of uneven sizes, sampled rows of every expert
+    E, M, K = 32, 1024, 2048
+    counts = np.random.default_rng(5).multinomial(2048, np.ones(E) / E)
+    codes, scales, ts, offsets, x, P = _grouped_case(E, M, K, counts, seed=3)
+    y = run_grouped(codes, scales, ts, offsets, x, E, M, K, P)
+    rows = np.array([0, 1, 255, 256, 511, 777, 1023])
+    for e in range(0, E, 5):
+        a, b = offsets[e], offsets[e + 1]
+        ref, tol = oracle.nvfp4_gemv(codes[e], scales[e], ts[e], x[a:b], M, K, rows=rows)
+        assert_within(y[a:b][:, rows], ref, tol, f"expert {e}")
+    y2 = run_grouped(codes, scales, ts, offsets, x, E, M, K, P)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+def test_grouped_rejections():
+    codes, scales, ts, offsets, x, P = _grouped_case(2, 128, 128, [3, 4], seed=1)
+    with pytest.raises(bqd.BqdError):  # K % 64 != 0
+        run_grouped(codes, scales, ts, offsets, x, 2, 128, 96, P)
+    with pytest.raises(bqd.BqdError):  # E = 0
+        bqd.nvfp4_gemm_grouped(dev(codes), dev(scales), dev(ts), dev(x), dev(offsets), Guarded(P * 128).ptr, 0, 128,
+                               128, P)
