@@ -25,6 +25,8 @@ from ._binding import (  # noqa: F401
     moe_grouped_gemv_noalloc,
     moe_layer,
     moe_layer_workspace_bytes,
+    moe_prefill_layer,
+    moe_prefill_workspace_bytes,
     moe_route_topk,
     moe_workspace_bytes,
     nvfp4_dequant,

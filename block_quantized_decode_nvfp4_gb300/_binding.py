@@ -48,6 +48,8 @@ SIGNATURES = {
     "q8_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q8_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "nvfp4_gemm": (_i32, [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "moe_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "moe_prefill_layer": (_i32, [_vp] * 10 + [_sz, _i32, _i32, _i32, _i32, _i32, _vp]),
     "nvfp4_gemm_grouped": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i64, _vp]),
     "q4_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q4_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
@@ -203,6 +205,17 @@ def nvfp4_gemm(codes, scales, tensor_scale, x, y, M, K, T, stream=None):
 def nvfp4_gemm_grouped(codes, scales, tensor_scales, x, expert_offsets, y, E, M, K, P, stream=None):
     _check(lib().nvfp4_gemm_grouped(_ptr(codes), _ptr(scales), _ptr(tensor_scales), _ptr(x), _ptr(expert_offsets),
                                     _ptr(y), E, M, K, P, _stream(stream)), "nvfp4_gemm_grouped")
+
+
+def moe_prefill_workspace_bytes(T, topk, H, I, E):
+    return int(lib().moe_prefill_workspace_bytes(T, topk, H, I, E))
+
+
+def moe_prefill_layer(logits, gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x, y, workspace,
+                      workspace_bytes, E, H, I, T, topk, stream=None):
+    _check(lib().moe_prefill_layer(_ptr(logits), _ptr(gu_codes), _ptr(gu_scales), _ptr(gu_ts), _ptr(dn_codes),
+                                   _ptr(dn_scales), _ptr(dn_ts), _ptr(x), _ptr(y), _ptr(workspace), workspace_bytes,
+                                   E, H, I, T, topk, _stream(stream)), "moe_prefill_layer")
 
 
 def q4_0_gemv(codes, d, x, y, M, K, N, stream=None):

@@ -225,6 +225,37 @@ bqd_status nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const
         bqd::launch_nvfp4_gemm_grouped(codes, scales, tensor_scales, expert_offsets, E, x, y, M, K, P, stream));
 }
 
+size_t moe_prefill_workspace_bytes(int T, int topk, int H, int I, int E)
+{
+    if (T < 1 || topk < 1 || H < 1 || I < 1 || E < 1) return 0;
+    return bqd::moe_prefill_workspace_size(T, topk, H, I, E);
+}
+
+bqd_status moe_prefill_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales,
+                             const float* gu_ts, const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts,
+                             const uint16_t* x, float* y, void* workspace, size_t workspace_bytes, int E, int H, int I,
+                             int T, int topk, cudaStream_t stream)
+{
+    if (T < 1 || E < 1 || E > bqd::kMoeMaxExperts || topk < 1 || topk > E || topk > bqd::kMoeMaxTopk ||
+        static_cast<int64_t>(T) * topk > bqd::kMoeMaxPairs || H < 64 || H % 64 != 0 || I < 64 || I % 64 != 0 ||
+        H > (1 << 16) || I > (1 << 16))
+        return BQD_ERR_SHAPE;
+    if (!logits || !gu_codes || !gu_scales || !gu_ts || !dn_codes || !dn_scales || !dn_ts || !x || !y)
+        return BQD_ERR_NULL;
+    if (!workspace || workspace_bytes < bqd::moe_prefill_workspace_size(T, topk, H, I, E)) return BQD_ERR_WORKSPACE;
+    for (const void* p : {static_cast<const void*>(logits), static_cast<const void*>(gu_codes),
+                          static_cast<const void*>(gu_scales), static_cast<const void*>(dn_codes),
+                          static_cast<const void*>(dn_scales), static_cast<const void*>(x), static_cast<const void*>(y),
+                          static_cast<const void*>(workspace)})
+        if (!aligned16(p)) return BQD_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(gu_ts) & 3u) != 0 || (reinterpret_cast<uintptr_t>(dn_ts) & 3u) != 0)
+        return BQD_ERR_ALIGN;
+    const bqd_status st = check_arch();
+    if (st != BQD_OK) return st;
+    return from_cuda(bqd::launch_moe_prefill_layer(logits, gu_codes, gu_scales, gu_ts, dn_codes, dn_scales, dn_ts, x,
+                                                   y, workspace, E, H, I, T, topk, stream));
+}
+
 // ---------------------------------------------------------------- encoders
 bqd_status nvfp4_encode(const uint16_t* w, float tensor_scale, uint8_t* codes, uint8_t* scales, int64_t M, int64_t K,
                         cudaStream_t stream)

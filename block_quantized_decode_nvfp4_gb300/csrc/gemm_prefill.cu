@@ -180,7 +180,8 @@ template <int BN>
 __global__ void __launch_bounds__(kGThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ codes,
                       const uint8_t* __restrict__ scales, float ts, const float* __restrict__ ts_e,
-                      const int32_t* __restrict__ offsets, int E, float* __restrict__ y, int64_t M, int K, int T)
+                      const int32_t* __restrict__ offsets, int E, float* __restrict__ y, int64_t M, int K, int T,
+                      int accumulate)
 {
     using S = GemmShape<BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -370,7 +371,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int n = n0 + 16 * c + j;
-                        if (n < nend) y[static_cast<int64_t>(n) * M + m] = __uint_as_float(v[j]) * ts;
+                        if (n < nend) {
+                            float* o = y + static_cast<int64_t>(n) * M + m;
+                            *o = accumulate ? *o + __uint_as_float(v[j]) * ts : __uint_as_float(v[j]) * ts;
+                        }
                     }
                 }
             }
@@ -427,7 +431,7 @@ bool make_x_map(CUtensorMap* map, const uint16_t* x, int64_t K, int64_t P, int b
 template <int BN>
 cudaError_t launch_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const float* ts_e,
                         const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M, int64_t K, int64_t P,
-                        int64_t tiles, cudaStream_t s)
+                        int64_t tiles, int accumulate, cudaStream_t s)
 {
     CUtensorMap map;
     if (!make_x_map(&map, x, K, P, BN)) return cudaErrorInvalidValue;
@@ -448,7 +452,7 @@ cudaError_t launch_gemm(const uint8_t* codes, const uint8_t* scales, float ts, c
     cfg.attrs = attr;
     cfg.numAttrs = launch_flags() & kLaunchPdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, map, codes, scales, ts, ts_e, offsets, E, y, M, static_cast<int>(K),
-                              static_cast<int>(P));
+                              static_cast<int>(P), accumulate);
 }
 
 }  // namespace
@@ -468,15 +472,16 @@ bool gemm_grouped_supported(int64_t E, int64_t M, int64_t K, int64_t P)
 cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
                               int64_t M, int64_t K, int64_t T, cudaStream_t s)
 {
-    return launch_gemm<256>(codes, scales, ts, nullptr, nullptr, 1, x, y, M, K, T, (T + 255) / 256, s);
+    return launch_gemm<256>(codes, scales, ts, nullptr, nullptr, 1, x, y, M, K, T, (T + 255) / 256, 0, s);
 }
 
 cudaError_t launch_nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const float* ts,
                                       const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M,
-                                      int64_t K, int64_t P, cudaStream_t s)
+                                      int64_t K, int64_t P, cudaStream_t s, bool accumulate)
 {
     // tile slots: sum over experts of ceil(n_e / 128) <= P / 128 + E
-    return launch_gemm<128>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 127) / 128 + E, s);
+    return launch_gemm<128>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 127) / 128 + E,
+                            accumulate ? 1 : 0, s);
 }
 
 cudaError_t read_and_clear_gemm_error(unsigned int* out)

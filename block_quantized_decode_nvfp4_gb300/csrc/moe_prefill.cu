@@ -1,0 +1,159 @@
+// moe_prefill.cu -- a routed MoE layer for many tokens (prefill) around the
+// grouped tensor-core GEMM: the pages' grouped-MoE prefill with a per-expert
+// variable-grid NVFP4 GEMM ("Vemloir/LumenLLM" README, Kernels bullet;
+// "robertbfuentes7-cloud/bw24" README, MoE bullet: experts decoded once for
+// all their tokens).
+//
+// The layer computes what the small-batch and stream paths compute (softmax
+// top-k routing, h = SiLU(gate) * up per (token, slot), y_t = sum over the
+// slots of w * (W_dn . h), slots added in order 0 .. topk - 1):
+//  1. the route kernel writes the expert-major pair list;
+//  2. a gather copies every pair's token row, expert-major, and records the
+//     pair of each (token, slot);
+//  3. the grouped GEMM gives gate and up of every pair: G [P][2I];
+//  4. h = SiLU(g) * u in fp32, split into two bf16 parts hi = bf16(h) and
+//     lo = bf16(h - hi), whose sum holds h to ~2^-17 of its size (a single
+//     bf16 operand would round h by up to 2^-9, beyond the tolerance);
+//  5. the grouped GEMM of W_dn with hi, then with lo accumulated: D [P][H];
+//  6. the combine adds each token's slots in order, weighted.
+// Every product inside the GEMMs is exact; the sums are fp32.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "gemv.h"
+
+namespace bqd {
+
+namespace {
+
+constexpr size_t al256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
+
+struct PrefillWs {
+    int32_t *offsets, *pair_token, *pair_slot, *inv;
+    float* pair_weight;
+    uint16_t *xg, *hhi, *hlo;
+    float *gu, *d;
+};
+
+PrefillWs carve(void* base, int T, int topk, int H, int I, int E, size_t* total)
+{
+    const size_t P = static_cast<size_t>(T) * topk;
+    uint8_t* p = static_cast<uint8_t*>(base);
+    size_t o = 0;
+    PrefillWs w{};
+    auto take = [&](size_t bytes) {
+        uint8_t* r = p ? p + o : nullptr;
+        o += al256(bytes);
+        return r;
+    };
+    w.offsets = reinterpret_cast<int32_t*>(take((static_cast<size_t>(E) + 1) * 4));
+    w.pair_token = reinterpret_cast<int32_t*>(take(P * 4));
+    w.pair_weight = reinterpret_cast<float*>(take(P * 4));
+    w.pair_slot = reinterpret_cast<int32_t*>(take(P * 4));
+    w.inv = reinterpret_cast<int32_t*>(take(P * 4));
+    w.xg = reinterpret_cast<uint16_t*>(take(P * H * 2));
+    w.gu = reinterpret_cast<float*>(take(P * 2 * I * 4));
+    w.hhi = reinterpret_cast<uint16_t*>(take(P * I * 2));
+    w.hlo = reinterpret_cast<uint16_t*>(take(P * I * 2));
+    w.d = reinterpret_cast<float*>(take(P * H * 4));
+    if (total) *total = o;
+    return w;
+}
+
+// Pair p's token row, 16 bytes per thread; and inv[(token, slot)] = p.
+__global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pair_token,
+                              const int32_t* __restrict__ pair_slot, uint16_t* __restrict__ xg,
+                              int32_t* __restrict__ inv, int P, int H, int T, int topk)
+{
+    const int per = H / 8;  // 16-byte pieces a row
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < static_cast<int64_t>(P) * per;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int p = static_cast<int>(i / per), c = static_cast<int>(i % per);
+        const int t = min(max(pair_token[p], 0), T - 1);
+        reinterpret_cast<uint4*>(xg)[i] = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * H)[c];
+        if (c == 0) {
+            const int s = pair_slot[p];
+            if (pair_token[p] >= 0 && pair_token[p] < T && s >= 0 && s < topk) inv[pair_token[p] * topk + s] = p;
+        }
+    }
+}
+
+// h = SiLU(g) * u, g = G[p][i], u = G[p][I + i]; hi = bf16(h), lo = bf16(h - hi).
+__global__ void silu_split_kernel(const float* __restrict__ gu, uint16_t* __restrict__ hhi,
+                                  uint16_t* __restrict__ hlo, int P, int I)
+{
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < static_cast<int64_t>(P) * I;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t p = i / I, k = i % I;
+        const float g = gu[p * 2 * I + k], u = gu[p * 2 * I + I + k];
+        const float h = g / (1.0f + expf(-g)) * u;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
+        hhi[i] = __bfloat16_as_ushort(hi);
+        hlo[i] = __bfloat16_as_ushort(lo);
+    }
+}
+
+// y[t][j] = sum over s = 0 .. topk - 1 of w(t, s) * D[pair(t, s)][j].
+__global__ void combine_kernel(const float* __restrict__ d, const float* __restrict__ pair_weight,
+                               const int32_t* __restrict__ inv, float* __restrict__ y, int T, int H, int topk, int P)
+{
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < static_cast<int64_t>(T) * H;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / H, j = i % H;
+        float acc = 0.f;
+        for (int s = 0; s < topk; ++s) {
+            const int p = inv[t * topk + s];  // every (token, slot) has one pair; the check keeps reads in bounds
+            if (p >= 0 && p < P) acc += pair_weight[p] * d[static_cast<int64_t>(p) * H + j];
+        }
+        y[i] = acc;
+    }
+}
+
+unsigned grid_for(int64_t work)
+{
+    int64_t g = (work + 255) / 256;
+    if (g > 152 * 8) g = 152 * 8;
+    return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+size_t moe_prefill_workspace_size(int T, int topk, int H, int I, int E)
+{
+    size_t total = 0;
+    carve(nullptr, T, topk, H, I, E, &total);
+    return total;
+}
+
+cudaError_t launch_moe_prefill_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales,
+                                     const float* gu_ts, const uint8_t* dn_codes, const uint8_t* dn_scales,
+                                     const float* dn_ts, const uint16_t* x, float* y, void* ws, int E, int H, int I,
+                                     int T, int topk, cudaStream_t s)
+{
+    const int P = T * topk;
+    const PrefillWs w = carve(ws, T, topk, H, I, E, nullptr);
+    cudaError_t e = launch_moe_route(logits, T, E, topk, w.offsets, w.pair_token, w.pair_weight, w.pair_slot, s);
+    if (e != cudaSuccess) return e;
+    gather_kernel<<<grid_for(static_cast<int64_t>(P) * H / 8), 256, 0, s>>>(x, w.pair_token, w.pair_slot, w.xg,
+                                                                            w.inv, P, H, T, topk);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_nvfp4_gemm_grouped(gu_codes, gu_scales, gu_ts, w.offsets, E, w.xg, w.gu, 2 * static_cast<int64_t>(I),
+                                  H, P, s);
+    if (e != cudaSuccess) return e;
+    silu_split_kernel<<<grid_for(static_cast<int64_t>(P) * I), 256, 0, s>>>(w.gu, w.hhi, w.hlo, P, I);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_nvfp4_gemm_grouped(dn_codes, dn_scales, dn_ts, w.offsets, E, w.hhi, w.d, H, I, P, s);
+    if (e != cudaSuccess) return e;
+    e = launch_nvfp4_gemm_grouped(dn_codes, dn_scales, dn_ts, w.offsets, E, w.hlo, w.d, H, I, P, s, true);
+    if (e != cudaSuccess) return e;
+    combine_kernel<<<grid_for(static_cast<int64_t>(T) * H), 256, 0, s>>>(w.d, w.pair_weight, w.inv, y, T, H, topk,
+                                                                         P);
+    return cudaGetLastError();
+}
+
+}  // namespace bqd

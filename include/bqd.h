@@ -326,6 +326,28 @@ bqd_status nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const
                               const uint16_t* x, const int32_t* expert_offsets, float* y, int E, int64_t M, int64_t K,
                               int64_t P, cudaStream_t stream);
 
+/*
+ * moe_prefill_layer -- the routed MoE layer of moe_layer for many tokens
+ * (prefill), on the tensor cores: routing as moe_route_topk, the routed
+ * tokens gathered expert-major, gate/up of every (token, slot) pair by
+ * nvfp4_gemm_grouped, h = SiLU(gate) * up in fp32, the down projection by
+ * nvfp4_gemm_grouped on h split into two bf16 parts (bf16(h) and the bf16
+ * of the rest, so h is kept to ~2^-17 of its size), and y_t = sum over the
+ * slots s = 0 .. topk - 1 of w(t, s) * down (in slot order; deterministic).
+ * ("Vemloir/LumenLLM" README, Kernels bullet: NVFP4 grouped-MoE prefill.)
+ *   Layout and meaning of logits, the weights, tensor scales, x and y as
+ *   moe_layer; workspace of moe_prefill_workspace_bytes(T, topk, H, I, E)
+ *   bytes, 16-byte aligned (about T * topk * (6 H + 12 I) bytes).
+ *   T * topk <= 8192, topk <= min(E, 32), E <= 1024, H and I multiples of 64
+ *   (up to 65536); else BQD_ERR_SHAPE. A too small workspace:
+ *   BQD_ERR_WORKSPACE. Pointers 16-byte aligned (the tensor scales 4).
+ */
+size_t moe_prefill_workspace_bytes(int T, int topk, int H, int I, int E);
+bqd_status moe_prefill_layer(const float* logits, const uint8_t* gu_codes, const uint8_t* gu_scales,
+                             const float* gu_ts, const uint8_t* dn_codes, const uint8_t* dn_scales, const float* dn_ts,
+                             const uint16_t* x, float* y, void* workspace, size_t workspace_bytes, int E, int H, int I,
+                             int T, int topk, cudaStream_t stream);
+
 /* q4_0_dequant -- w[m][k] = fp16(d[m][k/32]) * (q[m][k] - 8) (exact in
  * fp32); layout and shape rules as q4_0_gemv. */
 bqd_status q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64_t M, int64_t K,
