@@ -17,6 +17,10 @@ of 9B-dense layer shapes, a Q8_0 LM head, speculative-verify widths and a
 * Q8_0 weight: int8 uniform in [-127, 127]; one fp16 scale per 32 consecutive
   k of a row, uniform in [1e-4, 1e-2] and rounded to fp16. Stored planar
   (a q plane and a d plane), not as interleaved 34-byte blocks.
+* FP8 block-128 weight: E4M3 codes of N(0, 1) * 112 draws (a tile's
+  largest |value| lands near the format's 448, as in checkpoints scaled per
+  tile), rounded to E4M3; one fp32 scale per 128 x 128 tile, log2-uniform
+  over [2^-14, 2^-8].
 * Activations: bf16 ~ N(0, 1). Router logits: fp32 ~ N(0, 1).
 
 Every tensor gets its own child stream of ``numpy.random.SeedSequence(seed)``
@@ -33,16 +37,19 @@ __all__ = [
     "nvfp4_weight",
     "q8_0_weight",
     "q4_0_weight",
+    "fp8_b128_weight",
     "bf16_normal",
     "router_logits",
     "tiny_nvfp4",
     "dense_nvfp4",
     "dense_q8_0",
     "dense_q4_0",
+    "dense_fp8_b128",
     "moe_layer",
     "NVFP4_SHAPES",
     "Q8_0_SHAPES",
     "Q4_0_SHAPES",
+    "FP8_B128_SHAPES",
     "VERIFY_SHAPES",
 ]
 
@@ -52,6 +59,8 @@ NVFP4_SHAPES = [(12288, 4096), (4096, 12288), (4096, 4096)]
 Q8_0_SHAPES = [(12288, 4096), (4096, 12288), (151936, 4096)]
 # (M, K) of the Q4_0 weights (gate/up, down).
 Q4_0_SHAPES = [(12288, 4096), (4096, 12288)]
+# (M, K) of the FP8 block-128 weights (gate/up, down).
+FP8_B128_SHAPES = [(12288, 4096), (4096, 12288)]
 # (M, K) of the speculative-verify weights; N in {4, 8}.
 VERIFY_SHAPES = [(4096, 4096), (12288, 4096)]
 
@@ -100,6 +109,15 @@ def q4_0_weight(M: int, K: int, rng_c, rng_d) -> dict:
     return {"codes": codes, "d": d, "M": M, "K": K}
 
 
+def fp8_b128_weight(M: int, K: int, rng_c, rng_s) -> dict:
+    """FP8 block-128 planes: codes u8[M][K] (E4M3 bytes, row-major), scales
+    f32[ceil(M/128)][ceil(K/128)]."""
+    codes = _to_e4m3_bytes(np.clip(rng_c.standard_normal(size=(M, K), dtype=np.float32) * 112.0, -448.0, 448.0))
+    log2s = rng_s.uniform(-14.0, -8.0, size=((M + 127) // 128, (K + 127) // 128))
+    scales = np.exp2(log2s).astype(np.float32)
+    return {"codes": codes, "scales": scales, "M": M, "K": K}
+
+
 def bf16_normal(shape, rng) -> np.ndarray:
     """bf16 bits of N(0,1) draws (fp32 draw, then round-to-nearest-even)."""
     return _to_bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
@@ -142,6 +160,14 @@ def dense_q4_0(M: int, K: int, N: int = 1, seed: int = 0) -> dict:
     """Q4_0 weight with N bf16 columns. Streams: 0 codes, 1 d, 2 x."""
     rc, rd, rx = streams(seed, 3)
     w = q4_0_weight(M, K, rc, rd)
+    w["x"] = bf16_normal((N, K), rx)
+    return w
+
+
+def dense_fp8_b128(M: int, K: int, N: int = 1, seed: int = 0) -> dict:
+    """FP8 block-128 weight with N bf16 columns. Streams: 0 codes, 1 scales, 2 x."""
+    rc, rs, rx = streams(seed, 3)
+    w = fp8_b128_weight(M, K, rc, rs)
     w["x"] = bf16_normal((N, K), rx)
     return w
 

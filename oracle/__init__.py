@@ -40,6 +40,9 @@ def lib():
             ("oracle_q4_0_dequant_f64", None, [u8p, u16p, i64, i64, f64p]),
             ("oracle_q4_0_dequant_f32", None, [u8p, u16p, i64, i64, f32p]),
             ("oracle_q4_0_gemv", None, [u8p, u16p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
+            ("oracle_fp8_b128_dequant_f64", None, [u8p, f32p, i64, i64, f64p]),
+            ("oracle_fp8_b128_dequant_f32", None, [u8p, f32p, i64, i64, f32p]),
+            ("oracle_fp8_b128_gemv", None, [u8p, f32p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
             ("oracle_moe_route", None, [f32p, i64, i64, i64, i32p, f64p]),
             ("oracle_moe_layer", None, [u8p, u8p, f32p, u8p, u8p, f32p, u16p, i32p, f64p,
                                         i64, i64, i64, i64] + [f64p] * 8),
@@ -113,6 +116,18 @@ def q4_0_dequant(codes, d, M, K, dtype=np.float64):
     return w
 
 
+def fp8_b128_dequant(codes, scales, M, K, dtype=np.float64):
+    """FP8 block-128 weight [M][K]: e4m3(code) * the fp32 scale of the
+    128 x 128 tile holding the element (scales [ceil(M/128)][ceil(K/128)])."""
+    codes, scales = _c(codes, np.uint8), _c(scales, np.float32)
+    w = np.empty((M, K), dtype=dtype)
+    if dtype == np.float64:
+        lib().oracle_fp8_b128_dequant_f64(_p(codes, C.c_uint8), _p(scales, C.c_float), M, K, _p(w, C.c_double))
+    else:
+        lib().oracle_fp8_b128_dequant_f32(_p(codes, C.c_uint8), _p(scales, C.c_float), M, K, _p(w, C.c_float))
+    return w
+
+
 # ---------------------------------------------------------------- GEMV
 def nvfp4_gemv(codes, scales, ts, x, M, K, rows=None):
     """(y, a) as fp64 arrays [N][len(rows) or M]; x is bf16 bits [N][K]."""
@@ -161,6 +176,19 @@ def q4_0_gemv(codes, d, x, M, K, rows=None):
     lib().oracle_q4_0_gemv(_p(codes, C.c_uint8), _p(d, C.c_uint16), _p(x, C.c_uint16), M, K, N,
                            _p(r, C.c_int64), 0 if r is None else len(r),
                            _p(y, C.c_double), _p(a, C.c_double))
+    return y, a
+
+
+def fp8_b128_gemv(codes, scales, x, M, K, rows=None):
+    codes, scales = _c(codes, np.uint8), _c(scales, np.float32)
+    x = _c(x, np.uint16).reshape(-1, K)
+    N = x.shape[0]
+    r = None if rows is None else _c(rows, np.int64)
+    R = M if r is None else len(r)
+    y = np.empty((N, R)); a = np.empty((N, R))
+    lib().oracle_fp8_b128_gemv(_p(codes, C.c_uint8), _p(scales, C.c_float), _p(x, C.c_uint16), M, K, N,
+                               _p(r, C.c_int64), 0 if r is None else len(r),
+                               _p(y, C.c_double), _p(a, C.c_double))
     return y, a
 
 

@@ -18,6 +18,10 @@
  *  - "avifenesh/memra" README, Decode kernels bullet: NVFP4 / Q4_0 / Q8_0
  *    matvecs; "robertbfuentes7-cloud/bw24" README, GGUF bullet: files mix
  *    BF16, Q8_0, Q4_0, Q4_1 and the K-quants.
+ *  - "Vemloir/LumenLLM" README, Quantization bullet: FP8 (E4M3) weights
+ *    beside NVFP4; "avifenesh/memra" README, Loaders bullet: FP8 checkpoints
+ *    quantised in blocks of 128 (one scale per 128 x 128 tile of the weight,
+ *    the scale multiplying the E4M3 value).
  *  The pages never print the bit layouts. The element formats are the public
  *  closed forms: E2M1 and E4M3 from the OCP Microscaling (MX) v1.0 and OCP
  *  8-bit Floating Point v1.0 specifications, binary16 from IEEE 754-2008,
@@ -147,6 +151,15 @@ static double q4_0_elem(const uint8_t *codes, const uint16_t *d, int64_t K, int6
     return oracle_fp16(d[m * (K / 32) + k / 32]) * (double)(q4_0_code(codes, K, m, k) - 8);
 }
 
+/* FP8 block-128 element (m, k): e4m3(code[m][k]) * scale of the 128 x 128
+ * tile holding (m, k); scales are fp32 [ceil(M/128)][ceil(K/128)] row-major,
+ * so rows 0..127 share scale row 0 and k 0..127 scale column 0. */
+static double fp8_b128_elem(const uint8_t *codes, const float *scales, int64_t K, int64_t m, int64_t k)
+{
+    int64_t kb = (K + 127) / 128;
+    return oracle_e4m3(codes[m * K + k]) * (double)scales[(m / 128) * kb + k / 128];
+}
+
 /* ------------------------------------------------------------ dequantisation */
 
 /* w[m][k] = e2m1 * e4m3 * ts as a real number (fp64, exact: at most 30
@@ -196,6 +209,22 @@ void oracle_q4_0_dequant_f32(const uint8_t *codes, const uint16_t *d, int64_t M,
     for (int64_t m = 0; m < M; ++m)
         for (int64_t k = 0; k < K; ++k)
             w[m * K + k] = (float)q4_0_elem(codes, d, K, m, k);
+}
+
+/* FP8 block-128 dequantised weight: fp64 exact (4 + 24 significant bits);
+ * fp32 the exact value rounded once to nearest. */
+void oracle_fp8_b128_dequant_f64(const uint8_t *codes, const float *scales, int64_t M, int64_t K, double *w)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            w[m * K + k] = fp8_b128_elem(codes, scales, K, m, k);
+}
+
+void oracle_fp8_b128_dequant_f32(const uint8_t *codes, const float *scales, int64_t M, int64_t K, float *w)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            w[m * K + k] = (float)fp8_b128_elem(codes, scales, K, m, k);
 }
 
 /* ------------------------------------------------------------ GEMV */
@@ -260,6 +289,27 @@ void oracle_q4_0_gemv(const uint8_t *codes, const uint16_t *d, const uint16_t *x
             double sum = 0.0, abs_sum = 0.0;
             for (int64_t k = 0; k < K; ++k) {
                 double p = q4_0_elem(codes, d, K, m, k) * oracle_bf16(x[n * K + k]);
+                sum += p;
+                abs_sum += fabs(p);
+            }
+            y[n * R + i] = sum;
+            if (a)
+                a[n * R + i] = abs_sum;
+        }
+    }
+}
+
+void oracle_fp8_b128_gemv(const uint8_t *codes, const float *scales, const uint16_t *x,
+                          int64_t M, int64_t K, int64_t N,
+                          const int64_t *rows, int64_t nrows, double *y, double *a)
+{
+    int64_t R = rows ? nrows : M;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t i = 0; i < R; ++i) {
+            int64_t m = rows ? rows[i] : i;
+            double sum = 0.0, abs_sum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = fp8_b128_elem(codes, scales, K, m, k) * oracle_bf16(x[n * K + k]);
                 sum += p;
                 abs_sum += fabs(p);
             }

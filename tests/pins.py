@@ -61,3 +61,11 @@ def q4_0_codes_unpacked(codes: np.ndarray) -> np.ndarray:
 
 def q4_0_weight_lib(codes, d) -> np.ndarray:
     return (q4_0_codes_unpacked(codes).astype(np.float64) - 8.0) * np.repeat(fp16_lib(d), 32, axis=1)
+
+
+def fp8_b128_weight_lib(codes, scales) -> np.ndarray:
+    """Real-valued FP8 block-128 weight: torch's E4M3 decode of every code
+    times its tile's fp32 scale, the tile grid spread by numpy repeat."""
+    M, K = codes.shape
+    s = np.repeat(np.repeat(np.asarray(scales, dtype=np.float32).astype(np.float64), 128, axis=0), 128, axis=1)
+    return e4m3_lib(codes) * s[:M, :K]
