@@ -107,8 +107,11 @@ def extra_rows_spec():
     tokens and its grouped form over 256 experts (the MoE gate_up, 2I = 1024
     rows, H = 2048) for 2048 tokens routed top-8 (16384 pairs, multinomial
     expert counts), both reported in TFLOP/s against the measured bf16 peak;
-    and the bf16 -> NVFP4 / Q8_0 encoders on a 12288 x 4096 weight (bytes:
-    bf16 read, codes and scales written)."""
+    the whole routed MoE layer for a 1024-token prefill (E = 256, H = 2048,
+    I = 512, top-8: routing, gather, both grouped GEMMs, SiLU * up, combine;
+    flops 2 * T * topk * 3 * H * I, bytes the experts routed to once, x, y
+    and the logits); and the bf16 -> NVFP4 / Q8_0 encoders on a 12288 x 4096
+    weight (bytes: bf16 read, codes and scales written)."""
     return [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1)),
             ("nvfp4 gate_up+SiLU 12288x4096 N=1", "nvfp4_silu", dict(M=12288, K=4096, N=1)),
             ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1)),
@@ -117,6 +120,7 @@ def extra_rows_spec():
             ("nvfp4 prefill GEMM 12288x4096 T=2048", "nvfp4_gemm", dict(M=12288, K=4096, N=2048)),
             ("nvfp4 grouped prefill GEMM E=256 1024x2048 P=16384", "nvfp4_gemm_grouped",
              dict(E=256, M=1024, K=2048, N=16384)),
+            ("moe prefill T=1024", "moe_prefill", dict(T=1024, E=256, H=2048, I=512, topk=8)),
             ("nvfp4 encode 12288x4096", "nvfp4_encode", dict(M=12288, K=4096, N=1)),
             ("q8_0 encode 12288x4096", "q8_0_encode", dict(M=12288, K=4096, N=1))]
 
@@ -341,10 +345,14 @@ class Row:
             self.w = tuple(d(host[n]) for n in ("gu_codes", "gu_scales", "gu_ts", "dn_codes", "dn_scales", "dn_ts"))
             self.x_host, self.logits_host = host["x"], host["logits"]
             self.x, self.logits = d(host["x"]), d(host["logits"])
-            self.wsb = bqd.moe_layer_workspace_bytes(T, k, H, I, E)
+            if kind == "moe_prefill":
+                self.wsb = bqd.moe_prefill_workspace_bytes(T, k, H, I, E)
+                self.launches = 6  # route, gather, gate_up GEMM, SiLU * up, down GEMM, combine
+            else:
+                self.wsb = bqd.moe_layer_workspace_bytes(T, k, H, I, E)
+                self.launches = moe_launches(T, E, H, I, k)
             self.ws = torch.empty(self.wsb, dtype=torch.uint8, device="cuda")
             self.y = torch.empty(T * H, dtype=torch.float32, device="cuda")
-            self.launches = moe_launches(T, E, H, I, k)
             self.in_bytes = self.x.numel() * 2 + self.logits.numel() * 4
         self.out_bytes = self.y.numel() * self.y.element_size()
         self.weight_bytes = sum(t.numel() * t.element_size() for t in self.w)
@@ -383,6 +391,9 @@ class Row:
             b.nvfp4_gemm(w[0], w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "nvfp4_gemm_grouped":
             b.nvfp4_gemm_grouped(w[0], w[1], self.tse, self.x, self.offs, self.y, p["E"], p["M"], p["K"], p["N"])
+        elif self.kind == "moe_prefill":
+            T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
+            b.moe_prefill_layer(self.logits, *w, self.x, self.y, self.ws, self.wsb, E, H, I, T, k)
         else:
             T, E, H, I, k = p["T"], p["E"], p["H"], p["I"], p["topk"]
             b.moe_layer(self.logits, *w, self.x, self.y, self.ws, self.wsb, E, H, I, T, k)
@@ -712,15 +723,18 @@ def run_ours(args, rank, world):
         tr = profiled_traffic(r.name)
         ent["traffic"] = tr
         ent["traffic_ratio"] = None if tr is None else round(tr / r.bytes, 4)
-        if r.kind in ("nvfp4_gemm", "nvfp4_gemm_grouped"):  # contractions: flops against the bf16 tensor peak
-            fl = 2.0 * r.p["M"] * r.p["K"] * r.p["N"]
+        if r.kind in ("nvfp4_gemm", "nvfp4_gemm_grouped", "moe_prefill"):  # flops against the bf16 tensor peak
+            fl = (2.0 * r.p["M"] * r.p["K"] * r.p["N"] if r.kind != "moe_prefill"
+                  else 2.0 * r.p["T"] * r.p["topk"] * 3 * r.p["H"] * r.p["I"])
             ent["TFLOP_s"] = round(fl / us / 1e6, 1)
             ent["b2b_TFLOP_s"] = round(fl / bus / 1e6, 1)
             ent["frac_tensor"] = round(fl / bus / 1e6 / tensor_peak, 4)
             ent["tensor_peak_TFLOP_s"] = tensor_peak
-        if r.kind == "moe":
+        if r.kind in ("moe", "moe_prefill"):
             ent["us_per_token"] = round(us / r.p["T"], 3)
             ent["b2b_us_per_token"] = round(bus / r.p["T"], 3)
+            ent["tokens_per_s"] = round(r.p["T"] * 1e6 / us, 1)
+            ent["b2b_tokens_per_s"] = round(r.p["T"] * 1e6 / bus, 1)
         else:
             ent["tokens_per_s_equiv"] = round(r.p["N"] * 1e6 / us, 1)
             ent["b2b_tokens_per_s_equiv"] = round(r.p["N"] * 1e6 / bus, 1)

@@ -16,10 +16,14 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float
 // ts [E] (device), tokens [P][K] gathered expert-major, expert e's rows
 // [offsets[e], offsets[e + 1]) (device int32 [E + 1]), Y [P][M].
 bool gemm_grouped_supported(int64_t E, int64_t M, int64_t K, int64_t P);
-// accumulate: Y += instead of Y =.
+// accumulate: Y += instead of Y =. weight_k (default K): the weights' k; a
+// smaller divisor of K repeats them along the tokens' k, so that tokens
+// [P][r * weight_k] holding r parts of each activation row (side by side)
+// give W . (part 0 + ... + part r-1) in one call.
 cudaError_t launch_nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const float* ts,
                                       const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M,
-                                      int64_t K, int64_t P, cudaStream_t s, bool accumulate = false);
+                                      int64_t K, int64_t P, cudaStream_t s, bool accumulate = false,
+                                      int64_t weight_k = 0);
 
 // MoE prefill layer (moe_prefill.cu): route, gather, grouped gate_up GEMM,
 // SiLU(gate) * up split into two bf16 parts, grouped down GEMM of both

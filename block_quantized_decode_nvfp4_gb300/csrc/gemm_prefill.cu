@@ -171,17 +171,19 @@ struct RowLoad {  // 64 k of one weight row
     uint32_t s4;
 };
 
-// Grouped form (offsets != nullptr): E experts, weights [E][M][K], tokens
+// Grouped form (offsets != nullptr): E experts, weights [E][M][KW], tokens
 // [P][K] gathered expert-major, expert e's tokens [offsets[e],
 // offsets[e + 1]), its tensor scale ts_e[e]; grid row blockIdx.y is the
 // slot-th BN-token tile of all experts' tiles in expert order (slots past
 // the last tile do nothing). Dense form: E = 1, tokens [0, T), scale ts.
+// K is a multiple of KW: token k meets weight k % KW (KW = K but for the
+// MoE down projection, whose tokens hold two parts of h side by side).
 template <int BN>
 __global__ void __launch_bounds__(kGThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap map_x, const uint8_t* __restrict__ codes,
                       const uint8_t* __restrict__ scales, float ts, const float* __restrict__ ts_e,
                       const int32_t* __restrict__ offsets, int E, float* __restrict__ y, int64_t M, int K, int T,
-                      int accumulate)
+                      int accumulate, int KW)
 {
     using S = GemmShape<BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -194,7 +196,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     uint8_t* bstage = sm + kGS * kAStage;
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kGM;
-    const int nk = K / kGK;
+    const int nk = K / kGK;     // stages of B's k
+    const int nkw = KW / kGK;   // stages of the weights' k: B's k runs over them K / KW times
 
     // this CTA's expert and token range [n0, nend); an empty range: nothing to
     // do. Grouped: the experts' tile counts are scanned a block of experts at
@@ -242,8 +245,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     if (s_nend <= s_n0) return;  // uniform: before any barrier, copy or tensor-memory allocation
     const int e_cta = s_e, n0 = s_n0, nend = s_nend;
     if (offsets) {
-        codes += static_cast<int64_t>(e_cta) * M * (K / 2);
-        scales += static_cast<int64_t>(e_cta) * M * (K / 16);
+        codes += static_cast<int64_t>(e_cta) * M * (KW / 2);
+        scales += static_cast<int64_t>(e_cta) * M * (KW / 16);
         ts = ts_e[e_cta];
     }
 
@@ -316,15 +319,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int r = kGH * hf + 32 * q + lane;  // row of the tile
         const int64_t m = m0 + r;
         const bool live = m < M;
-        const uint8_t* crow = codes + (live ? m : 0) * static_cast<int64_t>(K / 2);
-        const uint8_t* srow = scales + (live ? m : 0) * static_cast<int64_t>(K / 16);
+        const uint8_t* crow = codes + (live ? m : 0) * static_cast<int64_t>(KW / 2);
+        const uint8_t* srow = scales + (live ? m : 0) * static_cast<int64_t>(KW / 16);
         RowLoad ring[kALoads];
         auto load = [&](int s) -> RowLoad {
             RowLoad v;
             if (live && s < nk) {
-                v.c0 = ld_stream_v4(crow + s * 32);
-                v.c1 = ld_stream_v4(crow + s * 32 + 16);
-                v.s4 = *reinterpret_cast<const uint32_t*>(srow + s * 4);
+                const int sw = s % nkw;
+                v.c0 = ld_stream_v4(crow + sw * 32);
+                v.c1 = ld_stream_v4(crow + sw * 32 + 16);
+                v.s4 = *reinterpret_cast<const uint32_t*>(srow + sw * 4);
             } else {
                 v.c0 = v.c1 = make_uint4(0u, 0u, 0u, 0u);
                 v.s4 = 0u;
@@ -431,7 +435,7 @@ bool make_x_map(CUtensorMap* map, const uint16_t* x, int64_t K, int64_t P, int b
 template <int BN>
 cudaError_t launch_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const float* ts_e,
                         const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M, int64_t K, int64_t P,
-                        int64_t tiles, int accumulate, cudaStream_t s)
+                        int64_t tiles, int accumulate, int64_t KW, cudaStream_t s)
 {
     CUtensorMap map;
     if (!make_x_map(&map, x, K, P, BN)) return cudaErrorInvalidValue;
@@ -452,7 +456,7 @@ cudaError_t launch_gemm(const uint8_t* codes, const uint8_t* scales, float ts, c
     cfg.attrs = attr;
     cfg.numAttrs = launch_flags() & kLaunchPdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, map, codes, scales, ts, ts_e, offsets, E, y, M, static_cast<int>(K),
-                              static_cast<int>(P), accumulate);
+                              static_cast<int>(P), accumulate, static_cast<int>(KW));
 }
 
 }  // namespace
@@ -472,16 +476,18 @@ bool gemm_grouped_supported(int64_t E, int64_t M, int64_t K, int64_t P)
 cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
                               int64_t M, int64_t K, int64_t T, cudaStream_t s)
 {
-    return launch_gemm<256>(codes, scales, ts, nullptr, nullptr, 1, x, y, M, K, T, (T + 255) / 256, 0, s);
+    return launch_gemm<256>(codes, scales, ts, nullptr, nullptr, 1, x, y, M, K, T, (T + 255) / 256, 0, K, s);
 }
 
 cudaError_t launch_nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const float* ts,
                                       const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M,
-                                      int64_t K, int64_t P, cudaStream_t s, bool accumulate)
+                                      int64_t K, int64_t P, cudaStream_t s, bool accumulate, int64_t weight_k)
 {
+    if (weight_k <= 0) weight_k = K;
+    if (weight_k % kGK != 0 || K % weight_k != 0) return cudaErrorInvalidValue;
     // tile slots: sum over experts of ceil(n_e / 128) <= P / 128 + E
     return launch_gemm<128>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 127) / 128 + E,
-                            accumulate ? 1 : 0, s);
+                            accumulate ? 1 : 0, weight_k, s);
 }
 
 cudaError_t read_and_clear_gemm_error(unsigned int* out)

@@ -13,8 +13,10 @@
 //  3. the grouped GEMM gives gate and up of every pair: G [P][2I];
 //  4. h = SiLU(g) * u in fp32, split into two bf16 parts hi = bf16(h) and
 //     lo = bf16(h - hi), whose sum holds h to ~2^-17 of its size (a single
-//     bf16 operand would round h by up to 2^-9, beyond the tolerance);
-//  5. the grouped GEMM of W_dn with hi, then with lo accumulated: D [P][H];
+//     bf16 operand would round h by up to 2^-9, beyond the tolerance),
+//     stored side by side: HL [P][2I] = [hi | lo];
+//  5. one grouped GEMM of W_dn, its k repeated twice, with HL:
+//     D [P][H] = W_dn . hi + W_dn . lo;
 //  6. the combine adds each token's slots in order, weighted.
 // Every product inside the GEMMs is exact; the sums are fp32.
 #include <cuda_bf16.h>
@@ -35,7 +37,7 @@ constexpr size_t al256(size_t n) { return (n + 255) & ~static_cast<size_t>(255);
 struct PrefillWs {
     int32_t *offsets, *pair_token, *pair_slot, *inv;
     float* pair_weight;
-    uint16_t *xg, *hhi, *hlo;
+    uint16_t *xg, *hl;
     float *gu, *d;
 };
 
@@ -57,8 +59,7 @@ PrefillWs carve(void* base, int T, int topk, int H, int I, int E, size_t* total)
     w.inv = reinterpret_cast<int32_t*>(take(P * 4));
     w.xg = reinterpret_cast<uint16_t*>(take(P * H * 2));
     w.gu = reinterpret_cast<float*>(take(P * 2 * I * 4));
-    w.hhi = reinterpret_cast<uint16_t*>(take(P * I * 2));
-    w.hlo = reinterpret_cast<uint16_t*>(take(P * I * 2));
+    w.hl = reinterpret_cast<uint16_t*>(take(P * 2 * I * 2));
     w.d = reinterpret_cast<float*>(take(P * H * 4));
     if (total) *total = o;
     return w;
@@ -82,9 +83,9 @@ __global__ void gather_kernel(const uint16_t* __restrict__ x, const int32_t* __r
     }
 }
 
-// h = SiLU(g) * u, g = G[p][i], u = G[p][I + i]; hi = bf16(h), lo = bf16(h - hi).
-__global__ void silu_split_kernel(const float* __restrict__ gu, uint16_t* __restrict__ hhi,
-                                  uint16_t* __restrict__ hlo, int P, int I)
+// h = SiLU(g) * u, g = G[p][i], u = G[p][I + i]; HL[p][i] = bf16(h),
+// HL[p][I + i] = bf16(h - bf16(h)).
+__global__ void silu_split_kernel(const float* __restrict__ gu, uint16_t* __restrict__ hl, int P, int I)
 {
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < static_cast<int64_t>(P) * I;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -93,8 +94,8 @@ __global__ void silu_split_kernel(const float* __restrict__ gu, uint16_t* __rest
         const float h = g / (1.0f + expf(-g)) * u;
         const __nv_bfloat16 hi = __float2bfloat16_rn(h);
         const __nv_bfloat16 lo = __float2bfloat16_rn(h - __bfloat162float(hi));
-        hhi[i] = __bfloat16_as_ushort(hi);
-        hlo[i] = __bfloat16_as_ushort(lo);
+        hl[p * 2 * I + k] = __bfloat16_as_ushort(hi);
+        hl[p * 2 * I + I + k] = __bfloat16_as_ushort(lo);
     }
 }
 
@@ -145,11 +146,10 @@ cudaError_t launch_moe_prefill_layer(const float* logits, const uint8_t* gu_code
     e = launch_nvfp4_gemm_grouped(gu_codes, gu_scales, gu_ts, w.offsets, E, w.xg, w.gu, 2 * static_cast<int64_t>(I),
                                   H, P, s);
     if (e != cudaSuccess) return e;
-    silu_split_kernel<<<grid_for(static_cast<int64_t>(P) * I), 256, 0, s>>>(w.gu, w.hhi, w.hlo, P, I);
+    silu_split_kernel<<<grid_for(static_cast<int64_t>(P) * I), 256, 0, s>>>(w.gu, w.hl, P, I);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    e = launch_nvfp4_gemm_grouped(dn_codes, dn_scales, dn_ts, w.offsets, E, w.hhi, w.d, H, I, P, s);
-    if (e != cudaSuccess) return e;
-    e = launch_nvfp4_gemm_grouped(dn_codes, dn_scales, dn_ts, w.offsets, E, w.hlo, w.d, H, I, P, s, true);
+    e = launch_nvfp4_gemm_grouped(dn_codes, dn_scales, dn_ts, w.offsets, E, w.hl, w.d, H, 2 * static_cast<int64_t>(I),
+                                  P, s, false, I);
     if (e != cudaSuccess) return e;
     combine_kernel<<<grid_for(static_cast<int64_t>(T) * H), 256, 0, s>>>(w.d, w.pair_weight, w.inv, y, T, H, topk,
                                                                          P);
