@@ -102,7 +102,8 @@ def extra_rows_spec():
     NVFP4 workload (ts = 1.0), whose time is launch latency, not bandwidth;
     the decode-path epilogue fusions on the layer shapes (gate_up with
     SiLU * up on the 12288 x 4096 gate/up weight, I = 6144; down with the
-    residual add on 4096 x 12288); the Q4_0 GEMV on the two layer shapes;
+    residual add on 4096 x 12288); the Q4_0 and FP8 block-128 GEMVs on the
+    two layer shapes;
     the tensor-core prefill GEMM of the 12288 x 4096 weight over 2048
     tokens and its grouped form over 256 experts (the MoE gate_up, 2I = 1024
     rows, H = 2048) for 2048 tokens routed top-8 (16384 pairs, multinomial
@@ -117,6 +118,8 @@ def extra_rows_spec():
             ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1)),
             ("q4_0 12288x4096 N=1", "q4_0", dict(M=12288, K=4096, N=1)),
             ("q4_0 4096x12288 N=1", "q4_0", dict(M=4096, K=12288, N=1)),
+            ("fp8_b128 12288x4096 N=1", "fp8_b128", dict(M=12288, K=4096, N=1)),
+            ("fp8_b128 4096x12288 N=1", "fp8_b128", dict(M=4096, K=12288, N=1)),
             ("nvfp4 prefill GEMM 12288x4096 T=2048", "nvfp4_gemm", dict(M=12288, K=4096, N=2048)),
             ("nvfp4 grouped prefill GEMM E=256 1024x2048 P=16384", "nvfp4_gemm_grouped",
              dict(E=256, M=1024, K=2048, N=16384)),
@@ -148,6 +151,8 @@ def host_inputs(kind, p, seed=0):
         return syn.dense_q8_0(p["M"], p["K"], N=p["N"], seed=seed)
     if kind == "q4_0":
         return syn.dense_q4_0(p["M"], p["K"], N=p["N"], seed=seed)
+    if kind == "fp8_b128":
+        return syn.dense_fp8_b128(p["M"], p["K"], N=p["N"], seed=seed)
     return syn.moe_layer(T=p["T"], E=p["E"], H=p["H"], I=p["I"], topk=p["topk"], seed=seed)
 
 
@@ -168,6 +173,9 @@ def row_bytes(kind, p, host):
         return q8_0_bytes(p["M"], p["K"], p["N"])
     if kind == "q4_0":  # 16 code bytes and a 2-byte scale per 32 weights
         return p["M"] * p["K"] // 2 + p["M"] * (p["K"] // 32) * 2 + 2 * p["N"] * p["K"] + 4 * p["N"] * p["M"]
+    if kind == "fp8_b128":  # a byte per weight, a 4-byte scale per 128 x 128 tile
+        return (p["M"] * p["K"] + ((p["M"] + 127) // 128) * ((p["K"] + 127) // 128) * 4 + 2 * p["N"] * p["K"]
+                + 4 * p["N"] * p["M"])
     return moe_bytes(p["T"], p["E"], p["H"], p["I"], p["topk"], host["logits"])
 
 
@@ -324,12 +332,14 @@ class Row:
             self.x_host, self.x = host["x"], d(host["x"])
             self.y = torch.empty(p["N"] * p["M"], dtype=torch.float32, device="cuda")
             self.in_bytes = self.x.numel() * 2
-        elif kind in ("nvfp4", "q8_0", "q4_0", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add", "nvfp4_gemm"):
+        elif kind in ("nvfp4", "q8_0", "q4_0", "fp8_b128", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add", "nvfp4_gemm"):
             M, K, N = p["M"], p["K"], p["N"]
             if kind == "q8_0":
                 self.w = (d(host["q"]), d(host["d"]))
             elif kind == "q4_0":
                 self.w = (d(host["codes"]), d(host["d"]))
+            elif kind == "fp8_b128":
+                self.w = (d(host["codes"]), d(host["scales"]))
             else:
                 self.w = (d(host["codes"]), d(host["scales"]))
                 self.ts = host["ts"]
@@ -387,6 +397,8 @@ class Row:
             b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "q4_0":
             b.q4_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
+        elif self.kind == "fp8_b128":
+            b.fp8_b128_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "nvfp4_gemm":
             b.nvfp4_gemm(w[0], w[1], self.ts, self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "nvfp4_gemm_grouped":
@@ -784,6 +796,101 @@ def run_profile_row(args):
     torch.cuda.synchronize()
 
 
+# Kernel sources each row's DRAM record depends on (a record is used only
+# while these files are unchanged).
+TRAFFIC_SOURCES = {
+    "direct": ["gemv_direct.cu", "common.cuh", "gemv.h", "host_util.h"],
+    "mma": ["gemv_mma.cu", "common.cuh", "stream.cuh", "gemv.h", "host_util.h"],
+    "stream": ["gemv_stream.cu", "common.cuh", "stream.cuh", "gemv.h", "host_util.h"],
+    "moe": ["moe_small.cu", "moe_route.cuh", "common.cuh", "stream.cuh", "gemv.h", "host_util.h"],
+    "encode": ["encode.cu", "common.cuh", "gemv.h", "host_util.h"],
+    "gemm": ["gemm_prefill.cu", "gemm.h", "common.cuh", "stream.cuh", "host_util.h"],
+    "moe_prefill": ["moe_prefill.cu", "moe_route.cuh", "gemm_prefill.cu", "gemm.h", "common.cuh", "stream.cuh",
+                    "gemv.h", "host_util.h"],
+}
+
+
+def traffic_sources(kind, p):
+    if kind == "moe":
+        return TRAFFIC_SOURCES["moe"]
+    if kind.endswith("encode"):
+        return TRAFFIC_SOURCES["encode"]
+    if kind in ("nvfp4_gemm", "nvfp4_gemm_grouped"):
+        return TRAFFIC_SOURCES["gemm"]
+    if kind == "moe_prefill":
+        return TRAFFIC_SOURCES["moe_prefill"]
+    if p.get("N", 1) > 1:
+        return TRAFFIC_SOURCES["mma"]
+    return TRAFFIC_SOURCES["stream" if p["K"] % 1024 else "direct"]
+
+
+SEPARATOR_KERNEL = "nvfp4_dequant_kernel"  # launched between rows by --profile-all; no row uses it
+
+
+def write_traffic(csv_path, calls, out_path=None):
+    """profiles/traffic.json from the ncu CSV (dram__bytes_read.sum,
+    dram__bytes_write.sum) of `bench.py --profile-all --profile-calls
+    <calls>`: the launches are split into rows at the separator kernel,
+    torch's own kernels (the rows' setup) are left out, and each row's bytes
+    are divided by the number of calls."""
+    import csv
+    spec = rows_spec() + extra_rows_spec()
+    with open(csv_path) as f:
+        recs = [r for r in csv.reader(f) if len(r) > 10]
+    h = recs[0]
+    ki, mi, vi, ii = (h.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value", "ID"))
+    launches = {}
+    for r in recs[1:]:
+        launches.setdefault(int(r[ii]), {"k": r[ki]})[r[mi]] = float(r[vi].replace(",", ""))
+    segs = None
+    for _, v in sorted(launches.items()):
+        name = v["k"]
+        if SEPARATOR_KERNEL in name:
+            segs = [] if segs is None else segs
+            segs.append([])
+        elif segs is not None and not (name.startswith("void at::") or name.startswith("at::")):
+            segs[-1].append(v)
+    if segs is None or len(segs) != len(spec):
+        raise SystemExit(f"{0 if segs is None else len(segs)} row segments in {csv_path}, {len(spec)} rows expected")
+    out = {}
+    for (row, kind, p), seg in zip(spec, segs):
+        rd = sum(v["dram__bytes_read.sum"] for v in seg) / calls
+        wr = sum(v["dram__bytes_write.sum"] for v in seg) / calls
+        kern = sorted({v["k"].split("(")[0].replace("void ", "").replace("(anonymous namespace)::", "")
+                       .replace("unnamed>::", "").replace("bqd::", "") for v in seg})
+        alg = row_bytes(kind, p, host_inputs(kind, p) if kind in ("moe", "moe_prefill") else None)
+        src = traffic_sources(kind, p)
+        out[row] = {"source_sha": source_sha(src), "sources": src, "kernels": kern,
+                    "launches_per_call": len(seg) // calls, "dram_bytes_per_launch": int(round(rd + wr)),
+                    "dram_read": int(round(rd)), "dram_write": int(round(wr)), "algorithmic_bytes": int(alg),
+                    "ratio": round((rd + wr) / alg, 4)}
+        print(f"{row:52s} {out[row]['dram_bytes_per_launch']:>12d} alg {alg:>12d} ratio {out[row]['ratio']}")
+    with open(out_path or os.path.join(ROOT, "profiles", "traffic.json"), "w") as f:
+        json.dump(out, f, indent=1)
+
+
+def run_profile_all(args):
+    """Every row (step rows, then extra rows) called --profile-calls times
+    and nothing else, a separator launch before each row; for a per-row ncu
+    capture in one process (see write_traffic)."""
+    import torch
+
+    import block_quantized_decode_nvfp4_gb300 as bqd
+    from block_quantized_decode_nvfp4_gb300 import build as _build
+
+    _build.build()
+    rows = [Row(n, k, p, host_inputs(k, p), torch, bqd) for n, k, p in rows_spec() + extra_rows_spec()]
+    sc = torch.zeros(16 * 8, dtype=torch.uint8, device="cuda")
+    ss = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    sw = torch.empty(16 * 16, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for r in rows:
+        bqd.nvfp4_dequant(sc, ss, 1.0, sw, 16, 16)
+        for _ in range(args.profile_calls):
+            r.run()
+    torch.cuda.synchronize()
+
+
 def run_profile_step(args):
     """Run --steps decode steps (every row once per step, in step order) and
     nothing else: the launch list of the timed region, for profilers."""
@@ -819,13 +926,28 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=3)
     ap.add_argument("--profile-step", action="store_true",
                     help="only run --steps decode steps (no per-row timings, no JSON line), for profilers")
+    ap.add_argument("--profile-all", action="store_true",
+                    help="call every row --profile-calls times, a separator launch before each (for ncu)")
+    ap.add_argument("--write-traffic", default=None, metavar="CSV",
+                    help="write profiles/traffic.json from the ncu CSV of --profile-all (no GPU needed)")
+    ap.add_argument("--list-rows", action="store_true", help="print the names of every row, one per line")
     args = ap.parse_args()
+    if args.list_rows:
+        for n, _, _ in rows_spec() + extra_rows_spec():
+            print(n)
+        return
+    if args.write_traffic is not None:
+        write_traffic(args.write_traffic, args.profile_calls)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.profile_row is not None:
         run_profile_row(args)
+        return
+    if args.profile_all:
+        run_profile_all(args)
         return
     if args.profile_step:
         run_profile_step(args)

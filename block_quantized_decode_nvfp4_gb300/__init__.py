@@ -45,6 +45,9 @@ from ._binding import (  # noqa: F401
     q4_0_gemv,
     q4_0_gemv_path,
     q4_0_dequant,
+    fp8_b128_gemv,
+    fp8_b128_gemv_path,
+    fp8_b128_dequant,
     q8_0_gemv_silu_mul,
     version,
 )

@@ -54,6 +54,9 @@ SIGNATURES = {
     "q4_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q4_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q4_0_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
+    "fp8_b128_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "fp8_b128_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
+    "fp8_b128_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
     "nvfp4_gemv_add": (_i32, [_vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "nvfp4_encode": (_i32, [_vp, _f32, _vp, _vp, _i64, _i64, _vp]),
     "q8_0_encode": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
@@ -229,6 +232,21 @@ def q4_0_gemv_path(codes, d, x, y, M, K, N, path, stream=None):
 
 def q4_0_dequant(codes, d, w, M, K, stream=None):
     _check(lib().q4_0_dequant(_ptr(codes), _ptr(d), _ptr(w), M, K, _stream(stream)), "q4_0_dequant")
+
+
+def fp8_b128_gemv(codes, scales, x, y, M, K, N, stream=None):
+    """FP8 block-128 GEMV: E4M3 codes [M][K], fp32 tile scales [ceil(M/128)][ceil(K/128)]."""
+    _check(lib().fp8_b128_gemv(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), M, K, N, _stream(stream)),
+           "fp8_b128_gemv")
+
+
+def fp8_b128_gemv_path(codes, scales, x, y, M, K, N, path, stream=None):
+    _check(lib().fp8_b128_gemv_path(_ptr(codes), _ptr(scales), _ptr(x), _ptr(y), M, K, N, path, _stream(stream)),
+           "fp8_b128_gemv_path")
+
+
+def fp8_b128_dequant(codes, scales, w, M, K, stream=None):
+    _check(lib().fp8_b128_dequant(_ptr(codes), _ptr(scales), _ptr(w), M, K, _stream(stream)), "fp8_b128_dequant")
 
 
 def moe_route_topk(logits, T, E, topk, expert_offsets, pair_token, pair_weight, pair_slot, stream=None):

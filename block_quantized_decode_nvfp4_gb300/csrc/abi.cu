@@ -186,6 +186,26 @@ bqd_status q4_0_gemv(const uint8_t* codes, const uint16_t* d, const uint16_t* x,
     return q4_0_gemv_path(codes, d, x, y, M, K, N, BQD_PATH_AUTO, stream);
 }
 
+bqd_status fp8_b128_gemv_path(const uint8_t* codes, const float* scales, const uint16_t* x, float* y, int64_t M,
+                              int64_t K, int N, int path, cudaStream_t stream)
+{
+    if (path != BQD_PATH_AUTO && path != BQD_PATH_CUDA_CORE && path != BQD_PATH_DIRECT) return BQD_ERR_PATH;
+    bqd_status st = check_dense(codes, scales, x, y, M, K, N, 32, true);
+    if (st != BQD_OK || M == 0) return st;
+    if (path == BQD_PATH_DIRECT && !bqd::direct_gemv_supported(M, K, N)) return BQD_ERR_PATH;
+    if ((st = check_arch()) != BQD_OK) return st;
+    if (K == 0) return zero_output(y, M * N, stream);
+    if (path == BQD_PATH_DIRECT || (path == BQD_PATH_AUTO && bqd::direct_gemv_supported(M, K, N)))
+        return from_cuda(bqd::launch_fp8_b128_gemv_direct(codes, scales, x, y, M, K, stream));
+    return from_cuda(bqd::launch_fp8_b128_gemv_cuda_core(codes, scales, x, y, M, K, N, stream));
+}
+
+bqd_status fp8_b128_gemv(const uint8_t* codes, const float* scales, const uint16_t* x, float* y, int64_t M,
+                         int64_t K, int N, cudaStream_t stream)
+{
+    return fp8_b128_gemv_path(codes, scales, x, y, M, K, N, BQD_PATH_AUTO, stream);
+}
+
 // ---------------------------------------------------------------- prefill GEMM
 bqd_status nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float tensor_scale, const uint16_t* x, float* y,
                       int64_t M, int64_t K, int64_t T, cudaStream_t stream)
@@ -378,6 +398,15 @@ bqd_status q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64
     if (st != BQD_OK || M == 0 || K == 0) return st;
     if ((st = check_arch()) != BQD_OK) return st;
     return from_cuda(bqd::launch_q4_0_dequant(codes, d, w, M, K, stream));
+}
+
+bqd_status fp8_b128_dequant(const uint8_t* codes, const float* scales, float* w, int64_t M, int64_t K,
+                            cudaStream_t stream)
+{
+    bqd_status st = check_dense(codes, scales, nullptr, w, M, K, 1, 32, false);
+    if (st != BQD_OK || M == 0 || K == 0) return st;
+    if ((st = check_arch()) != BQD_OK) return st;
+    return from_cuda(bqd::launch_fp8_b128_dequant(codes, scales, w, M, K, stream));
 }
 
 bqd_status moe_route_topk(const float* logits, int T, int E, int topk, int32_t* expert_offsets, int32_t* pair_token,

@@ -43,6 +43,13 @@ __device__ __forceinline__ uint32_t ld_stream_u16(const void* p)
     return r;
 }
 
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p)
+{
+    uint32_t r;
+    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t ld_stream_u8(const void* p)
 {
     uint16_t r;
@@ -411,28 +418,96 @@ struct Q4_0Fmt {
     }
 };
 
-// Bytes of the codes plane and of the scales plane per weight row.
+// FP8 block-128: a 32-element chunk is 32 E4M3 bytes in element order; its
+// fp32 scale is the one of the 128-element k tile holding it (four chunks
+// share it), and 128 consecutive rows share one row of scales.
+struct Fp8B128Fmt {
+    static constexpr int kElems = 32;
+    __device__ static __forceinline__ int swz(int c) { return c & 7; }
+    struct Chunk {
+        uint4 a, b;
+        uint32_t s;
+    };
+    __device__ static __forceinline__ Chunk load(const uint8_t* codes_row, const uint8_t* scales_row, int c)
+    {
+        Chunk ch;
+        ch.a = ld_stream_v4(codes_row + 32 * c);
+        ch.b = ld_stream_v4(codes_row + 32 * c + 16);
+        ch.s = ld_stream_u32(scales_row + 4 * (c >> 2));
+        return ch;
+    }
+    template <int RPW, int NC>
+    __device__ static __forceinline__ void dot(const Chunk (&ch)[RPW], const float* xs, int xstride, int sw,
+                                               float2 (&acc)[RPW][NC])
+    {
+        float2 part[RPW][NC];
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int n = 0; n < NC; ++n) part[r][n] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // word j: elements 4j .. 4j + 3
+            float2 lo[RPW], hi[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const uint32_t words[8] = {ch[r].a.x, ch[r].a.y, ch[r].a.z, ch[r].a.w,
+                                           ch[r].b.x, ch[r].b.y, ch[r].b.z, ch[r].b.w};
+                lo[r] = e4m3x2_to_float2(words[j]);
+                hi[r] = e4m3x2_to_float2(words[j] >> 16);
+            }
+#pragma unroll
+            for (int n = 0; n < NC; ++n) {
+                const float4 xv = *reinterpret_cast<const float4*>(xs + n * xstride + ((j ^ sw) << 2));
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    part[r][n] = __ffma2_rn(lo[r], make_float2(xv.x, xv.y), part[r][n]);
+                    part[r][n] = __ffma2_rn(hi[r], make_float2(xv.z, xv.w), part[r][n]);
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float s = __uint_as_float(ch[r].s);
+#pragma unroll
+            for (int n = 0; n < NC; ++n) acc[r][n].x = fmaf(s, part[r][n].x + part[r][n].y, acc[r][n].x);
+        }
+    }
+};
+
+// Bytes of the codes plane per weight row; bytes of one row of the scales
+// plane; and the byte offset of weight row m's scales (rows share a scale
+// row only in the FP8 block-128 format).
 template <class F>
 struct RowPitch;
 template <>
 struct RowPitch<Nvfp4Vec> {
     __host__ __device__ static int64_t codes(int64_t K) { return K / 2; }
     __host__ __device__ static int64_t scales(int64_t K) { return K / 16; }
+    __host__ __device__ static int64_t srow(int64_t m, int64_t K) { return m * scales(K); }
 };
 template <>
 struct RowPitch<Nvfp4Narrow> {
     __host__ __device__ static int64_t codes(int64_t K) { return K / 2; }
     __host__ __device__ static int64_t scales(int64_t K) { return K / 16; }
+    __host__ __device__ static int64_t srow(int64_t m, int64_t K) { return m * scales(K); }
 };
 template <>
 struct RowPitch<Q8_0Fmt> {
     __host__ __device__ static int64_t codes(int64_t K) { return K; }
     __host__ __device__ static int64_t scales(int64_t K) { return (K / 32) * 2; }
+    __host__ __device__ static int64_t srow(int64_t m, int64_t K) { return m * scales(K); }
 };
 template <>
 struct RowPitch<Q4_0Fmt> {
     __host__ __device__ static int64_t codes(int64_t K) { return K / 2; }
     __host__ __device__ static int64_t scales(int64_t K) { return (K / 32) * 2; }
+    __host__ __device__ static int64_t srow(int64_t m, int64_t K) { return m * scales(K); }
+};
+template <>
+struct RowPitch<Fp8B128Fmt> {
+    __host__ __device__ static int64_t codes(int64_t K) { return K; }
+    __host__ __device__ static int64_t scales(int64_t K) { return (K + 127) / 128 * 4; }
+    __host__ __device__ static int64_t srow(int64_t m, int64_t K) { return (m >> 7) * scales(K); }
 };
 
 // ------------------------------------------------------------------ rows

@@ -41,16 +41,16 @@ constexpr int kXsBudgetBytes = 96 * 1024;
 // seg_len elements: the CTA owns a balanced row range, walks it in batches of
 // kWarps * RPW rows and restages the activations for each segment.
 // Row pointers of the group starting at r0 (rows past r_end repeat r0).
-template <int RPW>
-__device__ __forceinline__ void group_rows(const uint8_t* codes, const uint8_t* scales, int64_t cpitch,
-                                           int64_t spitch, int64_t r0, int64_t r_end, const uint8_t* (&crow)[RPW],
+template <class F, int RPW>
+__device__ __forceinline__ void group_rows(const uint8_t* codes, const uint8_t* scales, int64_t cpitch, int64_t K,
+                                           int64_t r0, int64_t r_end, const uint8_t* (&crow)[RPW],
                                            const uint8_t* (&srow)[RPW])
 {
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         const int64_t m = r0 + r < r_end ? r0 + r : r0;
         crow[r] = codes + m * cpitch;
-        srow[r] = scales + m * spitch;
+        srow[r] = scales + RowPitch<F>::srow(m, K);
     }
 }
 
@@ -64,7 +64,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const uint8_t* __rest
     const int lane = threadIdx.x % kWarp;
     const int warp = threadIdx.x / kWarp;
     const int64_t cpitch = RowPitch<F>::codes(K);
-    const int64_t spitch = RowPitch<F>::scales(K);
     const int chunks = static_cast<int>(K / F::kElems);
     RowStream<F, RPW, D> rs;
 
@@ -74,13 +73,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const uint8_t* __rest
         const int64_t r_lo = M * gw / nw, r_hi = M * (gw + 1) / nw;
         const uint8_t* crow[RPW];
         const uint8_t* srow[RPW];
-        group_rows(codes, scales, cpitch, spitch, r_lo, r_hi, crow, srow);
+        group_rows<F>(codes, scales, cpitch, K, r_lo, r_hi, crow, srow);
         if (r_lo < r_hi) rs.start(crow, srow, 0, chunks, lane);
         stage_x_bf16<F>(x, K, NC, 0, static_cast<int>(K), xs);
         __syncthreads();
         for (int64_t r0 = r_lo; r0 < r_hi; r0 += RPW) {
             if (r0 != r_lo) {
-                group_rows(codes, scales, cpitch, spitch, r0, r_hi, crow, srow);
+                group_rows<F>(codes, scales, cpitch, K, r0, r_hi, crow, srow);
                 rs.start(crow, srow, 0, chunks, lane);
             }
             const int nrows = static_cast<int>(r_hi - r0 < RPW ? r_hi - r0 : RPW);
@@ -114,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const uint8_t* __rest
         for (int r = 0; r < RPW; ++r) {
             const int64_t m = nrows > 0 ? r0 + (r < nrows ? r : 0) : 0;
             crow[r] = codes + m * cpitch;
-            srow[r] = scales + m * spitch;
+            srow[r] = scales + RowPitch<F>::srow(m, K);
         }
         float2 acc[RPW][NC];
 #pragma unroll
@@ -186,6 +185,23 @@ __global__ void q4_0_dequant_kernel(const uint8_t* __restrict__ codes, const uin
         const int c = codes[i];
         w[m * K + k0] = s * static_cast<float>((c & 15) - 8);
         w[m * K + k0 + 16] = s * static_cast<float>((c >> 4) - 8);
+    }
+}
+
+// w[m][k] = e4m3(code) * the fp32 scale of the 128 x 128 tile holding
+// (m, k), in fp32: the E4M3 value is exact in fp32 and the one multiply
+// rounds the exact product once to nearest. One thread per pair of codes
+// (K is even, so a pair never straddles two rows).
+__global__ void fp8_b128_dequant_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
+                                        float* __restrict__ w, int64_t M, int64_t K)
+{
+    const int64_t npairs = M * K / 2, kt = (K + 127) / 128;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < npairs;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = (2 * i) / K, k = 2 * i - m * K;
+        const float2 v = e4m3x2_to_float2(codes[2 * i] | (static_cast<uint32_t>(codes[2 * i + 1]) << 8));
+        w[2 * i] = v.x * scales[(m / 128) * kt + k / 128];
+        w[2 * i + 1] = v.y * scales[(m / 128) * kt + (k + 1) / 128];
     }
 }
 
@@ -272,6 +288,12 @@ cudaError_t launch_q4_0_gemv_cuda_core(const uint8_t* codes, const uint16_t* d, 
     return launch_gemv<Q4_0Fmt>(codes, reinterpret_cast<const uint8_t*>(d), 1.0f, x, y, M, K, N, s);
 }
 
+cudaError_t launch_fp8_b128_gemv_cuda_core(const uint8_t* codes, const float* scales, const uint16_t* x, float* y,
+                                           int64_t M, int64_t K, int N, cudaStream_t s)
+{
+    return launch_gemv<Fp8B128Fmt>(codes, reinterpret_cast<const uint8_t*>(scales), 1.0f, x, y, M, K, N, s);
+}
+
 static unsigned dequant_grid(int64_t work)
 {
     int64_t g = (work + 255) / 256;
@@ -297,6 +319,13 @@ cudaError_t launch_q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* 
                                 cudaStream_t s)
 {
     q4_0_dequant_kernel<<<dequant_grid(M * K / 2), 256, 0, s>>>(codes, d, w, M, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_b128_dequant(const uint8_t* codes, const float* scales, float* w, int64_t M, int64_t K,
+                                    cudaStream_t s)
+{
+    fp8_b128_dequant_kernel<<<dequant_grid(M * K / 2), 256, 0, s>>>(codes, scales, w, M, K);
     return cudaGetLastError();
 }
 

@@ -37,6 +37,15 @@ cudaError_t launch_q4_0_gemv_cuda_core(const uint8_t* codes, const uint16_t* d, 
                                        int64_t M, int64_t K, int N, cudaStream_t s);
 cudaError_t launch_q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64_t M, int64_t K,
                                 cudaStream_t s);
+// FP8 block-128 (E4M3 codes [M][K], fp32 scales [ceil(M/128)][ceil(K/128)]):
+// the direct kernel (N == 1, the K above), the CUDA-core path (any M,
+// K % 32 == 0, 1 <= N <= 16) and the dequantisation.
+cudaError_t launch_fp8_b128_gemv_direct(const uint8_t* codes, const float* scales, const uint16_t* x, float* y,
+                                        int64_t M, int64_t K, cudaStream_t s);
+cudaError_t launch_fp8_b128_gemv_cuda_core(const uint8_t* codes, const float* scales, const uint16_t* x, float* y,
+                                           int64_t M, int64_t K, int N, cudaStream_t s);
+cudaError_t launch_fp8_b128_dequant(const uint8_t* codes, const float* scales, float* w, int64_t M, int64_t K,
+                                    cudaStream_t s);
 // The same kernel with a fused epilogue: y = W x + r (y may be r); and, on a
 // gate_up weight of 2I rows (gate rows 0..I-1, up rows I..2I-1),
 // h = SiLU(gate . x) * (up . x).

@@ -90,7 +90,18 @@ struct Q8Item {  // 32 elements of one row: 32 int8, one fp16 scale
     uint32_t d;
 };
 
-struct DirNvfp4 {
+// Scale addressing of a format: weight row pr's scales start at
+// srow(pr) * spitch(K) bytes, and lane l's chunk of each 1024-element step
+// nc finds its scale at slane(l) + nc * kSChunk bytes from there. Here: one
+// 2-byte scale per 32-element chunk and per row.
+struct DirScale16 {
+    static constexpr int kSChunk = 64;
+    __host__ __device__ static constexpr int64_t spitch(int64_t K) { return K / 16; }
+    __device__ static __forceinline__ int64_t srow(int64_t pr) { return pr; }
+    __device__ static __forceinline__ int slane(int lane) { return lane * 2; }
+};
+
+struct DirNvfp4 : DirScale16 {
     using Item = Nvfp4Item;
     static constexpr int kCodeBytes = 16;  // per 32-element chunk
     __device__ static __forceinline__ Item load(const uint8_t* c, const uint8_t* s)
@@ -137,7 +148,7 @@ struct DirNvfp4 {
 // elements 4w .. 4w + 3 and 16 + 4w .. 16 + 4w + 3: activation pieces w / 2
 // and 2 + w / 2. q - 8 is exact in f16 (1024 + q from the byte's mantissa
 // bits, minus 1032).
-struct DirQ4 {
+struct DirQ4 : DirScale16 {
     using Item = Nvfp4Item;  // 16 code bytes, the fp16 scale
     static constexpr int kCodeBytes = 16;
     __device__ static __forceinline__ Item load(const uint8_t* c, const uint8_t* s)
@@ -185,7 +196,7 @@ struct DirQ4 {
     }
 };
 
-struct DirQ8 {
+struct DirQ8 : DirScale16 {
     using Item = Q8Item;
     static constexpr int kCodeBytes = 32;
     __device__ static __forceinline__ Item load(const uint8_t* c, const uint8_t* s)
@@ -224,6 +235,55 @@ struct DirQ8 {
             }
         }
         acc = fmaf(fp16_to_float(it.d), a0 + a1, acc);
+    }
+};
+
+// FP8 block-128: the chunk is 32 E4M3 bytes in element order (word w holds
+// elements 4w .. 4w + 3, activation piece w / 2); lanes 4i .. 4i + 3 take
+// the four chunks of one 128-element k tile and read its one fp32 scale, and
+// 128 consecutive rows share a row of scales. E4M3 -> f16 is exact, and so
+// is its product with an f16 activation in fp32.
+struct DirFp8 {
+    using Item = Q8Item;  // 32 code bytes, the fp32 scale's bits
+    static constexpr int kCodeBytes = 32;
+    static constexpr int kSChunk = 32;  // eight tile scales per 1024-element step
+    __host__ __device__ static constexpr int64_t spitch(int64_t K) { return K / 32; }  // (K / 128) scales
+    __device__ static __forceinline__ int64_t srow(int64_t pr) { return pr >> 7; }
+    __device__ static __forceinline__ int slane(int lane) { return lane & ~3; }
+    __device__ static __forceinline__ Item load(const uint8_t* c, const uint8_t* s)
+    {
+        Item it;
+        it.a = ld_stream_v4(c);
+        it.b = ld_stream_v4(c + 16);
+        it.d = ld_stream_u32(s);
+        return it;
+    }
+    template <bool FAST>
+    __device__ static __forceinline__ void dot(const Item& it, const uint16_t* xc, int sw, float& acc)
+    {
+        const uint32_t words[8] = {it.a.x, it.a.y, it.a.z, it.a.w, it.b.x, it.b.y, it.b.z, it.b.w};
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {  // 8 elements = 2 code words = activation piece p
+            const uint4 xq = *reinterpret_cast<const uint4*>(xc + ((p ^ sw) << 3));
+            const uint32_t xp[4] = {xq.x, xq.y, xq.z, xq.w};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t w = words[2 * p + h];
+                const uint32_t q01 = e4m3x2_to_f16x2(w), q23 = e4m3x2_to_f16x2(w >> 16);
+                if constexpr (FAST) {
+                    fma_f16x2(q01, xp[2 * h], a0, a1);
+                    fma_f16x2(q23, xp[2 * h + 1], a0, a1);
+                } else {
+                    const float2 lo = f16x2_to_float2(q01), hi = f16x2_to_float2(q23);
+                    a0 = fmaf(lo.x, bf16_lo(xp[2 * h]), a0);
+                    a1 = fmaf(lo.y, bf16_hi(xp[2 * h]), a1);
+                    a0 = fmaf(hi.x, bf16_lo(xp[2 * h + 1]), a0);
+                    a1 = fmaf(hi.y, bf16_hi(xp[2 * h + 1]), a1);
+                }
+            }
+        }
+        acc = fmaf(__uint_as_float(it.d), a0 + a1, acc);
     }
 };
 
@@ -268,7 +328,8 @@ __device__ __forceinline__ void direct_rows(typename F::Item (&buf)[D], const ui
                     const int nr = (g + D) / CPL, nc = (g + D) % CPL;
                     if (row0 + nr < r_hi) {
                         const int64_t pr = phys_row<EPI>(row0 + nr, half);
-                        buf[g % D] = F::load(cp + pr * cpitch + nc * 32 * F::kCodeBytes, sp + pr * spitch + nc * 64);
+                        buf[g % D] = F::load(cp + pr * cpitch + nc * 32 * F::kCodeBytes,
+                                             sp + F::srow(pr) * spitch + nc * F::kSChunk);
                     }
                     F::template dot<FAST>(cur, xl + i * 1024, sw, acc);
                     // keep the next chunk's shared-memory loads after this chunk's arithmetic
@@ -301,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t half = M / 2;
     constexpr int W = THREADS / kWarp;
     constexpr int64_t K = 1024 * CPL;
-    constexpr int64_t cpitch = K / 32 * F::kCodeBytes, spitch = K / 16;
+    constexpr int64_t cpitch = K / 32 * F::kCodeBytes, spitch = F::spitch(K);
     constexpr int NP = CPL * 128;                        // 16-byte activation pieces
     constexpr int PPT = (NP + THREADS - 1) / THREADS;    // pieces per thread
     extern __shared__ __align__(16) uint16_t xs[];
@@ -324,7 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         r_hi *= 2;
     }
     const uint8_t* cp = codes + lane * F::kCodeBytes;
-    const uint8_t* sp = scales + lane * 2;
+    const uint8_t* sp = scales + F::slane(lane);
     if (threadIdx.x == 0) {
         s_emax = 0;
         s_emin = INT_MAX;
@@ -337,7 +398,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int64_t row = r_lo + d / CPL;
         if (row < r_hi) {
             const int64_t pr = phys_row<EPI>(row, half);
-            buf[d] = F::load(cp + pr * cpitch + (d % CPL) * 32 * F::kCodeBytes, sp + pr * spitch + (d % CPL) * 64);
+            buf[d] = F::load(cp + pr * cpitch + (d % CPL) * 32 * F::kCodeBytes,
+                             sp + F::srow(pr) * spitch + (d % CPL) * F::kSChunk);
         }
     }
     pdl_trigger();
@@ -437,6 +499,8 @@ struct DirCfg<DirQ8> {
     template <int CPL>
     static constexpr int depth() { return CPL == 3 ? 3 : 2; }
 };
+template <>
+struct DirCfg<DirFp8> : DirCfg<DirQ8> {};  // the same bytes per element
 
 template <class F, int CPL, int EPI>
 cudaError_t launch_cpl(const uint8_t* codes, const uint8_t* scales, float ts, const uint16_t* x, float* y,
@@ -505,6 +569,13 @@ cudaError_t launch_q4_0_gemv_direct(const uint8_t* codes, const uint16_t* d, con
                                     int64_t M, int64_t K, cudaStream_t s)
 {
     return launch_direct<DirQ4, kEpiPlain>(codes, reinterpret_cast<const uint8_t*>(d), 1.0f, x, y, nullptr, M, K, s);
+}
+
+cudaError_t launch_fp8_b128_gemv_direct(const uint8_t* codes, const float* scales, const uint16_t* x, float* y,
+                                        int64_t M, int64_t K, cudaStream_t s)
+{
+    return launch_direct<DirFp8, kEpiPlain>(codes, reinterpret_cast<const uint8_t*>(scales), 1.0f, x, y, nullptr, M,
+                                            K, s);
 }
 
 cudaError_t launch_q8_0_gemv_direct(const int8_t* q, const uint16_t* d, const uint16_t* x, float* y, int64_t M,

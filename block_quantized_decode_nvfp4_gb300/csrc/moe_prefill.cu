@@ -7,7 +7,12 @@
 // The layer computes what the small-batch and stream paths compute (softmax
 // top-k routing, h = SiLU(gate) * up per (token, slot), y_t = sum over the
 // slots of w * (W_dn . h), slots added in order 0 .. topk - 1):
-//  1. the route kernel writes the expert-major pair list;
+//  1. routing in three kernels that spread the tokens over the GPU: every
+//     token's top-k (route_token, the same selection and weights as the
+//     decode router) with per-block expert counts; one CTA turning the
+//     counts into the CSR offsets and each block's cursors; every block
+//     placing its pairs. The list is the decode router's: expert-major,
+//     tokens ascending within an expert;
 //  2. a gather copies every pair's token row, expert-major, and records the
 //     pair of each (token, slot);
 //  3. the grouped GEMM gives gate and up of every pair: G [P][2I];
@@ -27,6 +32,7 @@
 #include "common.cuh"
 #include "gemm.h"
 #include "gemv.h"
+#include "moe_route.cuh"
 
 namespace bqd {
 
@@ -34,9 +40,15 @@ namespace {
 
 constexpr size_t al256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
+constexpr int kRouteTok = 32;        // tokens per routing block
+constexpr int kRouteThreads = 256;   // eight warps, a token each at a time
+constexpr int kScanThreads = 1024;   // >= the largest E
+
+int route_blocks(int T) { return (T + kRouteTok - 1) / kRouteTok; }
+
 struct PrefillWs {
-    int32_t *offsets, *pair_token, *pair_slot, *inv;
-    float* pair_weight;
+    int32_t *offsets, *pair_token, *pair_slot, *inv, *sel_e, *blk_cnt;
+    float *pair_weight, *sel_w;
     uint16_t *xg, *hl;
     float *gu, *d;
 };
@@ -57,12 +69,110 @@ PrefillWs carve(void* base, int T, int topk, int H, int I, int E, size_t* total)
     w.pair_weight = reinterpret_cast<float*>(take(P * 4));
     w.pair_slot = reinterpret_cast<int32_t*>(take(P * 4));
     w.inv = reinterpret_cast<int32_t*>(take(P * 4));
+    w.sel_e = reinterpret_cast<int32_t*>(take(P * 4));
+    w.sel_w = reinterpret_cast<float*>(take(P * 4));
+    w.blk_cnt = reinterpret_cast<int32_t*>(take(static_cast<size_t>(route_blocks(T)) * E * 4));
     w.xg = reinterpret_cast<uint16_t*>(take(P * H * 2));
     w.gu = reinterpret_cast<float*>(take(P * 2 * I * 4));
     w.hl = reinterpret_cast<uint16_t*>(take(P * 2 * I * 2));
     w.d = reinterpret_cast<float*>(take(P * H * 4));
     if (total) *total = o;
     return w;
+}
+
+// Routing, pass 1: block b's tokens [32 b, 32 b + 32), a warp per token:
+// slot s of token t goes to sel_e/sel_w[t * topk + s]; blk_cnt[b][e] counts
+// the block's pairs of expert e.
+__global__ void __launch_bounds__(kRouteThreads)
+    route_select_kernel(const float* __restrict__ logits, int T, int E, int topk, int32_t* __restrict__ sel_e,
+                        float* __restrict__ sel_w, int32_t* __restrict__ blk_cnt)
+{
+    extern __shared__ int s_cnt[];  // [E]
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = 0;
+    __syncthreads();
+    const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+    const int t0 = blockIdx.x * kRouteTok, t1 = min(T, t0 + kRouteTok);
+    for (int t = t0 + warp; t < t1; t += kRouteThreads / kWarp) {  // warp-uniform
+        int e = 0;
+        float w = 0.f;
+        route_token(logits + static_cast<int64_t>(t) * E, E, topk, lane, &e, &w);
+        if (lane < topk) {  // e < E: route_token picks untaken experts only, and topk <= E
+            sel_e[t * topk + lane] = e;
+            sel_w[t * topk + lane] = w;
+            atomicAdd(&s_cnt[e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) blk_cnt[static_cast<int64_t>(blockIdx.x) * E + e] = s_cnt[e];
+}
+
+// Routing, pass 2 (one CTA, thread e per expert, E <= 1024): blk_cnt[b][e]
+// becomes the number of expert e's pairs in blocks before b, and offsets the
+// exclusive scan of the experts' totals (offsets[E] = P).
+__global__ void __launch_bounds__(kScanThreads)
+    route_scan_kernel(int32_t* __restrict__ blk_cnt, int nb, int E, int P, int32_t* __restrict__ offsets)
+{
+    __shared__ int s_warp[kScanThreads / kWarp];
+    const int e = threadIdx.x, lane = e % kWarp, warp = e / kWarp;
+    int tot = 0;
+    if (e < E) {
+        for (int b = 0; b < nb; ++b) {
+            const int c = blk_cnt[static_cast<int64_t>(b) * E + e];
+            blk_cnt[static_cast<int64_t>(b) * E + e] = tot;
+            tot += c;
+        }
+    }
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == kWarp - 1) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = s_warp[lane], vi = v;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int n = __shfl_up_sync(0xFFFFFFFFu, vi, o);
+            if (lane >= o) vi += n;
+        }
+        s_warp[lane] = vi - v;  // exclusive prefix of the warps' totals
+    }
+    __syncthreads();
+    if (e < E) offsets[e] = s_warp[warp] + incl - tot;
+    if (e == 0) offsets[E] = P;
+}
+
+// Routing, pass 3: one warp per block writes the block's pairs, token by
+// token in order, at its experts' cursors (offsets[e] + blk_cnt[b][e]); a
+// token's experts are distinct, so its lanes never share a cursor.
+__global__ void __launch_bounds__(kWarp)
+    route_place_kernel(const int32_t* __restrict__ sel_e, const float* __restrict__ sel_w,
+                       const int32_t* __restrict__ blk_cnt, const int32_t* __restrict__ offsets, int T, int E,
+                       int topk, int P, int32_t* __restrict__ pair_token, float* __restrict__ pair_weight,
+                       int32_t* __restrict__ pair_slot)
+{
+    extern __shared__ int s_cur[];  // [E] cursors, then the block's sel_e [kRouteTok * topk]
+    int* s_sel = s_cur + E;
+    const int lane = threadIdx.x, b = blockIdx.x;
+    const int t0 = b * kRouteTok, t1 = min(T, t0 + kRouteTok);
+    for (int e = lane; e < E; e += kWarp) s_cur[e] = offsets[e] + blk_cnt[static_cast<int64_t>(b) * E + e];
+    for (int i = lane; i < (t1 - t0) * topk; i += kWarp) s_sel[i] = sel_e[t0 * topk + i];
+    __syncwarp();
+    for (int t = t0; t < t1; ++t) {
+        if (lane < topk) {
+            const int e = s_sel[(t - t0) * topk + lane];
+            const int pos = s_cur[e];
+            s_cur[e] = pos + 1;
+            if (pos >= 0 && pos < P) {  // always, as both passes read the same selection; keeps writes in bounds
+                pair_token[pos] = t;
+                pair_slot[pos] = lane;
+                pair_weight[pos] = sel_w[t * topk + lane];
+            }
+        }
+        __syncwarp();
+    }
 }
 
 // Pair p's token row, 16 bytes per thread; and inv[(token, slot)] = p.
@@ -138,8 +248,16 @@ cudaError_t launch_moe_prefill_layer(const float* logits, const uint8_t* gu_code
 {
     const int P = T * topk;
     const PrefillWs w = carve(ws, T, topk, H, I, E, nullptr);
-    cudaError_t e = launch_moe_route(logits, T, E, topk, w.offsets, w.pair_token, w.pair_weight, w.pair_slot, s);
+    const int nb = route_blocks(T);
+    route_select_kernel<<<nb, kRouteThreads, static_cast<size_t>(E) * 4, s>>>(logits, T, E, topk, w.sel_e, w.sel_w,
+                                                                             w.blk_cnt);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    route_scan_kernel<<<1, kScanThreads, 0, s>>>(w.blk_cnt, nb, E, P, w.offsets);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    route_place_kernel<<<nb, kWarp, (static_cast<size_t>(E) + kRouteTok * topk) * 4, s>>>(
+        w.sel_e, w.sel_w, w.blk_cnt, w.offsets, T, E, topk, P, w.pair_token, w.pair_weight, w.pair_slot);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     gather_kernel<<<grid_for(static_cast<int64_t>(P) * H / 8), 256, 0, s>>>(x, w.pair_token, w.pair_slot, w.xg,
                                                                             w.inv, P, H, T, topk);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -291,6 +291,31 @@ bqd_status q4_0_gemv_path(const uint8_t* codes, const uint16_t* d, const uint16_
                           int64_t K, int N, int path, cudaStream_t stream);
 
 /*
+ * fp8_b128_gemv -- y[n][m] = sum_k e4m3(c[m][k]) * s[m/128][k/128] * x[n][k]
+ * ("Vemloir/LumenLLM" README, Quantization bullet: FP8 E4M3 weights beside
+ * NVFP4; "avifenesh/memra" README, Loaders bullet: FP8 checkpoints
+ * quantised in blocks of 128, one scale per 128 x 128 tile).
+ *   codes  u8 [M][K]: E4M3 bytes (OCP 8-bit FP, E4M3FN; 0x7f and 0xff are
+ *          NaN and give NaN), row-major.
+ *   scales fp32 [ceil(M/128)][ceil(K/128)], row-major: the tile scale that
+ *          multiplies the E4M3 values (a checkpoint's "scale_inv").
+ *   x bf16 bits [N][K]; y fp32 [N][M]. K % 32 == 0, 1 <= N <= 16; M == 0 and
+ *   K == 0 behave as in nvfp4_gemv. codes, scales, x, y 16-byte aligned.
+ *   AUTO: BQD_PATH_DIRECT for N == 1 and the K it takes (K a multiple of
+ *   1024 with K / 1024 in {1, 2, 3, 4, 6, 8, 12, 16}), else
+ *   BQD_PATH_CUDA_CORE. Products are exact (E4M3 values are f16 values, the
+ *   activations f16 after an exact per-call power-of-two prescale, or fp32
+ *   FMAs outside that range); the sums and the scale multiply are fp32.
+ */
+bqd_status fp8_b128_gemv(const uint8_t* codes, const float* scales, const uint16_t* x, float* y, int64_t M,
+                         int64_t K, int N, cudaStream_t stream);
+
+/* fp8_b128_gemv with an explicit compute path: BQD_PATH_AUTO, BQD_PATH_DIRECT
+ * or BQD_PATH_CUDA_CORE (others: BQD_ERR_PATH). */
+bqd_status fp8_b128_gemv_path(const uint8_t* codes, const float* scales, const uint16_t* x, float* y, int64_t M,
+                              int64_t K, int N, int path, cudaStream_t stream);
+
+/*
  * nvfp4_gemm -- Y[t][m] = ts * sum_k e2m1(c[m][k]) * e4m3(s[m][k/16]) * x[t][k]
  * for many tokens (prefill) on the tensor cores ("Vemloir/LumenLLM" README,
  * Kernels bullet: NVFP4 grouped-MoE prefill, a per-expert variable-grid
@@ -352,6 +377,12 @@ bqd_status moe_prefill_layer(const float* logits, const uint8_t* gu_codes, const
  * fp32); layout and shape rules as q4_0_gemv. */
 bqd_status q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* w, int64_t M, int64_t K,
                         cudaStream_t stream);
+
+/* fp8_b128_dequant -- w[m][k] = e4m3(c[m][k]) * s[m/128][k/128] in fp32 (the
+ * exact product rounded once to nearest); layout and shape rules as
+ * fp8_b128_gemv. */
+bqd_status fp8_b128_dequant(const uint8_t* codes, const float* scales, float* w, int64_t M, int64_t K,
+                            cudaStream_t stream);
 
 /*
  * moe_route_topk -- router and expert-major list of a top-k routed MoE layer

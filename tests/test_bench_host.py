@@ -71,7 +71,7 @@ def test_traffic_record_lookup():
             assert ent["algorithmic_bytes"] == bench.q8_0_bytes(p["M"], p["K"], p["N"])
         elif kind in ("nvfp4", "nvfp4_tiny"):
             assert ent["algorithmic_bytes"] == bench.nvfp4_bytes(p["M"], p["K"], p["N"])
-        if kind != "moe":  # every other row: the bench's own byte count of the row
+        if kind not in ("moe", "moe_prefill"):  # every other row: the bench's own byte count of the row
             assert ent["algorithmic_bytes"] == bench.row_bytes(kind, p, None)
         # per-call means, each rounded to a byte
         assert abs(ent["dram_bytes_per_launch"] - (ent["dram_read"] + ent["dram_write"])) <= 1
@@ -97,3 +97,35 @@ def test_moe_launch_count():
     # beyond the batched kernels' limits: route, gate_up, down, combine
     assert bench.moe_launches(32, 256, 2048, 512, 8) == 4
     assert bench.moe_launches(1, 256, 2048, 384, 8) == 4
+
+
+def test_write_traffic_splits_rows_at_the_separator(tmp_path, monkeypatch):
+    # a fake ncu CSV of --profile-all with two rows, two calls each: torch's
+    # setup kernels are dropped, each row's bytes are halved
+    rows = [("nvfp4 256x512 N=1", "nvfp4_tiny", dict(M=256, K=512, N=1)),
+            ("q8_0 32x64 N=2", "q8_0", dict(M=32, K=64, N=2))]
+    monkeypatch.setattr(bench, "rows_spec", lambda: rows[:1])
+    monkeypatch.setattr(bench, "extra_rows_spec", lambda: rows[1:])
+    hdr = ["ID", "Process ID", "Process Name", "Host Name", "Kernel Name", "Context", "Stream", "Block Size",
+           "Grid Size", "Device", "CC", "Section Name", "Metric Name", "Metric Unit", "Metric Value"]
+    launches = [("void at::native::fill", 5, 0), ("void bqd::nvfp4_dequant_kernel(int)", 7, 1),
+                ("void bqd::gemv_direct_kernel<A>(int)", 100, 4), ("void bqd::gemv_direct_kernel<A>(int)", 102, 6),
+                ("void bqd::nvfp4_dequant_kernel(int)", 7, 1), ("void at::native::copy", 9, 9),
+                ("void bqd::gemv_kernel<B>(int)", 1000, 0), ("void bqd::gemv_kernel<B>(int)", 1000, 0)]
+    lines = [",".join(f'"{c}"' for c in hdr)]
+    for i, (k, rd, wr) in enumerate(launches):
+        for m, v in (("dram__bytes_read.sum", rd), ("dram__bytes_write.sum", wr)):
+            lines.append(",".join(f'"{c}"' for c in [i, 1, "python", "h", k, 1, 7, "(1, 1, 1)", "(1, 1, 1)", 0,
+                                                    "10.3", "Command line profiler metrics", m, "byte", v]))
+    csv_path = tmp_path / "all.csv"
+    csv_path.write_text("\n".join(lines) + "\n")
+    out = tmp_path / "traffic.json"
+    bench.write_traffic(str(csv_path), 2, out_path=str(out))
+    import json
+    rec = json.loads(out.read_text())
+    a, b = rec["nvfp4 256x512 N=1"], rec["q8_0 32x64 N=2"]
+    assert (a["dram_read"], a["dram_write"], a["launches_per_call"]) == (101, 5, 1)
+    assert (b["dram_read"], b["dram_write"], b["launches_per_call"]) == (1000, 0, 1)
+    assert a["algorithmic_bytes"] == bench.nvfp4_bytes(256, 512, 1)
+    assert b["algorithmic_bytes"] == bench.q8_0_bytes(32, 64, 2)
+    assert a["kernels"] == ["gemv_direct_kernel<A>"] and b["kernels"] == ["gemv_kernel<B>"]
