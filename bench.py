@@ -856,8 +856,8 @@ def write_traffic(csv_path, calls, out_path=None):
     for (row, kind, p), seg in zip(spec, segs):
         rd = sum(v["dram__bytes_read.sum"] for v in seg) / calls
         wr = sum(v["dram__bytes_write.sum"] for v in seg) / calls
-        kern = sorted({v["k"].split("(")[0].replace("void ", "").replace("(anonymous namespace)::", "")
-                       .replace("unnamed>::", "").replace("bqd::", "") for v in seg})
+        kern = sorted({v["k"].split("(")[0].replace("void ", "").replace("bqd::", "").replace("<unnamed>::", "")
+                       .replace("(anonymous namespace)::", "") for v in seg})
         alg = row_bytes(kind, p, host_inputs(kind, p) if kind in ("moe", "moe_prefill") else None)
         src = traffic_sources(kind, p)
         out[row] = {"source_sha": source_sha(src), "sources": src, "kernels": kern,

@@ -60,10 +60,11 @@ constexpr int kGThreads = (2 + kGDec) * kWarp;
 constexpr int kALoads = 8;                  // stages of a row's codes in flight per decoder thread
 constexpr int kAHalf = kGH * kGK * 2;       // 16 KiB of bf16
 constexpr int kAStage = 2 * kAHalf;
-// BN tokens per tile (the MMA's N): 256 for one weight matrix, 128 for the
-// experts' token segments of a grouped call (an expert of a top-8 layer over
-// 256 experts sees ~64 of 2048 tokens, so its weights are read about once). B is BN x 64 k of bf16, and the two
-// halves' fp32 accumulators take 2 BN columns of tensor memory.
+// BN tokens per tile (the MMA's N): 256 for one weight matrix; 32, 64 or 128
+// for the experts' token segments of a grouped call, by the mean tokens per
+// expert (an expert of a top-8 layer over 256 experts sees ~32 of 1024
+// tokens). B is BN x 64 k of bf16, and the two halves' fp32 accumulators
+// take 2 BN columns of tensor memory (a power of two, at least 32).
 // The ring has as many stages as fit in shared memory, at most kGSMax.
 template <int BN>
 struct GemmShape {
@@ -479,15 +480,33 @@ cudaError_t launch_nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float
     return launch_gemm<256>(codes, scales, ts, nullptr, nullptr, 1, x, y, M, K, T, (T + 255) / 256, 0, K, s);
 }
 
+// Token-tile width of the grouped form from the mean tokens per expert: a
+// tile's MMAs cost BN columns however few of its tokens are real, and an
+// expert with more tokens than BN has its weights decoded once per tile,
+// which costs more. Measured on 256 experts of 1024 x 2048 (GB300, µs per
+// call for BN = 32 / 64 / 128): mean 16: 211 / 220 / 238; 32: 311 / 237 /
+// 254; 48: 428 / 243 / 260; 64: 516 / 336 / 265; 128: 904 / 553 / 377.
+static int grouped_tile_tokens(int64_t P, int64_t E)
+{
+    const int64_t mean = (P + E - 1) / E;
+    return mean <= 16 ? 32 : (mean <= 48 ? 64 : 128);
+}
+
 cudaError_t launch_nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scales, const float* ts,
                                       const int32_t* offsets, int E, const uint16_t* x, float* y, int64_t M,
                                       int64_t K, int64_t P, cudaStream_t s, bool accumulate, int64_t weight_k)
 {
     if (weight_k <= 0) weight_k = K;
     if (weight_k % kGK != 0 || K % weight_k != 0) return cudaErrorInvalidValue;
-    // tile slots: sum over experts of ceil(n_e / 128) <= P / 128 + E
-    return launch_gemm<128>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 127) / 128 + E,
-                            accumulate ? 1 : 0, weight_k, s);
+    // tile slots: sum over experts of ceil(n_e / BN) <= P / BN + E
+    const int bn = grouped_tile_tokens(P, E);
+    const int acc = accumulate ? 1 : 0;
+    if (bn == 32)
+        return launch_gemm<32>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 31) / 32 + E, acc, weight_k, s);
+    if (bn == 64)
+        return launch_gemm<64>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 63) / 64 + E, acc, weight_k, s);
+    return launch_gemm<128>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 127) / 128 + E, acc, weight_k,
+                            s);
 }
 
 cudaError_t read_and_clear_gemm_error(unsigned int* out)

@@ -40,11 +40,18 @@ namespace {
 
 constexpr size_t al256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
 
-constexpr int kRouteTok = 32;        // tokens per routing block
 constexpr int kRouteThreads = 256;   // eight warps, a token each at a time
 constexpr int kScanThreads = 1024;   // >= the largest E
+constexpr int kScanBatch = 8;        // block counts loaded together by the scan
 
-int route_blocks(int T) { return (T + kRouteTok - 1) / kRouteTok; }
+// Tokens per routing block: 8 (a token per warp) up to 1024 tokens, then a
+// multiple of 8 that keeps the blocks at most 128 (64 at T = 8192).
+int route_block_tokens(int T)
+{
+    const int per = (T + 127) / 128;
+    return per <= 8 ? 8 : (per + 7) / 8 * 8;
+}
+int route_blocks(int T) { return (T + route_block_tokens(T) - 1) / route_block_tokens(T); }
 
 struct PrefillWs {
     int32_t *offsets, *pair_token, *pair_slot, *inv, *sel_e, *blk_cnt;
@@ -80,18 +87,18 @@ PrefillWs carve(void* base, int T, int topk, int H, int I, int E, size_t* total)
     return w;
 }
 
-// Routing, pass 1: block b's tokens [32 b, 32 b + 32), a warp per token:
+// Routing, pass 1: block b's tokens [tb b, tb b + tb), a warp per token:
 // slot s of token t goes to sel_e/sel_w[t * topk + s]; blk_cnt[b][e] counts
 // the block's pairs of expert e.
 __global__ void __launch_bounds__(kRouteThreads)
-    route_select_kernel(const float* __restrict__ logits, int T, int E, int topk, int32_t* __restrict__ sel_e,
-                        float* __restrict__ sel_w, int32_t* __restrict__ blk_cnt)
+    route_select_kernel(const float* __restrict__ logits, int T, int E, int topk, int tb,
+                        int32_t* __restrict__ sel_e, float* __restrict__ sel_w, int32_t* __restrict__ blk_cnt)
 {
     extern __shared__ int s_cnt[];  // [E]
     for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = 0;
     __syncthreads();
     const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
-    const int t0 = blockIdx.x * kRouteTok, t1 = min(T, t0 + kRouteTok);
+    const int t0 = blockIdx.x * tb, t1 = min(T, t0 + tb);
     for (int t = t0 + warp; t < t1; t += kRouteThreads / kWarp) {  // warp-uniform
         int e = 0;
         float w = 0.f;
@@ -116,10 +123,16 @@ __global__ void __launch_bounds__(kScanThreads)
     const int e = threadIdx.x, lane = e % kWarp, warp = e / kWarp;
     int tot = 0;
     if (e < E) {
-        for (int b = 0; b < nb; ++b) {
-            const int c = blk_cnt[static_cast<int64_t>(b) * E + e];
-            blk_cnt[static_cast<int64_t>(b) * E + e] = tot;
-            tot += c;
+        for (int b0 = 0; b0 < nb; b0 += kScanBatch) {  // the loads of a batch in flight together
+            int c[kScanBatch];
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j)
+                c[j] = b0 + j < nb ? blk_cnt[static_cast<int64_t>(b0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < kScanBatch; ++j) {
+                if (b0 + j < nb) blk_cnt[static_cast<int64_t>(b0 + j) * E + e] = tot;
+                tot += c[j];
+            }
         }
     }
     int incl = tot;
@@ -150,15 +163,19 @@ __global__ void __launch_bounds__(kScanThreads)
 __global__ void __launch_bounds__(kWarp)
     route_place_kernel(const int32_t* __restrict__ sel_e, const float* __restrict__ sel_w,
                        const int32_t* __restrict__ blk_cnt, const int32_t* __restrict__ offsets, int T, int E,
-                       int topk, int P, int32_t* __restrict__ pair_token, float* __restrict__ pair_weight,
+                       int topk, int tb, int P, int32_t* __restrict__ pair_token, float* __restrict__ pair_weight,
                        int32_t* __restrict__ pair_slot)
 {
-    extern __shared__ int s_cur[];  // [E] cursors, then the block's sel_e [kRouteTok * topk]
+    extern __shared__ int s_cur[];  // [E] cursors, then the block's sel_e and sel_w [tb * topk] each
     int* s_sel = s_cur + E;
+    float* s_w = reinterpret_cast<float*>(s_sel + tb * topk);
     const int lane = threadIdx.x, b = blockIdx.x;
-    const int t0 = b * kRouteTok, t1 = min(T, t0 + kRouteTok);
+    const int t0 = b * tb, t1 = min(T, t0 + tb);
     for (int e = lane; e < E; e += kWarp) s_cur[e] = offsets[e] + blk_cnt[static_cast<int64_t>(b) * E + e];
-    for (int i = lane; i < (t1 - t0) * topk; i += kWarp) s_sel[i] = sel_e[t0 * topk + i];
+    for (int i = lane; i < (t1 - t0) * topk; i += kWarp) {
+        s_sel[i] = sel_e[t0 * topk + i];
+        s_w[i] = sel_w[t0 * topk + i];
+    }
     __syncwarp();
     for (int t = t0; t < t1; ++t) {
         if (lane < topk) {
@@ -168,7 +185,7 @@ __global__ void __launch_bounds__(kWarp)
             if (pos >= 0 && pos < P) {  // always, as both passes read the same selection; keeps writes in bounds
                 pair_token[pos] = t;
                 pair_slot[pos] = lane;
-                pair_weight[pos] = sel_w[t * topk + lane];
+                pair_weight[pos] = s_w[(t - t0) * topk + lane];
             }
         }
         __syncwarp();
@@ -248,15 +265,15 @@ cudaError_t launch_moe_prefill_layer(const float* logits, const uint8_t* gu_code
 {
     const int P = T * topk;
     const PrefillWs w = carve(ws, T, topk, H, I, E, nullptr);
-    const int nb = route_blocks(T);
-    route_select_kernel<<<nb, kRouteThreads, static_cast<size_t>(E) * 4, s>>>(logits, T, E, topk, w.sel_e, w.sel_w,
-                                                                             w.blk_cnt);
+    const int tb = route_block_tokens(T), nb = route_blocks(T);
+    route_select_kernel<<<nb, kRouteThreads, static_cast<size_t>(E) * 4, s>>>(logits, T, E, topk, tb, w.sel_e,
+                                                                             w.sel_w, w.blk_cnt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     route_scan_kernel<<<1, kScanThreads, 0, s>>>(w.blk_cnt, nb, E, P, w.offsets);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    route_place_kernel<<<nb, kWarp, (static_cast<size_t>(E) + kRouteTok * topk) * 4, s>>>(
-        w.sel_e, w.sel_w, w.blk_cnt, w.offsets, T, E, topk, P, w.pair_token, w.pair_weight, w.pair_slot);
+    route_place_kernel<<<nb, kWarp, (static_cast<size_t>(E) + 2 * static_cast<size_t>(tb) * topk) * 4, s>>>(
+        w.sel_e, w.sel_w, w.blk_cnt, w.offsets, T, E, topk, tb, P, w.pair_token, w.pair_weight, w.pair_slot);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     gather_kernel<<<grid_for(static_cast<int64_t>(P) * H / 8), 256, 0, s>>>(x, w.pair_token, w.pair_slot, w.xg,
                                                                             w.inv, P, H, T, topk);

@@ -343,7 +343,9 @@ bqd_status nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float tensor_
  *   offsets[E] = P; y fp32 [P][M]. K % 64 == 0, E >= 1; M == 0 or P == 0:
  *   BQD_OK without touching the GPU; K == 0: y set to zero. codes, scales,
  *   x, y 16-byte aligned; tensor_scales and expert_offsets 4-byte aligned.
- *   One launch: tiles of 256 weight rows x 128 of an expert's tokens. Offsets
+ *   One launch: tiles of 256 weight rows x BN of an expert's tokens, BN =
+ *   32, 64 or 128 for a mean of at most 16, at most 48, or more tokens per
+ *   expert (P / E rounded up). Offsets
  *   outside [0, P] are clamped (no access leaves the arrays; the outputs of
  *   such a call are unspecified).
  */

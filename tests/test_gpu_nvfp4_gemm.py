@@ -98,7 +98,11 @@ def run_grouped(codes, scales, ts, offsets, x, E, M, K, P):
     return out.get().reshape(P, M)
 
 
+# mean tokens per expert 14, 30, 66 and above 100: token tiles of 32, 64,
+# 128 and 128, experts of one or several tiles each
 @pytest.mark.parametrize("E,M,K,counts", [
+    (8, 384, 1024, [0, 1, 15, 16, 17, 40, 3, 20]),
+    (8, 384, 1024, [0, 1, 31, 32, 33, 100, 3, 40]),
     (8, 384, 1024, [0, 1, 63, 64, 65, 200, 3, 130]),
     (3, 256, 64, [17, 0, 300]),
     (1, 100, 512, [129]),
