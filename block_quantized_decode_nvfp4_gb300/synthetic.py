@@ -37,6 +37,7 @@ __all__ = [
     "nvfp4_weight",
     "q8_0_weight",
     "q4_0_weight",
+    "q4_1_weight",
     "fp8_b128_weight",
     "bf16_normal",
     "router_logits",
@@ -44,6 +45,7 @@ __all__ = [
     "dense_nvfp4",
     "dense_q8_0",
     "dense_q4_0",
+    "dense_q4_1",
     "dense_fp8_b128",
     "moe_layer",
     "NVFP4_SHAPES",
@@ -109,6 +111,19 @@ def q4_0_weight(M: int, K: int, rng_c, rng_d) -> dict:
     return {"codes": codes, "d": d, "M": M, "K": K}
 
 
+def q4_1_weight(M: int, K: int, rng_c, rng_d) -> dict:
+    """Q4_1 planes: codes u8[M][K/2] (the Q4_0 block order, uniform over all
+    bytes), dm fp16 bits u16[M][K/32][2]: d uniform in [1e-3, 1e-1], m
+    uniform in [-1, 1] (a block's minimum, as encoders store it)."""
+    if K % 32:
+        raise ValueError("Q4_1 needs K % 32 == 0")
+    codes = rng_c.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    d = rng_d.uniform(1e-3, 1e-1, size=(M, K // 32))
+    m = rng_d.uniform(-1.0, 1.0, size=(M, K // 32))
+    dm = np.stack([d, m], axis=-1).astype(np.float16).view(np.uint16)
+    return {"codes": codes, "dm": np.ascontiguousarray(dm), "M": M, "K": K}
+
+
 def fp8_b128_weight(M: int, K: int, rng_c, rng_s) -> dict:
     """FP8 block-128 planes: codes u8[M][K] (E4M3 bytes, row-major), scales
     f32[ceil(M/128)][ceil(K/128)]."""
@@ -160,6 +175,14 @@ def dense_q4_0(M: int, K: int, N: int = 1, seed: int = 0) -> dict:
     """Q4_0 weight with N bf16 columns. Streams: 0 codes, 1 d, 2 x."""
     rc, rd, rx = streams(seed, 3)
     w = q4_0_weight(M, K, rc, rd)
+    w["x"] = bf16_normal((N, K), rx)
+    return w
+
+
+def dense_q4_1(M: int, K: int, N: int = 1, seed: int = 0) -> dict:
+    """Q4_1 weight with N bf16 columns. Streams: 0 codes, 1 dm, 2 x."""
+    rc, rd, rx = streams(seed, 3)
+    w = q4_1_weight(M, K, rc, rd)
     w["x"] = bf16_normal((N, K), rx)
     return w
 

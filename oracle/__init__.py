@@ -40,6 +40,9 @@ def lib():
             ("oracle_q4_0_dequant_f64", None, [u8p, u16p, i64, i64, f64p]),
             ("oracle_q4_0_dequant_f32", None, [u8p, u16p, i64, i64, f32p]),
             ("oracle_q4_0_gemv", None, [u8p, u16p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
+            ("oracle_q4_1_dequant_f64", None, [u8p, u16p, i64, i64, f64p]),
+            ("oracle_q4_1_dequant_f32", None, [u8p, u16p, i64, i64, f32p]),
+            ("oracle_q4_1_gemv", None, [u8p, u16p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
             ("oracle_fp8_b128_dequant_f64", None, [u8p, f32p, i64, i64, f64p]),
             ("oracle_fp8_b128_dequant_f32", None, [u8p, f32p, i64, i64, f32p]),
             ("oracle_fp8_b128_gemv", None, [u8p, f32p, u16p, i64, i64, i64, i64p, i64, f64p, f64p]),
@@ -116,6 +119,18 @@ def q4_0_dequant(codes, d, M, K, dtype=np.float64):
     return w
 
 
+def q4_1_dequant(codes, dm, M, K, dtype=np.float64):
+    """Q4_1 weight [M][K]: fp16(d) * q + fp16(m) per 32-block, q in the
+    Q4_0 block order, dm [M][K/32][2] = the block's (d, m) fp16 bits."""
+    codes, dm = _c(codes, np.uint8), _c(dm, np.uint16)
+    w = np.empty((M, K), dtype=dtype)
+    if dtype == np.float64:
+        lib().oracle_q4_1_dequant_f64(_p(codes, C.c_uint8), _p(dm, C.c_uint16), M, K, _p(w, C.c_double))
+    else:
+        lib().oracle_q4_1_dequant_f32(_p(codes, C.c_uint8), _p(dm, C.c_uint16), M, K, _p(w, C.c_float))
+    return w
+
+
 def fp8_b128_dequant(codes, scales, M, K, dtype=np.float64):
     """FP8 block-128 weight [M][K]: e4m3(code) * the fp32 scale of the
     128 x 128 tile holding the element (scales [ceil(M/128)][ceil(K/128)])."""
@@ -174,6 +189,19 @@ def q4_0_gemv(codes, d, x, M, K, rows=None):
     R = M if r is None else len(r)
     y = np.empty((N, R)); a = np.empty((N, R))
     lib().oracle_q4_0_gemv(_p(codes, C.c_uint8), _p(d, C.c_uint16), _p(x, C.c_uint16), M, K, N,
+                           _p(r, C.c_int64), 0 if r is None else len(r),
+                           _p(y, C.c_double), _p(a, C.c_double))
+    return y, a
+
+
+def q4_1_gemv(codes, dm, x, M, K, rows=None):
+    codes, dm = _c(codes, np.uint8), _c(dm, np.uint16)
+    x = _c(x, np.uint16).reshape(-1, K)
+    N = x.shape[0]
+    r = None if rows is None else _c(rows, np.int64)
+    R = M if r is None else len(r)
+    y = np.empty((N, R)); a = np.empty((N, R))
+    lib().oracle_q4_1_gemv(_p(codes, C.c_uint8), _p(dm, C.c_uint16), _p(x, C.c_uint16), M, K, N,
                            _p(r, C.c_int64), 0 if r is None else len(r),
                            _p(y, C.c_double), _p(a, C.c_double))
     return y, a

@@ -151,6 +151,17 @@ static double q4_0_elem(const uint8_t *codes, const uint16_t *d, int64_t K, int6
     return oracle_fp16(d[m * (K / 32) + k / 32]) * (double)(q4_0_code(codes, K, m, k) - 8);
 }
 
+/* Q4_1 element (m, k): fp16(d) * q + fp16(m) of the element's 32-block, q
+ * its 4-bit code in the Q4_0 block order (low nibbles of the block's 16
+ * bytes are elements 0..15, the high nibbles elements 16..31); d and m are
+ * the block's two fp16 fields, stored side by side: dm[m][k/32] = (d, m).
+ * Exact in fp64 (at most 44 bits between the two terms' extreme bits). */
+static double q4_1_elem(const uint8_t *codes, const uint16_t *dm, int64_t K, int64_t m, int64_t k)
+{
+    const uint16_t *f = dm + (m * (K / 32) + k / 32) * 2;
+    return oracle_fp16(f[0]) * (double)q4_0_code(codes, K, m, k) + oracle_fp16(f[1]);
+}
+
 /* FP8 block-128 element (m, k): e4m3(code[m][k]) * scale of the 128 x 128
  * tile holding (m, k); scales are fp32 [ceil(M/128)][ceil(K/128)] row-major,
  * so rows 0..127 share scale row 0 and k 0..127 scale column 0. */
@@ -209,6 +220,21 @@ void oracle_q4_0_dequant_f32(const uint8_t *codes, const uint16_t *d, int64_t M,
     for (int64_t m = 0; m < M; ++m)
         for (int64_t k = 0; k < K; ++k)
             w[m * K + k] = (float)q4_0_elem(codes, d, K, m, k);
+}
+
+/* Q4_1 dequantised weight, fp64 (exact) and fp32 (rounded once). */
+void oracle_q4_1_dequant_f64(const uint8_t *codes, const uint16_t *dm, int64_t M, int64_t K, double *w)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            w[m * K + k] = q4_1_elem(codes, dm, K, m, k);
+}
+
+void oracle_q4_1_dequant_f32(const uint8_t *codes, const uint16_t *dm, int64_t M, int64_t K, float *w)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            w[m * K + k] = (float)q4_1_elem(codes, dm, K, m, k);
 }
 
 /* FP8 block-128 dequantised weight: fp64 exact (4 + 24 significant bits);
@@ -289,6 +315,27 @@ void oracle_q4_0_gemv(const uint8_t *codes, const uint16_t *d, const uint16_t *x
             double sum = 0.0, abs_sum = 0.0;
             for (int64_t k = 0; k < K; ++k) {
                 double p = q4_0_elem(codes, d, K, m, k) * oracle_bf16(x[n * K + k]);
+                sum += p;
+                abs_sum += fabs(p);
+            }
+            y[n * R + i] = sum;
+            if (a)
+                a[n * R + i] = abs_sum;
+        }
+    }
+}
+
+void oracle_q4_1_gemv(const uint8_t *codes, const uint16_t *dm, const uint16_t *x,
+                      int64_t M, int64_t K, int64_t N,
+                      const int64_t *rows, int64_t nrows, double *y, double *a)
+{
+    int64_t R = rows ? nrows : M;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t i = 0; i < R; ++i) {
+            int64_t m = rows ? rows[i] : i;
+            double sum = 0.0, abs_sum = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = q4_1_elem(codes, dm, K, m, k) * oracle_bf16(x[n * K + k]);
                 sum += p;
                 abs_sum += fabs(p);
             }

@@ -69,3 +69,11 @@ def fp8_b128_weight_lib(codes, scales) -> np.ndarray:
     M, K = codes.shape
     s = np.repeat(np.repeat(np.asarray(scales, dtype=np.float32).astype(np.float64), 128, axis=0), 128, axis=1)
     return e4m3_lib(codes) * s[:M, :K]
+
+
+def q4_1_weight_lib(codes, dm) -> np.ndarray:
+    """Real-valued Q4_1 weight: numpy's fp16 decode of (d, m), codes unpacked
+    in the Q4_0 block order."""
+    f = fp16_lib(dm)  # [M][K/32][2]
+    return (q4_0_codes_unpacked(codes).astype(np.float64) * np.repeat(f[..., 0], 32, axis=1)
+            + np.repeat(f[..., 1], 32, axis=1))

@@ -129,3 +129,19 @@ def test_write_traffic_splits_rows_at_the_separator(tmp_path, monkeypatch):
     assert a["algorithmic_bytes"] == bench.nvfp4_bytes(256, 512, 1)
     assert b["algorithmic_bytes"] == bench.q8_0_bytes(32, 64, 2)
     assert a["kernels"] == ["gemv_direct_kernel<A>"] and b["kernels"] == ["gemv_kernel<B>"]
+
+
+def test_traffic_record_sources_match_the_rows():
+    # every record names the kernel sources its row runs (the files exist),
+    # so that a change to any of them retires the record
+    import json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    rows = {n: (k, p) for n, k, p in bench.rows_spec() + bench.extra_rows_spec()}
+    csrc = os.path.join(ROOT, "block_quantized_decode_nvfp4_gb300", "csrc")
+    for name, ent in rec.items():
+        kind, p = rows[name]
+        assert ent["sources"] == bench.traffic_sources(kind, p), name
+        assert all(os.path.exists(os.path.join(csrc, f)) for f in ent["sources"]), name
+    assert bench.traffic_sources("fp8_b128", dict(M=4096, K=12288, N=1)) == bench.TRAFFIC_SOURCES["direct"]
+    assert bench.traffic_sources("moe_prefill", dict(T=1024))[0] == "moe_prefill.cu"
