@@ -54,6 +54,8 @@ SIGNATURES = {
     "q4_0_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "q4_0_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "q4_0_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
+    "q4_1_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
+    "q4_1_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
     "fp8_b128_gemv": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]),
     "fp8_b128_gemv_path": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _i32, _vp]),
     "fp8_b128_dequant": (_i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
@@ -232,6 +234,15 @@ def q4_0_gemv_path(codes, d, x, y, M, K, N, path, stream=None):
 
 def q4_0_dequant(codes, d, w, M, K, stream=None):
     _check(lib().q4_0_dequant(_ptr(codes), _ptr(d), _ptr(w), M, K, _stream(stream)), "q4_0_dequant")
+
+
+def q4_1_gemv(codes, dm, x, y, M, K, N, stream=None):
+    """Q4_1 GEMV: codes [M][K/2] (Q4_0 nibble order), dm [M][K/32][2] fp16 (d, m)."""
+    _check(lib().q4_1_gemv(_ptr(codes), _ptr(dm), _ptr(x), _ptr(y), M, K, N, _stream(stream)), "q4_1_gemv")
+
+
+def q4_1_dequant(codes, dm, w, M, K, stream=None):
+    _check(lib().q4_1_dequant(_ptr(codes), _ptr(dm), _ptr(w), M, K, _stream(stream)), "q4_1_dequant")
 
 
 def fp8_b128_gemv(codes, scales, x, y, M, K, N, stream=None):

@@ -10,6 +10,7 @@
 #include "gemm.h"
 #include "gemv.h"
 #include "host_util.h"
+#include "q4_1.cuh"
 
 namespace {
 
@@ -184,6 +185,24 @@ bqd_status q4_0_gemv(const uint8_t* codes, const uint16_t* d, const uint16_t* x,
                      int N, cudaStream_t stream)
 {
     return q4_0_gemv_path(codes, d, x, y, M, K, N, BQD_PATH_AUTO, stream);
+}
+
+bqd_status q4_1_gemv(const uint8_t* codes, const uint16_t* dm, const uint16_t* x, float* y, int64_t M, int64_t K,
+                     int N, cudaStream_t stream)
+{
+    bqd_status st = check_dense(codes, dm, x, y, M, K, N, 32, true);
+    if (st != BQD_OK || M == 0) return st;
+    if ((st = check_arch()) != BQD_OK) return st;
+    if (K == 0) return zero_output(y, M * N, stream);
+    return from_cuda(bqd::launch_q4_1_gemv_cuda_core(codes, dm, x, y, M, K, N, stream));
+}
+
+bqd_status q4_1_dequant(const uint8_t* codes, const uint16_t* dm, float* w, int64_t M, int64_t K, cudaStream_t stream)
+{
+    bqd_status st = check_dense(codes, dm, nullptr, w, M, K, 1, 32, false);
+    if (st != BQD_OK || M == 0 || K == 0) return st;
+    if ((st = check_arch()) != BQD_OK) return st;
+    return from_cuda(bqd::launch_q4_1_dequant(codes, dm, w, M, K, stream));
 }
 
 bqd_status fp8_b128_gemv_path(const uint8_t* codes, const float* scales, const uint16_t* x, float* y, int64_t M,

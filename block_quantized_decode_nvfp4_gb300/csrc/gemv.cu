@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "host_util.h"
+#include "q4_1.cuh"
 
 namespace bqd {
 
@@ -188,6 +189,25 @@ __global__ void q4_0_dequant_kernel(const uint8_t* __restrict__ codes, const uin
     }
 }
 
+// w[m][k] = fp16(d) * q + fp16(m) in fp32 (the exact value rounded once:
+// one fused multiply-add), q in the Q4_0 block order. One thread per code
+// byte (elements k0 and k0 + 16 of a block).
+__global__ void q4_1_dequant_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ dm,
+                                    float* __restrict__ w, int64_t M, int64_t K)
+{
+    const int64_t nbytes = M * (K / 2);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nbytes;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / (K / 2), bi = i - m * (K / 2);  // byte index within the row
+        const int64_t k0 = (bi / 16) * 32 + bi % 16;          // element of the low nibble
+        const uint16_t* f = dm + (m * (K / 32) + k0 / 32) * 2;
+        const float d = fp16_to_float(f[0]), mn = fp16_to_float(f[1]);
+        const int c = codes[i];
+        w[m * K + k0] = fmaf(d, static_cast<float>(c & 15), mn);
+        w[m * K + k0 + 16] = fmaf(d, static_cast<float>(c >> 4), mn);
+    }
+}
+
 // w[m][k] = e4m3(code) * the fp32 scale of the 128 x 128 tile holding
 // (m, k), in fp32: the E4M3 value is exact in fp32 and the one multiply
 // rounds the exact product once to nearest. One thread per pair of codes
@@ -288,6 +308,12 @@ cudaError_t launch_q4_0_gemv_cuda_core(const uint8_t* codes, const uint16_t* d, 
     return launch_gemv<Q4_0Fmt>(codes, reinterpret_cast<const uint8_t*>(d), 1.0f, x, y, M, K, N, s);
 }
 
+cudaError_t launch_q4_1_gemv_cuda_core(const uint8_t* codes, const uint16_t* dm, const uint16_t* x, float* y,
+                                       int64_t M, int64_t K, int N, cudaStream_t s)
+{
+    return launch_gemv<Q4_1Fmt>(codes, reinterpret_cast<const uint8_t*>(dm), 1.0f, x, y, M, K, N, s);
+}
+
 cudaError_t launch_fp8_b128_gemv_cuda_core(const uint8_t* codes, const float* scales, const uint16_t* x, float* y,
                                            int64_t M, int64_t K, int N, cudaStream_t s)
 {
@@ -319,6 +345,13 @@ cudaError_t launch_q4_0_dequant(const uint8_t* codes, const uint16_t* d, float* 
                                 cudaStream_t s)
 {
     q4_0_dequant_kernel<<<dequant_grid(M * K / 2), 256, 0, s>>>(codes, d, w, M, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_q4_1_dequant(const uint8_t* codes, const uint16_t* dm, float* w, int64_t M, int64_t K,
+                                cudaStream_t s)
+{
+    q4_1_dequant_kernel<<<dequant_grid(M * K / 2), 256, 0, s>>>(codes, dm, w, M, K);
     return cudaGetLastError();
 }
 

@@ -291,6 +291,29 @@ bqd_status q4_0_gemv_path(const uint8_t* codes, const uint16_t* d, const uint16_
                           int64_t K, int N, int path, cudaStream_t stream);
 
 /*
+ * q4_1_gemv -- y[n][m] = sum_k (fp16(d[m][k/32]) * q[m][k] + fp16(mn[m][k/32])) * x[n][k]
+ * ("robertbfuentes7-cloud/bw24" README, GGUF bullet: Q4_1 among the file
+ * formats).
+ *   codes u8 [M][K/2]: 16 bytes per 32-element block in the Q4_0 order
+ *         (byte j holds element j in its low and element j + 16 in its
+ *         high nibble), q in 0..15.
+ *   dm    fp16 bits [M][K/32][2]: each block's (d, mn), the two fp16 fields
+ *         of a GGUF Q4_1 block side by side, so a loader copies them byte
+ *         for byte.
+ *   x bf16 bits [N][K]; y fp32 [N][M]. K % 32 == 0, 1 <= N <= 16; M == 0 and
+ *   K == 0 behave as in nvfp4_gemv. codes, dm, x, y 16-byte aligned.
+ *   One path (the CUDA-core GEMV): per block, d * sum q x + mn * sum x, the
+ *   products q x exact in fp32, the sums fp32.
+ */
+bqd_status q4_1_gemv(const uint8_t* codes, const uint16_t* dm, const uint16_t* x, float* y, int64_t M, int64_t K,
+                     int N, cudaStream_t stream);
+
+/* q4_1_dequant -- w[m][k] = fp16(d) * q + fp16(mn) rounded once to fp32;
+ * layout and shape rules as q4_1_gemv. */
+bqd_status q4_1_dequant(const uint8_t* codes, const uint16_t* dm, float* w, int64_t M, int64_t K,
+                        cudaStream_t stream);
+
+/*
  * fp8_b128_gemv -- y[n][m] = sum_k e4m3(c[m][k]) * s[m/128][k/128] * x[n][k]
  * ("Vemloir/LumenLLM" README, Quantization bullet: FP8 E4M3 weights beside
  * NVFP4; "avifenesh/memra" README, Loaders bullet: FP8 checkpoints
