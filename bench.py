@@ -103,7 +103,7 @@ def extra_rows_spec():
     the decode-path epilogue fusions on the layer shapes (gate_up with
     SiLU * up on the 12288 x 4096 gate/up weight, I = 6144; down with the
     residual add on 4096 x 12288); the Q4_0 and FP8 block-128 GEMVs on the
-    two layer shapes;
+    two layer shapes and the Q4_1 GEMV (CUDA-core path) on 12288 x 4096;
     the tensor-core prefill GEMM of the 12288 x 4096 weight over 2048
     tokens and its grouped form over 256 experts (the MoE gate_up, 2I = 1024
     rows, H = 2048) for 2048 tokens routed top-8 (16384 pairs, multinomial
@@ -118,6 +118,7 @@ def extra_rows_spec():
             ("nvfp4 down+residual 4096x12288 N=1", "nvfp4_add", dict(M=4096, K=12288, N=1)),
             ("q4_0 12288x4096 N=1", "q4_0", dict(M=12288, K=4096, N=1)),
             ("q4_0 4096x12288 N=1", "q4_0", dict(M=4096, K=12288, N=1)),
+            ("q4_1 12288x4096 N=1", "q4_1", dict(M=12288, K=4096, N=1)),
             ("fp8_b128 12288x4096 N=1", "fp8_b128", dict(M=12288, K=4096, N=1)),
             ("fp8_b128 4096x12288 N=1", "fp8_b128", dict(M=4096, K=12288, N=1)),
             ("nvfp4 prefill GEMM 12288x4096 T=2048", "nvfp4_gemm", dict(M=12288, K=4096, N=2048)),
@@ -151,6 +152,8 @@ def host_inputs(kind, p, seed=0):
         return syn.dense_q8_0(p["M"], p["K"], N=p["N"], seed=seed)
     if kind == "q4_0":
         return syn.dense_q4_0(p["M"], p["K"], N=p["N"], seed=seed)
+    if kind == "q4_1":
+        return syn.dense_q4_1(p["M"], p["K"], N=p["N"], seed=seed)
     if kind == "fp8_b128":
         return syn.dense_fp8_b128(p["M"], p["K"], N=p["N"], seed=seed)
     return syn.moe_layer(T=p["T"], E=p["E"], H=p["H"], I=p["I"], topk=p["topk"], seed=seed)
@@ -173,6 +176,8 @@ def row_bytes(kind, p, host):
         return q8_0_bytes(p["M"], p["K"], p["N"])
     if kind == "q4_0":  # 16 code bytes and a 2-byte scale per 32 weights
         return p["M"] * p["K"] // 2 + p["M"] * (p["K"] // 32) * 2 + 2 * p["N"] * p["K"] + 4 * p["N"] * p["M"]
+    if kind == "q4_1":  # 16 code bytes and two 2-byte fields (d, m) per 32 weights
+        return p["M"] * p["K"] // 2 + p["M"] * (p["K"] // 32) * 4 + 2 * p["N"] * p["K"] + 4 * p["N"] * p["M"]
     if kind == "fp8_b128":  # a byte per weight, a 4-byte scale per 128 x 128 tile
         return (p["M"] * p["K"] + ((p["M"] + 127) // 128) * ((p["K"] + 127) // 128) * 4 + 2 * p["N"] * p["K"]
                 + 4 * p["N"] * p["M"])
@@ -332,12 +337,15 @@ class Row:
             self.x_host, self.x = host["x"], d(host["x"])
             self.y = torch.empty(p["N"] * p["M"], dtype=torch.float32, device="cuda")
             self.in_bytes = self.x.numel() * 2
-        elif kind in ("nvfp4", "q8_0", "q4_0", "fp8_b128", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add", "nvfp4_gemm"):
+        elif kind in ("nvfp4", "q8_0", "q4_0", "q4_1", "fp8_b128", "nvfp4_tiny", "nvfp4_silu", "nvfp4_add",
+                      "nvfp4_gemm"):
             M, K, N = p["M"], p["K"], p["N"]
             if kind == "q8_0":
                 self.w = (d(host["q"]), d(host["d"]))
             elif kind == "q4_0":
                 self.w = (d(host["codes"]), d(host["d"]))
+            elif kind == "q4_1":
+                self.w = (d(host["codes"]), d(host["dm"]))
             elif kind == "fp8_b128":
                 self.w = (d(host["codes"]), d(host["scales"]))
             else:
@@ -397,6 +405,8 @@ class Row:
             b.q8_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "q4_0":
             b.q4_0_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
+        elif self.kind == "q4_1":
+            b.q4_1_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "fp8_b128":
             b.fp8_b128_gemv(w[0], w[1], self.x, self.y, p["M"], p["K"], p["N"])
         elif self.kind == "nvfp4_gemm":
