@@ -145,3 +145,51 @@ def test_traffic_record_sources_match_the_rows():
         assert all(os.path.exists(os.path.join(csrc, f)) for f in ent["sources"]), name
     assert bench.traffic_sources("fp8_b128", dict(M=4096, K=12288, N=1)) == bench.TRAFFIC_SOURCES["direct"]
     assert bench.traffic_sources("moe_prefill", dict(T=1024))[0] == "moe_prefill.cu"
+
+
+# A small instance of every row kind and the library call its row makes.
+SMALL_ROWS = {
+    "nvfp4": (dict(M=32, K=64, N=1), "nvfp4_gemv"),
+    "nvfp4_tiny": (dict(M=256, K=512, N=1), "nvfp4_gemv"),
+    "nvfp4_silu": (dict(M=64, K=64, N=1), "nvfp4_gemv_silu_mul"),
+    "nvfp4_add": (dict(M=32, K=64, N=1), "nvfp4_gemv_add"),
+    "q8_0": (dict(M=32, K=64, N=2), "q8_0_gemv"),
+    "q4_0": (dict(M=32, K=64, N=1), "q4_0_gemv"),
+    "q4_1": (dict(M=32, K=64, N=1), "q4_1_gemv"),
+    "fp8_b128": (dict(M=130, K=256, N=1), "fp8_b128_gemv"),
+    "nvfp4_gemm": (dict(M=32, K=64, N=16), "nvfp4_gemm"),
+    "nvfp4_gemm_grouped": (dict(E=4, M=32, K=64, N=64), "nvfp4_gemm_grouped"),
+    "nvfp4_encode": (dict(M=32, K=64, N=1), "nvfp4_encode"),
+    "q8_0_encode": (dict(M=32, K=64, N=1), "q8_0_encode"),
+    "moe": (dict(T=2, E=8, H=64, I=64, topk=2), "moe_layer"),
+    "moe_prefill": (dict(T=4, E=8, H=64, I=64, topk=2), "moe_prefill_layer"),
+}
+
+
+def test_every_row_kind_builds_and_calls_its_entry_point(monkeypatch):
+    # Row construction and run() on the CPU: torch's cuda calls kept on the
+    # host, the library replaced by a recorder; the call it records must be
+    # an entry point of the package, and every row kind of the bench is here
+    import torch
+    import block_quantized_decode_nvfp4_gb300 as real
+    kinds = {k for _, k, _ in bench.rows_spec() + bench.extra_rows_spec()}
+    assert kinds <= set(SMALL_ROWS), kinds - set(SMALL_ROWS)
+    monkeypatch.setattr(torch.Tensor, "cuda", lambda self, *a, **k: self)
+    empty = torch.empty
+    monkeypatch.setattr(torch, "empty", lambda *a, **k: empty(*a, **{n: v for n, v in k.items() if n != "device"}))
+    calls = []
+
+    class Recorder:
+        def __getattr__(self, name):
+            def f(*a, **k):
+                calls.append(name)
+                return 4096 if name.endswith("workspace_bytes") else None
+            return f
+
+    for kind, (p, entry) in SMALL_ROWS.items():
+        row = bench.Row(f"small {kind}", kind, p, bench.host_inputs(kind, p), torch, Recorder())
+        calls.clear()
+        row.run()
+        assert calls == [entry], (kind, calls)
+        assert callable(getattr(real, entry)), entry
+        assert row.bytes > 0 and row.weight_bytes > 0 and row.out_bytes > 0
