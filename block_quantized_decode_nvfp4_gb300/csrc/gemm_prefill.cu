@@ -499,7 +499,11 @@ cudaError_t launch_nvfp4_gemm_grouped(const uint8_t* codes, const uint8_t* scale
     if (weight_k <= 0) weight_k = K;
     if (weight_k % kGK != 0 || K % weight_k != 0) return cudaErrorInvalidValue;
     // tile slots: sum over experts of ceil(n_e / BN) <= P / BN + E
-    const int bn = grouped_tile_tokens(P, E);
+    int bn = grouped_tile_tokens(P, E);
+    // the tile slots are the grid's y dimension (at most 65535, which
+    // gemm_grouped_supported guarantees for 128-token tiles): wider tiles
+    // where narrow ones would not fit
+    while (bn < 128 && (P + bn - 1) / bn + E > 65535) bn *= 2;
     const int acc = accumulate ? 1 : 0;
     if (bn == 32)
         return launch_gemm<32>(codes, scales, 1.0f, ts, offsets, E, x, y, M, K, P, (P + 31) / 32 + E, acc, weight_k, s);

@@ -368,7 +368,8 @@ bqd_status nvfp4_gemm(const uint8_t* codes, const uint8_t* scales, float tensor_
  *   x, y 16-byte aligned; tensor_scales and expert_offsets 4-byte aligned.
  *   One launch: tiles of 256 weight rows x BN of an expert's tokens, BN =
  *   32, 64 or 128 for a mean of at most 16, at most 48, or more tokens per
- *   expert (P / E rounded up). Offsets
+ *   expert (P / E rounded up), wider where the tile count would exceed the
+ *   grid's 65535 rows (P / 128 + E <= 65535 is required). Offsets
  *   outside [0, P] are clamped (no access leaves the arrays; the outputs of
  *   such a call are unspecified).
  */
