@@ -143,3 +143,76 @@ def test_moe_layer_validation(L):
     assert L.moe_layer(*a, A + 16, wsb, 256, 2048, 512, 1, 8, s) == 6               # workspace misaligned
     assert L.moe_layer(*a[:8], U, A, wsb, 256, 2048, 512, 1, 8, s) == 3             # misaligned y
     assert L.moe_layer_workspace_bytes(0, 8, 2048, 512, 256) == 0
+
+
+def test_format_entry_points_validation(L):
+    # Q4_0, Q4_1 and FP8 block-128: shape, NULL, alignment and path errors on
+    # the host, before any CUDA call
+    s, CORE, MMA, DIRECT = None, 1, 3, 4
+    for gemv in (L.q4_0_gemv, L.q4_1_gemv, L.fp8_b128_gemv):
+        assert gemv(A, A, A, A, 4, 48, 1, s) == 2                        # K % 32
+        assert gemv(A, A, A, A, 4, 64, 17, s) == 2                       # N > 16
+        assert gemv(A, None, A, A, 4, 64, 1, s) == 1                     # NULL scales
+        assert gemv(A, A, U, A, 4, 64, 1, s) == 3                        # misaligned x
+        assert gemv(None, None, None, None, 0, 64, 1, s) == 0            # M == 0
+    for path in (L.q4_0_gemv_path, L.fp8_b128_gemv_path):
+        assert path(A, A, A, A, 4, 1024, 1, MMA, s) == 7                 # no tensor-core path
+        assert path(A, A, A, A, 4, 96, 1, DIRECT, s) == 7                # K the direct kernel does not take
+        assert path(A, A, A, A, 4, 1024, 2, DIRECT, s) == 7              # direct is N = 1 only
+        assert path(A, A, A, A, 4, 48, 1, CORE, s) == 2                  # argument errors first
+    for deq in (L.q4_0_dequant, L.q4_1_dequant, L.fp8_b128_dequant):
+        assert deq(A, A, U, 4, 32, s) == 3
+        assert deq(A, A, None, 4, 32, s) == 1
+        assert deq(A, A, A, 4, 48, s) == 2
+        assert deq(None, None, None, 0, 32, s) == 0
+
+
+def test_fusion_and_encoder_validation(L):
+    s = None
+    assert L.nvfp4_gemv_add(A, A, 1.0, A, A, A, 4, 1536, 1, s) == 2     # K the direct kernel does not take
+    assert L.nvfp4_gemv_add(A, A, 1.0, A, A, A, 4, 1024, 2, s) == 2     # N = 1 only
+    assert L.nvfp4_gemv_add(A, A, 1.0, A, None, A, 4, 1024, 1, s) == 1  # no residual
+    assert L.nvfp4_gemv_add(A, A, 1.0, A, U, A, 4, 1024, 1, s) == 3     # misaligned residual
+    assert L.q8_0_gemv_add(A, A, A, A, A, 4, 1000, 1, s) == 2           # K % 32
+    assert L.nvfp4_gemv_silu_mul(A, A, 1.0, A, A, 0, 1024, 1, s) == 2   # I = 0
+    assert L.q8_0_gemv_silu_mul(A, A, A, A, 8, 1536, 1, s) == 2
+    assert L.nvfp4_encode(A, 1.0, A, A, 4, 24, s) == 2                  # K % 16
+    assert L.nvfp4_encode(A, float("nan"), A, A, 4, 32, s) == 2         # tensor scale NaN
+    assert L.nvfp4_encode(A, 0.0, A, A, 4, 32, s) == 2                  # tensor scale 0
+    assert L.nvfp4_encode(A, 1.0, None, A, 4, 32, s) == 1
+    assert L.nvfp4_encode(U, 1.0, A, A, 4, 32, s) == 3
+    assert L.nvfp4_encode(None, 1.0, None, None, 0, 32, s) == 0
+    assert L.q8_0_encode(A, A, A, 4, 48, s) == 2
+    assert L.q8_0_encode(A, A, A + 1, 4, 64, s) == 3                    # odd fp16 plane
+
+
+def test_prefill_entry_points_validation(L):
+    s = None
+    assert L.nvfp4_gemm(A, A, 1.0, A, A, 4, 32, 8, s) == 2              # K % 64
+    assert L.nvfp4_gemm(A, A, 1.0, A, A, -1, 64, 8, s) == 2
+    assert L.nvfp4_gemm(A, A, 1.0, A, None, 4, 64, 8, s) == 1           # NULL y
+    assert L.nvfp4_gemm(A, A, 1.0, A, U, 4, 64, 8, s) == 3
+    assert L.nvfp4_gemm(None, None, 1.0, None, None, 4, 64, 0, s) == 0  # T == 0
+    g = L.nvfp4_gemm_grouped
+    assert g(A, A, A, A, A, A, 0, 32, 64, 8, s) == 2                    # E < 1
+    assert g(A, A, A, A, A, A, 2, 32, 96, 8, s) == 2                    # K % 64
+    assert g(A, A, A, A, A, None, 2, 32, 64, 8, s) == 1
+    assert g(A, A, A, A, A, U, 2, 32, 64, 8, s) == 3
+    assert g(None, None, None, None, None, None, 2, 0, 64, 8, s) == 0   # M == 0
+    wsb = L.moe_prefill_workspace_bytes(1024, 8, 2048, 512, 256)
+    assert wsb >= 8192 * (6 * 2048 + 12 * 512)
+    assert L.moe_prefill_workspace_bytes(0, 8, 2048, 512, 256) == 0
+    a = [A] * 9
+    lay = L.moe_prefill_layer
+    assert lay(*a, A, wsb, 256, 2048, 512, 1025, 8, s) == 2             # T * topk > 8192
+    assert lay(*a, A, wsb, 256, 2000, 512, 16, 8, s) == 2               # H % 64
+    assert lay(*a, A, wsb, 256, 2048, 32, 16, 8, s) == 2                # I < 64
+    assert lay(*a, A, wsb, 2048, 2048, 512, 16, 8, s) == 2              # E > 1024
+    assert lay(*a, A, wsb, 4, 2048, 512, 16, 8, s) == 2                 # topk > E
+    assert lay(None, *a[1:], A, wsb, 256, 2048, 512, 16, 8, s) == 1     # NULL logits
+    small = L.moe_prefill_workspace_bytes(16, 8, 2048, 512, 256)
+    assert lay(*a, A, small - 1, 256, 2048, 512, 16, 8, s) == 6         # workspace too small
+    assert lay(*a, A + 8, small, 256, 2048, 512, 16, 8, s) == 3         # misaligned workspace
+    bad = list(a)
+    bad[3] = A + 2                                                      # gate/up tensor scales not 4-byte aligned
+    assert lay(*bad, A, small, 256, 2048, 512, 16, 8, s) == 3
