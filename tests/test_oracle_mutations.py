@@ -6,10 +6,12 @@ import os
 import shutil
 import subprocess
 
+import numpy as np
 import pytest
 
 import oracle
 from oracle import build as obuild
+from tests import test_oracle_encoders as t_enc
 from tests import test_oracle_fp8_b128 as t_fp8
 from tests import test_oracle_gemv as t_gemv
 from tests import test_oracle_moe as t_moe
@@ -45,6 +47,15 @@ MUTANTS = [
      "(double)(q4_0_code(codes, K, m, k) - 8)",
      "(double)(q4_0_code(codes, K, m, k) - 7)",
      [lambda: t_q40.test_q4_0_worked_example(read_golden)]),
+    ("routing ties to the higher expert index",
+     "if (best < 0 || l[e] > l[best])",
+     "if (best < 0 || l[e] >= l[best])",
+     [lambda: t_moe.test_route_ties_and_full_selection()]),
+    ("routing weights not renormalised over the selected experts",
+     "sel_weight[t * topk + s] /= psum;",
+     "sel_weight[t * topk + s] /= 1.0;",
+     [lambda: t_moe.test_route_worked_example(read_golden),
+      lambda: t_moe.test_route_matches_library_softmax()]),
     ("SiLU with the wrong sign in the exponent",
      "h[i] = sg / (1.0 + exp(-sg)) * su;",
      "h[i] = sg / (1.0 + exp(sg)) * su;",
@@ -83,3 +94,26 @@ def test_real_oracle_passes_the_same_pins():
     for _, _, _, pins in MUTANTS:
         for pin in pins:
             pin()
+
+
+def test_encoder_pins_reject_ties_away_from_zero(monkeypatch):
+    # the encoders' grid rounding planted with ties to the larger value
+    # (away from zero) instead of ties to even
+    real = oracle._rn_grid
+
+    def ties_away(v, grid):
+        a = np.abs(np.asarray(v, dtype=np.float64))
+        g = np.asarray(grid, dtype=np.float64)
+        d = np.abs(a[..., None] - g)
+        cand = d == d.min(axis=-1, keepdims=True)
+        idx = len(g) - 1 - np.argmax(cand[..., ::-1], axis=-1)  # the highest index at the minimum distance
+        return np.where(a >= g[-1], len(g) - 1, idx)
+
+    monkeypatch.setattr(oracle, "_rn_grid", ties_away)
+    for pin in (t_enc.test_e4m3_encode_matches_torch_cast_in_range,
+                t_enc.test_e2m1_encode_grid_midpoints_saturation_and_sign):
+        with pytest.raises(AssertionError):
+            pin()
+    monkeypatch.setattr(oracle, "_rn_grid", real)
+    t_enc.test_e4m3_encode_matches_torch_cast_in_range()
+    t_enc.test_e2m1_encode_grid_midpoints_saturation_and_sign()
