@@ -11,6 +11,7 @@ import pytest
 
 import oracle
 from oracle import build as obuild
+from tests import test_oracle_decoders as t_dec
 from tests import test_oracle_encoders as t_enc
 from tests import test_oracle_fp8_b128 as t_fp8
 from tests import test_oracle_gemv as t_gemv
@@ -21,6 +22,31 @@ from tests.conftest import read_golden
 
 # (mistake, text in oracle.c, its replacement, pins that must catch it)
 MUTANTS = [
+    ("E2M1 subnormal read as m instead of 0.5 m",
+     "mag = 0.5 * m;",
+     "mag = 1.0 * m;",
+     [lambda: t_dec.test_e2m1_all_codes_match_ocp_table(read_golden)]),
+    ("fp16 exponent bias 14 instead of 15",
+     "mag = ldexp(1.0 + f / 1024.0, e - 15);",
+     "mag = ldexp(1.0 + f / 1024.0, e - 14);",
+     [lambda: t_dec.test_fp16_all_codes_match_numpy(),
+      lambda: t_q40.test_q4_0_worked_example(read_golden)]),
+    ("NVFP4 block scale per 32 k instead of 16",
+     "scales[m * (K / 16) + k / 16]",
+     "scales[m * (K / 16) + k / 32]",
+     [lambda: t_gemv.test_nvfp4_worked_example(read_golden),
+      lambda: t_gemv.test_nvfp4_dequant_matches_library_decoders()]),
+    ("GEMV magnitude sum without the absolute value",
+     "abs_sum += fabs(p);",
+     "abs_sum += p;",
+     [lambda: t_q40.test_q4_0_worked_example(read_golden),
+      lambda: t_fp8.test_fp8_b128_worked_example(read_golden)]),
+    ("MoE gate and up halves swapped",
+     "double pg = nvfp4_elem(gc, gs, H, i, k) * (double)gu_ts[e] * xv;\n"
+     "                    double pu = nvfp4_elem(gc, gs, H, I + i, k) * (double)gu_ts[e] * xv;",
+     "double pg = nvfp4_elem(gc, gs, H, I + i, k) * (double)gu_ts[e] * xv;\n"
+     "                    double pu = nvfp4_elem(gc, gs, H, i, k) * (double)gu_ts[e] * xv;",
+     [lambda: t_moe.test_moe_layer_matches_library_bruteforce(3, 4)]),
     ("NVFP4 nibble order swapped",
      "(k % 2 == 0) ? (uint8_t)(byte & 0x0F) : (uint8_t)(byte >> 4)",
      "(k % 2 == 0) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0x0F)",
