@@ -73,6 +73,12 @@ struct GemmShape {
                                                                               : kGSMax;
     static constexpr int kSmem = kStages * (kAStage + kBStage) + 1024;  // + alignment slack
     static constexpr int kTmemCols = 2 * BN;
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "an M = 128 MMA takes N = 16 .. 256 in steps of 16");
+    static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+                  "tensor memory is allocated in powers of two from 32 to 512 columns");
+    static_assert(kStages >= 2, "the ring needs two stages to overlap loads with MMAs");
+    static_assert(kSmem <= 227 * 1024, "dynamic shared memory of one CTA");
+    static_assert(kBStage % 1024 == 0, "B stages start on 1024-byte boundaries (128-byte swizzle atoms)");
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
