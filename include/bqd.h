@@ -1,8 +1,10 @@
 /*
  * bqd.h -- C ABI of libbqd.so, the GB300 (sm_103a) block-quantized decode
- * matvec library: y = W . x with NVFP4 or Q8_0 weights, for N = 1 token
- * (plain decode) up to N = 16 (speculative verify), and a top-k routed MoE
- * layer whose experts are NVFP4.
+ * matvec library: y = W . x with NVFP4 or Q8_0 weights (also Q4_0, Q4_1 and
+ * FP8 block-128), for N = 1 token (plain decode) up to N = 16 (speculative
+ * verify), and a top-k routed MoE layer whose experts are NVFP4; around
+ * them, decode-path epilogue fusions, bf16 -> NVFP4 / Q8_0 encoders, and
+ * NVFP4 prefill GEMMs on the tensor cores with a MoE prefill layer.
  *
  * Sources (what each call computes):
  *  - "Vemloir/LumenLLM" README, Quantization and Kernels bullets: weights in
@@ -13,7 +15,11 @@
  *    draft tokens in one batched target forward (a matvec with N = K+1
  *    columns); MoE batches routed tokens expert-major and decodes each
  *    selected expert's weights once.
- *  - "avifenesh/memra" README, Decode kernels bullet: NVFP4 and Q8_0 matvecs.
+ *  - "avifenesh/memra" README, Decode kernels bullet: NVFP4, Q4_0 and Q8_0
+ *    matvecs; Loaders bullet: FP8 checkpoints quantised in blocks of 128.
+ *  - "robertbfuentes7-cloud/bw24" README, GGUF bullet: Q4_0 and Q4_1 among
+ *    the file formats; safetensors loader bullet: large tensors re-encoded
+ *    to Q8_0 / NVFP4 at load.
  * The pages do not print the formats' bit layouts. Elements follow the
  * public closed forms (E2M1 per OCP MX v1.0, E4M3 per OCP OFP8 v1.0, fp16
  * per IEEE 754 binary16, bf16 = upper half of binary32); the block structure
